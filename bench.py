@@ -1,0 +1,366 @@
+"""Benchmark: ICP registration of the 100k <-> 100k synthetic scene on GB300.
+
+One step = one full registration of the resident source against the resident
+target tree (Morton ordering of the source, every fused correspondence pass,
+every host solve, the stopping rule, the final error pass).  The target's
+tree is built once per target (host) and uploaded once; `e2e` repeats the
+whole job from host buffers -- tree build, upload, source upload, registration
+-- through the C ABI every step.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the
+same workload instead.
+
+Launch: python bench.py [--gpus 1] [--steps K] [--warmup W]
+        python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
+(N > 1: independent replicas, one per GPU, no data exchange: weak scaling.)
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle (baseline leg) is timed single-threaded
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NN queries/s and ICP iterations/s at 100k↔100k pts; % of HBM/L2 roofline"
+UNIT = "ICP iterations/s"
+WORKLOAD = ("scene 100k<->100k: ground plane 40x40 m + 20 boxes + 10 cylinders, N(0,0.01 m) noise, "
+            "offset <=15 deg / <=1 m; leaf 12, max_iter 50, max correspondence 1.0 m, eps 1e-5 m^2")
+
+# Algorithmic bytes per query of one fused ICP pass over this registration,
+# counted by the oracle's reference search (python -m oracle.yardstick):
+# 16 B source record + 8 B per node entered + 16 B per reference point
+# measured, averaged over the 51 passes of the registration
+# (35.85 nodes, 101.24 points per query).
+ICP_BYTES_PER_QUERY = 1922.64
+
+SLOWDOWN_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_over_ranks(elapsed_s: float, units: float, group=None):
+    """(max elapsed over ranks, sum of units over ranks); identity without a
+    process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def run_ours(args):
+    import torch
+    import icp_nearest_neighbour_gb300 as nn
+    import workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    nn.load()
+
+    case = workloads.scene_case()
+    dmax = case.max_corr_dist[0]
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.zeros(2 * l2 // 4, dtype=torch.float32, device="cuda")
+
+    # once per target: host build + upload (timed separately, reported)
+    t0 = time.perf_counter()
+    tree = nn.kdtree_build(case.target, case.leaf_size)
+    build_ms = (time.perf_counter() - t0) * 1e3
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    nn.kdtree_upload(tree)
+    upload_ms = (time.perf_counter() - t0) * 1e3
+    info = nn.kdtree_info(tree)
+    src = torch.from_numpy(case.source).cuda()
+    n = len(case.source)
+
+    def step(timing):
+        return nn.icp_align(tree, src, case.max_iter, case.eps, dmax, timing=timing, stream=stream)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = nn.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    results = []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush_l2(flush)
+            ev[k][0].record(stream)
+            results.append(step(True))
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    launches = nn.launch_count() - launches0
+    barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = sum(step_ms) / 1e3
+    iters = sum(r["iters"] for r in results)
+    passes = sum(r["iters"] + 1 for r in results)
+    kernel_ms = [rec["kernel_ms"] for r in results for rec in r["trace"]]
+    t_max, iters_all = reduce_over_ranks(total_s, iters)
+    _, passes_all = reduce_over_ranks(total_s, passes)
+
+    # ---- end to end from host buffers: build + upload + registration
+    pinned_src = torch.from_numpy(case.source).pin_memory()
+    pinned_tgt = case.target
+    h2d = 0
+    d2h = 0
+    e2e_iters = 0
+    barrier()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(args.steps):
+        t_e = nn.kdtree_build(pinned_tgt, case.leaf_size)
+        nn.kdtree_upload(t_e, stream=stream)
+        r = nn.icp_align(t_e, pinned_src, case.max_iter, case.eps, dmax, stream=stream)
+        e2e_iters += r["iters"]
+        h2d += (2 ** (info["depth"] + 1)) * 8 + n * 16 + n * 12
+        d2h += 24 + (r["iters"] + 1) * 18 * 8
+        t_e.free()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - e0
+    e2e_max, e2e_iters_all = reduce_over_ranks(e2e_s, e2e_iters)
+
+    if rank != 0:
+        return None
+
+    avg_kernel_s = statistics.mean(kernel_ms) / 1e3
+    achieved = ICP_BYTES_PER_QUERY * n / avg_kernel_s / 1e9
+    peak, peak_src = measured_hbm_peak()
+    line = {
+        "metric": METRIC,
+        "value": iters_all / t_max,
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_max * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "n_target": len(case.target), "n_source": n, "leaf_size": case.leaf_size,
+            "tree_depth": info["depth"], "tree_nodes": info["n_nodes"],
+            "iters_per_step": iters // args.steps, "passes_per_step": passes // args.steps,
+            "l2": "flushed between steps (write of 2x L2 size); the tree stays L2-resident within a step",
+            "parallelism": f"replicas x{ws}",
+        },
+        "nn_queries_per_s": passes_all * n / t_max,
+        "roofline": {
+            "bound": "hbm", "kernel": "icp_pass_kernel",
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": peak_src,
+            "traffic": None,
+            "bytes_per_query": ICP_BYTES_PER_QUERY,
+            "avg_kernel_us": avg_kernel_s * 1e6,
+        },
+        "e2e": {"value": e2e_iters_all / e2e_max, "unit": UNIT,
+                "h2d_bytes_per_step": h2d // args.steps, "d2h_bytes_per_step": d2h // args.steps,
+                "includes": "host tree build + upload + source H2D + registration, via the C ABI"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "once_per_target_ms": {"kdtree_build": build_ms, "kdtree_upload": upload_ms},
+        "wall_s_timed_region": wall,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_iters)
+    return line
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (measured)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_registration(case, max_iter, eps):
+    """Build + one registration with the CPU oracle; returns (iters, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    tree = oracle.KDTree(case.target, case.leaf_size)
+    r = oracle.icp_align(tree, case.source, max_iter, eps, case.max_corr_dist[0])
+    return r["iters"], time.perf_counter() - t0
+
+
+def cpu_baseline(case, iters):
+    import oracle
+    oracle.build()
+    n_it, secs = oracle_registration(case, iters, 0.0)
+    return {"value": n_it / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_it} ICP iterations (+ tree build and final pass) of the same 100k<->100k "
+                      f"scene registration, oracle C KD-tree search + NumPy/LAPACK solve, 1 thread; "
+                      f"{secs:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    import workloads
+    oracle.build()
+    case = workloads.scene_case()
+    for _ in range(args.warmup):
+        oracle_registration(case, args.ref_iters, 0.0)
+    total_it = 0
+    total_s = 0.0
+    for _ in range(args.steps):
+        it, s = oracle_registration(case, args.ref_iters, 0.0)
+        total_it += it
+        total_s += s
+    value = total_it / total_s
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n_target": len(case.target), "n_source": len(case.source),
+                   "iters_per_step": args.ref_iters, "parallelism": "1 host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.ref_iters} ICP iterations (+ tree build and final pass) of "
+                                   "the scene registration per step, oracle as it stands, 1 thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-iters", type=int, default=50, help="oracle iterations in cpu_baseline")
+    ap.add_argument("--ref-iters", type=int, default=8, help="oracle iterations per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except ImportError:
+        pass
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,280 @@
+"""Python binding of libicpnn (KD-tree nearest neighbour + ICP on one GB300).
+
+Argument marshalling only: every step of the computation runs in the C/CUDA
+library (``libicpnn.so``, built in-tree by ``_build.build()``).  There is no
+fallback: if the library is missing or fails to load, importing the functions
+raises.  Functions carry the C names without the ``icpnn_`` prefix; see
+``include/icpnn.h`` for the full contract of each call.
+
+Arrays may be NumPy arrays (host memory) or torch tensors (host or CUDA
+memory); points are (n, 3) float32, C-contiguous.  PyTorch is used only to
+hold device memory and to name the stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from ._build import LIB as _LIB_PATH, build as _build_library
+
+__all__ = [
+    "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
+    "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "kabsch", "icp_align",
+    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "MAX_DEPTH",
+]
+
+MORTON_SORT = 1
+TRACE_TIMING = 2
+MAX_DEPTH = 20
+
+STATUS = {
+    0: "OK", -1: "INVALID_ARG", -2: "NOT_UPLOADED", -3: "CUDA", -4: "DEGENERATE",
+    -5: "TREE_DEPTH", -6: "NONFINITE", -7: "NO_MEMORY",
+}
+
+
+class IcpnnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+
+
+class Moments(ctypes.Structure):
+    _fields_ = [("n_accepted", ctypes.c_int64), ("n_nonfinite", ctypes.c_int64),
+                ("mu_src", ctypes.c_double * 3), ("mu_tgt", ctypes.c_double * 3),
+                ("H", ctypes.c_double * 9), ("sum_d2", ctypes.c_double), ("mse", ctypes.c_double)]
+
+    def as_dict(self):
+        return {"n_accepted": self.n_accepted, "n_nonfinite": self.n_nonfinite,
+                "mu_src": np.array(self.mu_src[:]), "mu_tgt": np.array(self.mu_tgt[:]),
+                "H": np.array(self.H[:]).reshape(3, 3), "sum_d2": self.sum_d2, "mse": self.mse}
+
+
+class IterRecord(ctypes.Structure):
+    _fields_ = [("iter", ctypes.c_int32), ("flags", ctypes.c_int32), ("n_accepted", ctypes.c_int64),
+                ("mse", ctypes.c_double), ("T", ctypes.c_double * 16), ("kernel_ms", ctypes.c_float),
+                ("reserved", ctypes.c_float)]
+
+
+_lib = None
+
+
+def load(build_if_missing: bool = False):
+    """Load libicpnn.so (building it first only when asked)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing:
+        _build_library()
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libicpnn.so not built ({_LIB_PATH}); run __graft_entry__.build() "
+                           "or python -m icp_nearest_neighbour_gb300._build")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i64, i32, u32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
+                             ctypes.c_double)
+    sig = {
+        "icpnn_kdtree_build": ([P, i64, i32, i32, ctypes.POINTER(P)], ctypes.c_int),
+        "icpnn_kdtree_upload": ([P, P], ctypes.c_int),
+        "icpnn_kdtree_free": ([P], None),
+        "icpnn_kdtree_info": ([P, P, P, P, P, P], ctypes.c_int),
+        "icpnn_kdtree_export": ([P, i64, P, P, P, P, P, P, P], ctypes.c_int),
+        "icpnn_nn_query": ([P, P, i64, P, P, u32, P], ctypes.c_int),
+        "icpnn_icp_step": ([P, P, i64, P, P, f64, P, P, P, P], ctypes.c_int),
+        "icpnn_kabsch": ([P, P], ctypes.c_int),
+        "icpnn_icp_align": ([P, P, i64, i32, f64, f64, P, P, P, P, P, i32, u32, P], ctypes.c_int),
+        "icpnn_last_error": ([], ctypes.c_char_p),
+        "icpnn_launch_count": ([], i64),
+        "icpnn_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load().icpnn_last_error().decode()
+
+
+def launch_count() -> int:
+    return int(load().icpnn_launch_count())
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise IcpnnError(rc, last_error())
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _is_torch(x) -> bool:
+    return type(x).__module__.startswith("torch")
+
+
+def _ptr(x, dtype, shape_last=None, name="array"):
+    """Address of a contiguous array of the given numpy dtype (None -> NULL)."""
+    if x is None:
+        return None
+    if _is_torch(x):
+        import torch
+        tdt = {np.float32: torch.float32, np.int32: torch.int32, np.float64: torch.float64}[dtype]
+        if x.dtype != tdt or not x.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous {tdt} tensor")
+        if shape_last is not None and (x.dim() != 2 or x.shape[1] != shape_last):
+            raise TypeError(f"{name}: expected shape (n, {shape_last})")
+        return ctypes.c_void_p(x.data_ptr())
+    if not isinstance(x, np.ndarray) or x.dtype != dtype or not x.flags.c_contiguous:
+        raise TypeError(f"{name}: expected a C-contiguous numpy {np.dtype(dtype)} array")
+    if shape_last is not None and (x.ndim != 2 or x.shape[1] != shape_last):
+        raise TypeError(f"{name}: expected shape (n, {shape_last})")
+    return ctypes.c_void_p(x.ctypes.data)
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------- tree
+
+class KDTree:
+    """Owner of an ``icpnn_tree`` handle."""
+
+    def __init__(self, handle):
+        self._h = handle
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("tree has been freed")
+        return self._h
+
+    def free(self):
+        if self._h is not None and _lib is not None:
+            _lib.icpnn_kdtree_free(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+    def info(self):
+        return kdtree_info(self)
+
+
+def kdtree_build(points, leaf_size: int, max_depth: int = -1) -> KDTree:
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
+    lib = load()
+    h = ctypes.c_void_p()
+    _check(lib.icpnn_kdtree_build(_ptr(pts, np.float32, 3, "points"), len(pts), int(leaf_size),
+                                  int(max_depth), ctypes.byref(h)))
+    return KDTree(h)
+
+
+def kdtree_upload(tree: KDTree, stream=None):
+    _check(load().icpnn_kdtree_upload(tree.handle, _stream(stream)))
+
+
+def kdtree_free(tree: KDTree):
+    tree.free()
+
+
+def kdtree_info(tree: KDTree) -> dict:
+    n = ctypes.c_int64()
+    leaf = ctypes.c_int32()
+    md = ctypes.c_int32()
+    depth = ctypes.c_int32()
+    nodes = ctypes.c_int64()
+    _check(load().icpnn_kdtree_info(tree.handle, ctypes.byref(n), ctypes.byref(leaf), ctypes.byref(md),
+                                    ctypes.byref(depth), ctypes.byref(nodes)))
+    return {"n_points": n.value, "leaf_size": leaf.value, "max_depth": md.value, "depth": depth.value,
+            "n_nodes": nodes.value}
+
+
+def kdtree_export(tree: KDTree) -> dict:
+    info = kdtree_info(tree)
+    m, n = info["n_nodes"], info["n_points"]
+    out = {"split_val": np.empty(m, np.float32), "split_dim": np.empty(m, np.int32),
+           "left": np.empty(m, np.int32), "right": np.empty(m, np.int32), "start": np.empty(m, np.int32),
+           "end": np.empty(m, np.int32), "leaf_index": np.empty(n, np.int32)}
+    keys = ["split_val", "split_dim", "left", "right", "start", "end", "leaf_index"]
+    _check(load().icpnn_kdtree_export(tree.handle, m, *[ctypes.c_void_p(out[k].ctypes.data) for k in keys]))
+    return out
+
+
+# ---------------------------------------------------------------- query / ICP
+
+def nn_query(tree: KDTree, xyz, idx, dist2, flags: int = MORTON_SORT, stream=None):
+    """Fill idx (int32, n) and dist2 (float32, n) with each query's exact nearest target point."""
+    n = int(xyz.shape[0])
+    _check(load().icpnn_nn_query(tree.handle, _ptr(xyz, np.float32, 3, "xyz"), n,
+                                 _ptr(idx, np.int32, None, "idx"), _ptr(dist2, np.float32, None, "dist2"),
+                                 int(flags), _stream(stream)))
+
+
+def icp_step(tree: KDTree, src, R, t, max_corr_dist: float = float("inf"), idx=None, dist2=None,
+             stream=None) -> dict:
+    """One fused correspondence pass under float32 (R, t); returns the moments as a dict."""
+    R32 = np.ascontiguousarray(R, dtype=np.float32).reshape(9)
+    t32 = np.ascontiguousarray(t, dtype=np.float32).reshape(3)
+    m = Moments()
+    _check(load().icpnn_icp_step(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
+                                 ctypes.c_void_p(R32.ctypes.data), ctypes.c_void_p(t32.ctypes.data),
+                                 float(max_corr_dist), _ptr(idx, np.int32, None, "idx"),
+                                 _ptr(dist2, np.float32, None, "dist2"), ctypes.byref(m), _stream(stream)))
+    return m.as_dict()
+
+
+def kabsch(moments: dict) -> np.ndarray:
+    """Host solve from a moments dict (as returned by icp_step): 4x4 transform."""
+    m = Moments()
+    m.n_accepted = int(moments["n_accepted"])
+    m.n_nonfinite = int(moments.get("n_nonfinite", 0))
+    m.mu_src[:] = [float(v) for v in moments["mu_src"]]
+    m.mu_tgt[:] = [float(v) for v in moments["mu_tgt"]]
+    m.H[:] = [float(v) for v in np.asarray(moments["H"]).reshape(9)]
+    T = np.zeros(16)
+    _check(load().icpnn_kabsch(ctypes.byref(m), ctypes.c_void_p(T.ctypes.data)))
+    return T.reshape(4, 4)
+
+
+def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
+              init_T=None, trace: bool = False, timing: bool = False, stream=None) -> dict:
+    """Register src onto the tree's points; returns dict(T, final_mse, iters, trace)."""
+    T = np.zeros(16)
+    fmse = ctypes.c_double()
+    iters = ctypes.c_int32()
+    init = None
+    if init_T is not None:
+        init_arr = np.ascontiguousarray(init_T, dtype=np.float64).reshape(16)
+        init = ctypes.c_void_p(init_arr.ctypes.data)
+    cap = int(max_iter) if (trace or timing) else 0
+    recs = (IterRecord * max(cap, 1))()
+    flags = TRACE_TIMING if timing else 0
+    _check(load().icpnn_icp_align(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
+                                  int(max_iter), float(eps), float(max_corr_dist), init,
+                                  ctypes.c_void_p(T.ctypes.data), ctypes.byref(fmse), ctypes.byref(iters),
+                                  ctypes.cast(recs, ctypes.c_void_p) if cap else None, cap, flags,
+                                  _stream(stream)))
+    out = {"T": T.reshape(4, 4), "final_mse": fmse.value, "iters": iters.value}
+    if cap:
+        out["trace"] = [{"iter": r.iter, "n_accepted": r.n_accepted, "mse": r.mse,
+                         "T": np.array(r.T[:]).reshape(4, 4), "kernel_ms": r.kernel_ms}
+                        for r in recs[:min(iters.value, cap)]]
+    return out

@@ -1,0 +1,577 @@
+// C ABI of libicpnn: argument checking, device memory, the host ICP loop of
+// "Implementing ICP with CUDA-KDTree" section 3.3 with the section 4.6
+// stopping rule.  The per-iteration device work is one fused kernel; the only
+// per-iteration host crossing is its 18-double moment record, written by the
+// kernel straight into mapped pinned memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cfloat>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "icpnn_internal.h"
+#include "kernels.cuh"
+
+namespace icpnn {
+
+extern std::atomic<int64_t> g_launch_count;
+
+namespace {
+thread_local std::string tl_error;
+}
+
+int fail(int code, const std::string& msg) {
+  tl_error = msg;
+  return code;
+}
+void clear_error() { tl_error.clear(); }
+
+namespace {
+
+#define ICPNN_CUDA(call)                                                              \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess) {                                                          \
+      if (e_ == cudaErrorMemoryAllocation) {                                          \
+        cudaGetLastError();                                                           \
+        return fail(ICPNN_ERR_NO_MEMORY, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+      }                                                                               \
+      return fail(ICPNN_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    }                                                                                 \
+  } while (0)
+
+bool is_device_pointer(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// Device allocations from the stream-ordered pool, returned on the same stream.
+class Scratch {
+ public:
+  explicit Scratch(cudaStream_t s) : s_(s) {}
+  ~Scratch() {
+    for (void* p : ptrs_) cudaFreeAsync(p, s_);
+  }
+  template <typename T>
+  cudaError_t alloc(T** out, int64_t count) {
+    void* p = nullptr;
+    const size_t bytes = static_cast<size_t>(std::max<int64_t>(count, 1)) * sizeof(T);
+    cudaError_t e = cudaMallocAsync(&p, bytes, s_);
+    if (e != cudaSuccess) return e;
+    ptrs_.push_back(p);
+    *out = static_cast<T*>(p);
+    return cudaSuccess;
+  }
+
+ private:
+  cudaStream_t s_;
+  std::vector<void*> ptrs_;
+};
+
+// Per-thread pinned, device-mapped buffer for the per-pass moment record and
+// other small device->host results.  Kept for the life of the thread.
+struct MappedBuffer {
+  double* host = nullptr;
+  double* dev = nullptr;
+};
+thread_local MappedBuffer tl_mapped;
+constexpr int kMappedDoubles = 64;
+
+int mapped_buffer(MappedBuffer** out) {
+  if (tl_mapped.host == nullptr) {
+    void* h = nullptr;
+    ICPNN_CUDA(cudaHostAlloc(&h, kMappedDoubles * sizeof(double),
+                             cudaHostAllocMapped | cudaHostAllocPortable));
+    void* d = nullptr;
+    const cudaError_t e = cudaHostGetDevicePointer(&d, h, 0);
+    if (e != cudaSuccess) {
+      cudaFreeHost(h);
+      return fail(ICPNN_ERR_CUDA, std::string("cudaHostGetDevicePointer: ") + cudaGetErrorString(e));
+    }
+    tl_mapped.host = static_cast<double*>(h);
+    tl_mapped.dev = static_cast<double*>(d);
+  }
+  *out = &tl_mapped;
+  return ICPNN_OK;
+}
+
+int check_tree_on_device(const icpnn_tree* t) {
+  if (t == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "tree is NULL");
+  if (t->dev.nodes == nullptr) return fail(ICPNN_ERR_NOT_UPLOADED, "tree has not been uploaded");
+  int cur = -1;
+  ICPNN_CUDA(cudaGetDevice(&cur));
+  if (cur != t->dev.device)
+    return fail(ICPNN_ERR_NOT_UPLOADED, "tree was uploaded to device " + std::to_string(t->dev.device) +
+                                            ", current device is " + std::to_string(cur));
+  return ICPNN_OK;
+}
+
+// Largest float f such that, for every float d, d <= f exactly when
+// double(d) <= dmax^2.  No rejection -> +inf.
+float rejection_threshold(double dmax) {
+  if (!(dmax > 0.0) || std::isinf(dmax)) return INFINITY;
+  const double d2 = dmax * dmax;
+  if (std::isinf(d2)) return INFINITY;
+  if (d2 >= static_cast<double>(FLT_MAX)) return FLT_MAX;
+  float f = static_cast<float>(d2);
+  if (static_cast<double>(f) > d2) f = std::nextafter(f, -INFINITY);
+  return f;
+}
+
+// The source in Morton order as float4 records, plus the float32 centre of
+// its bounding box (the shift c_s of the moment sums).
+struct Source {
+  float4* recs = nullptr;
+  float shift[3] = {0, 0, 0};
+};
+
+int prepare_source(const float* xyz, int64_t n, bool morton, bool want_shift, cudaStream_t s,
+                   Scratch& sc, Source* out) {
+  const float* d_xyz = xyz;
+  if (!is_device_pointer(xyz)) {
+    float* tmp = nullptr;
+    ICPNN_CUDA(sc.alloc(&tmp, 3 * n));
+    ICPNN_CUDA(cudaMemcpyAsync(tmp, xyz, static_cast<size_t>(n) * 3 * sizeof(float),
+                               cudaMemcpyHostToDevice, s));
+    d_xyz = tmp;
+  }
+  ICPNN_CUDA(sc.alloc(&out->recs, n));
+  const uint32_t* perm = nullptr;
+  int32_t* bbox6 = nullptr;
+  if (morton || want_shift) {
+    ICPNN_CUDA(sc.alloc(&bbox6, 6));
+    ICPNN_CUDA(launch_bbox(d_xyz, n, bbox6, s));
+  }
+  if (morton && n > 1) {
+    uint32_t *keys, *vals, *keys2, *vals2, *temp, *sorted;
+    ICPNN_CUDA(sc.alloc(&keys, n));
+    ICPNN_CUDA(sc.alloc(&vals, n));
+    ICPNN_CUDA(sc.alloc(&keys2, n));
+    ICPNN_CUDA(sc.alloc(&vals2, n));
+    ICPNN_CUDA(sc.alloc(&temp, radix_temp_words(n)));
+    ICPNN_CUDA(launch_morton(d_xyz, n, bbox6, keys, vals, s));
+    ICPNN_CUDA(radix_sort(keys, vals, keys2, vals2, temp, n, 30, s, &sorted));
+    perm = sorted;
+  }
+  ICPNN_CUDA(launch_gather(d_xyz, n, perm, out->recs, s));
+  if (want_shift) {
+    MappedBuffer* mb = nullptr;
+    if (int rc = mapped_buffer(&mb)) return rc;
+    int32_t* h6 = reinterpret_cast<int32_t*>(mb->host);
+    ICPNN_CUDA(cudaMemcpyAsync(h6, bbox6, 6 * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    ICPNN_CUDA(cudaStreamSynchronize(s));
+    float lo[3], hi[3];
+    decode_bbox(h6, lo, hi);
+    for (int d = 0; d < 3; ++d) out->shift[d] = 0.5f * (lo[d] + hi[d]);
+  }
+  return ICPNN_OK;
+}
+
+void decode_moments(const double raw[kMomentSlots], const float cs[3], const float cq[3],
+                    icpnn_moments* m) {
+  const double N = raw[0];
+  m->n_accepted = static_cast<int64_t>(N);
+  m->n_nonfinite = static_cast<int64_t>(raw[1]);
+  m->sum_d2 = raw[17];
+  if (N > 0) {
+    for (int a = 0; a < 3; ++a) {
+      m->mu_src[a] = static_cast<double>(cs[a]) + raw[2 + a] / N;
+      m->mu_tgt[a] = static_cast<double>(cq[a]) + raw[5 + a] / N;
+    }
+    for (int a = 0; a < 3; ++a)
+      for (int b = 0; b < 3; ++b) m->H[3 * a + b] = raw[8 + 3 * a + b] - raw[2 + a] * raw[5 + b] / N;
+    m->mse = raw[17] / N;
+  } else {
+    for (int a = 0; a < 3; ++a) m->mu_src[a] = m->mu_tgt[a] = NAN;
+    for (int k = 0; k < 9; ++k) m->H[k] = 0.0;
+    m->mse = NAN;
+  }
+}
+
+// Per-point outputs of a pass or query: the caller's device buffers, or
+// staging buffers copied back to the caller's host buffers.
+struct PointOutputs {
+  int32_t* idx = nullptr;
+  float* d2 = nullptr;
+  int32_t* host_idx = nullptr;
+  float* host_d2 = nullptr;
+};
+
+int bind_point_outputs(int32_t* idx, float* d2, int64_t n, Scratch& sc, PointOutputs* po) {
+  if (idx == nullptr) return ICPNN_OK;
+  if (is_device_pointer(idx)) {
+    po->idx = idx;
+  } else {
+    ICPNN_CUDA(sc.alloc(&po->idx, n));
+    po->host_idx = idx;
+  }
+  if (is_device_pointer(d2)) {
+    po->d2 = d2;
+  } else {
+    ICPNN_CUDA(sc.alloc(&po->d2, n));
+    po->host_d2 = d2;
+  }
+  return ICPNN_OK;
+}
+
+int copy_back(const PointOutputs& po, int64_t n, cudaStream_t s) {
+  if (po.host_idx)
+    ICPNN_CUDA(cudaMemcpyAsync(po.host_idx, po.idx, n * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  if (po.host_d2)
+    ICPNN_CUDA(cudaMemcpyAsync(po.host_d2, po.d2, n * sizeof(float), cudaMemcpyDeviceToHost, s));
+  if (po.host_idx || po.host_d2) ICPNN_CUDA(cudaStreamSynchronize(s));
+  return ICPNN_OK;
+}
+
+// Device state of one registration: sorted source, reduction scratch.
+struct Pass {
+  const icpnn_tree* tree = nullptr;
+  Source src;
+  int64_t n = 0;
+  int grid = 0;
+  double* partials = nullptr;
+  uint32_t* counter = nullptr;
+  MappedBuffer* mb = nullptr;
+  float shift_q[3] = {0, 0, 0};
+  float max_d2 = INFINITY;
+};
+
+int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, cudaStream_t s,
+               Scratch& sc, Pass* ps) {
+  ps->tree = t;
+  ps->n = n;
+  if (int rc = prepare_source(src, n, true, true, s, sc, &ps->src)) return rc;
+  ps->grid = icp_pass_grid(*t, n);
+  ICPNN_CUDA(sc.alloc(&ps->partials, static_cast<int64_t>(ps->grid) * kMomentSlots));
+  ICPNN_CUDA(sc.alloc(&ps->counter, 1));
+  ICPNN_CUDA(cudaMemsetAsync(ps->counter, 0, sizeof(uint32_t), s));
+  if (int rc = mapped_buffer(&ps->mb)) return rc;
+  for (int d = 0; d < 3; ++d) ps->shift_q[d] = 0.5f * (t->bbox_lo[d] + t->bbox_hi[d]);
+  ps->max_d2 = rejection_threshold(dmax);
+  return ICPNN_OK;
+}
+
+int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, float* d2,
+             cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m, float* ms) {
+  IcpPassParams p;
+  std::memcpy(p.R, R, sizeof(p.R));
+  std::memcpy(p.t, tr, sizeof(p.t));
+  std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
+  std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
+  p.max_d2 = ps.max_d2;
+  if (ev0) ICPNN_CUDA(cudaEventRecord(ev0, s));
+  ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev,
+                             idx, d2, ps.grid, s));
+  if (ev1) ICPNN_CUDA(cudaEventRecord(ev1, s));
+  ICPNN_CUDA(cudaStreamSynchronize(s));
+  if (ms != nullptr) {
+    *ms = 0.f;
+    if (ev0 && ev1) ICPNN_CUDA(cudaEventElapsedTime(ms, ev0, ev1));
+  }
+  double raw[kMomentSlots];
+  std::memcpy(raw, ps.mb->host, sizeof(raw));
+  decode_moments(raw, ps.src.shift, ps.shift_q, m);
+  return ICPNN_OK;
+}
+
+void transform_to_f32(const double T[16], float R[9], float t[3]) {
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j) R[3 * i + j] = static_cast<float>(T[4 * i + j]);
+    t[i] = static_cast<float>(T[4 * i + 3]);
+  }
+}
+
+struct EventPair {
+  cudaEvent_t a = nullptr, b = nullptr;
+  ~EventPair() {
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+  }
+};
+
+}  // namespace
+}  // namespace icpnn
+
+using namespace icpnn;
+
+extern "C" {
+
+int icpnn_kdtree_build(const float* xyz_host, int64_t n, int32_t leaf_size, int32_t max_depth,
+                       icpnn_tree** out) {
+  clear_error();
+  if (out == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: out is NULL");
+  *out = nullptr;
+  if (xyz_host == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: xyz is NULL");
+  if (n < 1 || n > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: n must be in [1, 2^31-1]");
+  if (leaf_size < 1 || leaf_size > ICPNN_MAX_LEAF_SIZE)
+    return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: leaf_size must be in [1, 64]");
+  if (max_depth == -1) max_depth = ICPNN_MAX_DEPTH;
+  if (max_depth < 0 || max_depth > ICPNN_MAX_DEPTH)
+    return fail(ICPNN_ERR_TREE_DEPTH, "kdtree_build: max_depth must be in [0, 20] or -1");
+  icpnn_tree* t = new (std::nothrow) icpnn_tree();
+  if (t == nullptr) return fail(ICPNN_ERR_NO_MEMORY, "kdtree_build: host allocation failed");
+  const int rc = build_tree(xyz_host, n, leaf_size, max_depth, t);
+  if (rc != ICPNN_OK) {
+    delete t;
+    return rc;
+  }
+  *out = t;
+  return ICPNN_OK;
+}
+
+void icpnn_kdtree_free(icpnn_tree* t) {
+  if (t == nullptr) return;
+  if (t->dev.nodes != nullptr) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    cudaSetDevice(t->dev.device);
+    cudaFree(t->dev.nodes);
+    cudaFree(t->dev.points);
+    cudaSetDevice(cur);
+  }
+  delete t;
+}
+
+int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
+  clear_error();
+  if (t == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_upload: tree is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int cur = -1;
+  ICPNN_CUDA(cudaGetDevice(&cur));
+  if (t->dev.nodes != nullptr && t->dev.device == cur) return ICPNN_OK;
+  if (t->dev.nodes != nullptr) {
+    cudaSetDevice(t->dev.device);
+    cudaFree(t->dev.nodes);
+    cudaFree(t->dev.points);
+    cudaSetDevice(cur);
+    t->dev = DeviceTree{};
+  }
+  Node* nodes = nullptr;
+  float* pts = nullptr;
+  const size_t nb = static_cast<size_t>(t->heap_slots) * sizeof(Node);
+  const size_t pb = static_cast<size_t>(t->n) * 4 * sizeof(float);
+  cudaError_t e = cudaMalloc(&nodes, nb);
+  if (e == cudaSuccess) e = cudaMalloc(&pts, pb);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(nodes, t->nodes.data(), nb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(pts, t->records.data(), pb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (nodes) cudaFree(nodes);
+    if (pts) cudaFree(pts);
+    return fail(e == cudaErrorMemoryAllocation ? ICPNN_ERR_NO_MEMORY : ICPNN_ERR_CUDA,
+                std::string("kdtree_upload: ") + cudaGetErrorString(e));
+  }
+  t->dev.device = cur;
+  t->dev.nodes = nodes;
+  t->dev.points = pts;
+  return ICPNN_OK;
+}
+
+int icpnn_kdtree_info(const icpnn_tree* t, int64_t* n_points, int32_t* leaf_size, int32_t* max_depth,
+                      int32_t* depth, int64_t* n_nodes) {
+  clear_error();
+  if (t == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_info: tree is NULL");
+  if (n_points) *n_points = t->n;
+  if (leaf_size) *leaf_size = t->leaf_size;
+  if (max_depth) *max_depth = t->max_depth;
+  if (depth) *depth = t->depth;
+  if (n_nodes) *n_nodes = t->n_nodes;
+  return ICPNN_OK;
+}
+
+int icpnn_kdtree_export(const icpnn_tree* t, int64_t node_capacity, float* split_val,
+                        int32_t* split_dim, int32_t* left, int32_t* right, int32_t* start,
+                        int32_t* end, int32_t* leaf_index) {
+  clear_error();
+  if (t == nullptr || !split_val || !split_dim || !left || !right || !start || !end || !leaf_index)
+    return fail(ICPNN_ERR_INVALID_ARG, "kdtree_export: NULL argument");
+  if (node_capacity < t->n_nodes) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_export: node_capacity too small");
+  // Walk the heap depth-first, left first: that numbering is the page's
+  // recursion order.  Returns [start, end) of the subtree's points.
+  struct Frame {
+    uint64_t heap;
+    int32_t pre;
+    int stage;
+  };
+  std::vector<Frame> stack;
+  int32_t next = 0;
+  stack.push_back({1, next++, 0});
+  while (!stack.empty()) {
+    Frame& f = stack.back();
+    const Node& nd = t->nodes[f.heap];
+    if (node_is_leaf(nd)) {
+      split_val[f.pre] = 0.0f;
+      split_dim[f.pre] = -1;
+      left[f.pre] = right[f.pre] = -1;
+      start[f.pre] = static_cast<int32_t>(nd.a);
+      end[f.pre] = static_cast<int32_t>(nd.a + (nd.meta >> 2));
+      stack.pop_back();
+      continue;
+    }
+    if (f.stage == 0) {
+      std::memcpy(&split_val[f.pre], &nd.a, sizeof(float));
+      split_dim[f.pre] = static_cast<int32_t>(nd.meta);
+      left[f.pre] = next;
+      f.stage = 1;
+      const uint64_t child = 2 * f.heap;
+      stack.push_back({child, next++, 0});
+    } else if (f.stage == 1) {
+      right[f.pre] = next;
+      f.stage = 2;
+      const uint64_t child = 2 * f.heap + 1;
+      stack.push_back({child, next++, 0});
+    } else {
+      start[f.pre] = start[left[f.pre]];
+      end[f.pre] = end[right[f.pre]];
+      stack.pop_back();
+    }
+  }
+  for (int64_t k = 0; k < t->n; ++k) std::memcpy(&leaf_index[k], &t->records[4 * k + 3], sizeof(int32_t));
+  return ICPNN_OK;
+}
+
+int icpnn_nn_query(const icpnn_tree* t, const float* xyz, int64_t n, int32_t* idx, float* dist2,
+                   uint32_t flags, void* stream) {
+  clear_error();
+  if (n < 0 || n > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "nn_query: n out of range");
+  if (flags & ~ICPNN_MORTON_SORT) return fail(ICPNN_ERR_INVALID_ARG, "nn_query: unknown flag");
+  if (int rc = check_tree_on_device(t)) return rc;
+  if (n == 0) return ICPNN_OK;
+  if (!xyz || !idx || !dist2) return fail(ICPNN_ERR_INVALID_ARG, "nn_query: NULL pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PointOutputs po;
+  {
+    Scratch sc(s);
+    Source src;
+    if (int rc = prepare_source(xyz, n, (flags & ICPNN_MORTON_SORT) != 0, false, s, sc, &src)) return rc;
+    if (int rc = bind_point_outputs(idx, dist2, n, sc, &po)) return rc;
+    ICPNN_CUDA(launch_nn(*t, src.recs, n, po.idx, po.d2, s));
+    if (int rc = copy_back(po, n, s)) return rc;
+  }
+  return ICPNN_OK;
+}
+
+int icpnn_icp_step(const icpnn_tree* t, const float* src, int64_t n, const float* R, const float* tr,
+                   double max_corr_dist, int32_t* idx, float* dist2, icpnn_moments* out, void* stream) {
+  clear_error();
+  if (int rc = check_tree_on_device(t)) return rc;
+  if (!src || !R || !tr || !out) return fail(ICPNN_ERR_INVALID_ARG, "icp_step: NULL pointer");
+  if ((idx == nullptr) != (dist2 == nullptr))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_step: idx and dist2 must both be given or both NULL");
+  if (n < 1 || n > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "icp_step: n out of range");
+  if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_step: max_corr_dist is NaN");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Scratch sc(s);
+  Pass ps;
+  if (int rc = pass_setup(t, src, n, max_corr_dist, s, sc, &ps)) return rc;
+  PointOutputs po;
+  if (int rc = bind_point_outputs(idx, dist2, n, sc, &po)) return rc;
+  if (int rc = pass_run(ps, R, tr, po.idx, po.d2, s, nullptr, nullptr, out, nullptr)) return rc;
+  if (int rc = copy_back(po, n, s)) return rc;
+  if (out->n_nonfinite > 0)
+    return fail(ICPNN_ERR_NONFINITE, "icp_step: " + std::to_string(out->n_nonfinite) +
+                                         " source points have non-finite coordinates");
+  return ICPNN_OK;
+}
+
+int icpnn_kabsch(const icpnn_moments* m, double* T) {
+  clear_error();
+  if (m == nullptr || T == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kabsch: NULL pointer");
+  const int rc = kabsch_solve(*m, T);
+  if (rc != ICPNN_OK) return fail(rc, "kabsch: fewer than 3 pairs or cross-covariance of rank < 2");
+  return ICPNN_OK;
+}
+
+int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_t max_iter, double eps,
+                    double max_corr_dist, const double* init_T, double* out_T, double* final_mse,
+                    int32_t* iters, icpnn_iter_record* trace, int32_t trace_cap, uint32_t flags,
+                    void* stream) {
+  clear_error();
+  if (int rc = check_tree_on_device(t)) return rc;
+  if (!src || !out_T || !final_mse || !iters) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: NULL pointer");
+  if (n_src < 1 || n_src > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: n_src out of range");
+  if (max_iter < 1) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: max_iter must be >= 1");
+  if (!(eps >= 0.0)) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: eps must be >= 0");
+  if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: max_corr_dist is NaN");
+  if (trace_cap < 0 || (trace_cap > 0 && trace == nullptr))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_align: bad trace buffer");
+  if (flags & ~ICPNN_TRACE_TIMING) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: unknown flag");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  double T[16];
+  if (init_T) {
+    std::memcpy(T, init_T, sizeof(T));
+  } else {
+    for (int k = 0; k < 16; ++k) T[k] = (k % 5 == 0) ? 1.0 : 0.0;
+  }
+  EventPair ev;
+  if ((flags & ICPNN_TRACE_TIMING) && trace_cap > 0) {
+    ICPNN_CUDA(cudaEventCreate(&ev.a));
+    ICPNN_CUDA(cudaEventCreate(&ev.b));
+  }
+  Scratch sc(s);
+  Pass ps;
+  if (int rc = pass_setup(t, src, n_src, max_corr_dist, s, sc, &ps)) return rc;
+
+  double mse_hist[3] = {0, 0, 0};
+  int32_t done = 0;
+  for (int32_t k = 0; k < max_iter; ++k) {
+    float R32[9], t32[3];
+    transform_to_f32(T, R32, t32);
+    icpnn_moments m;
+    float ms = 0.f;
+    if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, ev.a, ev.b, &m, &ms)) return rc;
+    if (m.n_nonfinite > 0)
+      return fail(ICPNN_ERR_NONFINITE, "icp_align: " + std::to_string(m.n_nonfinite) +
+                                           " source points have non-finite coordinates");
+    if (m.n_accepted < 3)
+      return fail(ICPNN_ERR_DEGENERATE, "icp_align: fewer than 3 correspondences accepted at iteration " +
+                                            std::to_string(k));
+    if (k < trace_cap) {
+      icpnn_iter_record& r = trace[k];
+      r.iter = k;
+      r.flags = 0;
+      r.n_accepted = m.n_accepted;
+      r.mse = m.mse;
+      std::memcpy(r.T, T, sizeof(T));
+      r.kernel_ms = ms;
+      r.reserved = 0.f;
+    }
+    double Tn[16];
+    if (kabsch_solve(m, Tn) != ICPNN_OK)
+      return fail(ICPNN_ERR_DEGENERATE, "icp_align: rank-deficient cross-covariance at iteration " +
+                                            std::to_string(k));
+    std::memcpy(T, Tn, sizeof(T));
+    mse_hist[0] = mse_hist[1];
+    mse_hist[1] = mse_hist[2];
+    mse_hist[2] = m.mse;
+    done = k + 1;
+    if (k >= 2 && std::fabs(mse_hist[1] - mse_hist[2]) < eps && std::fabs(mse_hist[0] - mse_hist[1]) < eps)
+      break;
+  }
+  float R32[9], t32[3];
+  transform_to_f32(T, R32, t32);
+  icpnn_moments fin;
+  if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, &fin, nullptr)) return rc;
+  std::memcpy(out_T, T, sizeof(T));
+  *final_mse = fin.mse;
+  *iters = done;
+  return ICPNN_OK;
+}
+
+const char* icpnn_last_error(void) { return tl_error.c_str(); }
+
+int64_t icpnn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
+
+int32_t icpnn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Internal declarations shared by the host and device parts of libicpnn.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "icpnn.h"
+
+namespace icpnn {
+
+// ---------------------------------------------------------------------------
+// Device tree layout.
+//
+// The page's node (section 3.1) is a 24-byte record with explicit child links
+// and a [start, end) range into a separate leaf index table.  Here the tree is
+// stored as an implicit binary heap, 1-based: the root is node 1 and the
+// children of node i are 2i and 2i+1, so siblings share one 16-byte-aligned
+// pair and a single vector load fetches both children of a node.  With median
+// splits every node at depth k holds floor or ceil of n / 2^k points, so leaves
+// sit on at most two adjacent levels and the heap wastes at most half its
+// slots.
+//
+// Each node is 8 bytes {uint32 a, uint32 meta}:
+//   inner: a = float bits of the split value, meta = split axis (0, 1, 2)
+//   leaf : a = first point record,            meta = 3 | (count << 2)
+// Slot 0 is unused (zeroed).
+//
+// Points are stored in leaf order as float4 records {x, y, z, index bits}:
+// one 16-byte load returns both the coordinates and the original target index
+// (the page's leaf_index indirection, section 3.2, disappears).
+// ---------------------------------------------------------------------------
+struct Node {
+  uint32_t a;
+  uint32_t meta;
+};
+static_assert(sizeof(Node) == 8, "node must be 8 bytes");
+
+constexpr uint32_t kLeafTag = 3u;
+
+inline bool node_is_leaf(const Node& n) { return (n.meta & 3u) == kLeafTag; }
+
+struct DeviceTree {
+  int device = -1;
+  Node* nodes = nullptr;      // heap_slots entries
+  float* points = nullptr;    // n float4 records (x, y, z, index bits)
+};
+
+}  // namespace icpnn
+
+struct icpnn_tree {
+  int64_t n = 0;
+  int32_t leaf_size = 0;
+  int32_t max_depth = 0;
+  int32_t depth = 0;          // deepest level holding a node (root = 0)
+  int64_t n_nodes = 0;        // nodes in use
+  int64_t heap_slots = 0;     // 2^(depth+1)
+  float bbox_lo[3] = {0, 0, 0};
+  float bbox_hi[3] = {0, 0, 0};
+  std::vector<icpnn::Node> nodes;   // heap layout, heap_slots entries
+  std::vector<float> records;       // 4 floats per point, leaf order
+  icpnn::DeviceTree dev;
+};
+
+namespace icpnn {
+
+// Thread-local error message; returns `code` so callers can `return fail(...)`.
+int fail(int code, const std::string& msg);
+void clear_error();
+
+// Host tree build (kdtree_build.cpp).
+int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth,
+               icpnn_tree* t);
+
+// Host Kabsch solve (kabsch.cpp).  Returns ICPNN_OK or ICPNN_ERR_DEGENERATE.
+int kabsch_solve(const icpnn_moments& m, double T[16]);
+
+}  // namespace icpnn

@@ -1,0 +1,617 @@
+// Device code of libicpnn for sm_103a.
+//
+//  * Morton ordering of queries ("Implementing ICP with CUDA-KDTree",
+//    section 5.3): bounding box, 30-bit Morton code per point, stable LSD
+//    radix sort of (code, index), gather into float4 records.
+//  * Exact KD-tree 1-NN search (section 3.2): depth-first, near child first,
+//    far child kept on a per-thread stack with the squared distance to its
+//    splitting plane and skipped when that bound exceeds the best distance.
+//    The top levels of the tree are staged in shared memory.
+//  * The fused ICP pass (sections 2.1, 3.3, 4.4): transform the original
+//    source point, search, reject beyond the maximum distance, accumulate the
+//    centroid and cross-covariance moments; warp-shuffle, then block, then a
+//    last-block grid reduction, all in a fixed order so the result is
+//    bit-reproducible run to run.
+//
+// Exactness.  Distances are d2 = (dx*dx + dy*dy) + dz*dz with dx = r.x - q.x,
+// every operation an explicit round-to-nearest intrinsic, so no FMA
+// contraction can change a bit.  The far child of a node is skipped only when
+// fl(delta*delta) > best, where delta = fl(q_dim - split): rounding is
+// monotone, so every point beyond the plane has |fl(r_dim - q_dim)| >=
+// |delta| and hence d2 >= fl(delta*delta); a point at the best distance (a
+// tie that may carry a lower index) is therefore never pruned, and the search
+// returns the lexicographic minimum of (d2, index) whatever the tree shape or
+// visiting order.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstring>
+
+#include "kernels.cuh"
+
+namespace icpnn {
+
+std::atomic<int64_t> g_launch_count{0};
+
+namespace {
+
+constexpr int kStack = ICPNN_MAX_DEPTH + 1;  // at most one pending far child per level
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xffffffffu;
+
+// ------------------------------------------------------------ helpers ---
+
+__host__ __device__ inline int32_t ordered_from_bits(int32_t i) { return i >= 0 ? i : (i ^ 0x7fffffff); }
+
+__device__ __forceinline__ bool finite3(float x, float y, float z) {
+  return isfinite(x) && isfinite(y) && isfinite(z);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+inline int num_sms() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
+inline int blocks_for(int64_t n, int per_block, int cap) {
+  int64_t b = (n + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return static_cast<int>(b);
+}
+
+// ------------------------------------------------------------ bbox ------
+
+__global__ void bbox_init_kernel(int32_t* bbox6) {
+  const int i = threadIdx.x;
+  if (i < 3) bbox6[i] = INT_MAX;
+  else if (i < 6) bbox6[i] = INT_MIN;
+}
+
+__global__ void __launch_bounds__(kThreads) bbox_kernel(const float* __restrict__ xyz, int64_t n,
+                                                        int32_t* __restrict__ bbox6) {
+  int32_t lo[3] = {INT_MAX, INT_MAX, INT_MAX};
+  int32_t hi[3] = {INT_MIN, INT_MIN, INT_MIN};
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float x = xyz[3 * i], y = xyz[3 * i + 1], z = xyz[3 * i + 2];
+    if (!finite3(x, y, z)) continue;
+    const int32_t o[3] = {ordered_from_bits(__float_as_int(x)), ordered_from_bits(__float_as_int(y)),
+                          ordered_from_bits(__float_as_int(z))};
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      lo[d] = min(lo[d], o[d]);
+      hi[d] = max(hi[d], o[d]);
+    }
+  }
+#pragma unroll
+  for (int d = 0; d < 3; ++d) {
+    lo[d] = __reduce_min_sync(kFull, lo[d]);
+    hi[d] = __reduce_max_sync(kFull, hi[d]);
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      if (lo[d] != INT_MAX) atomicMin(&bbox6[d], lo[d]);
+      if (hi[d] != INT_MIN) atomicMax(&bbox6[3 + d], hi[d]);
+    }
+  }
+}
+
+// ------------------------------------------------------------ Morton ----
+
+__device__ __forceinline__ uint32_t spread10(uint32_t v) {
+  v &= 0x3ffu;
+  v = (v | (v << 16)) & 0x030000ffu;
+  v = (v | (v << 8)) & 0x0300f00fu;
+  v = (v | (v << 4)) & 0x030c30c3u;
+  v = (v | (v << 2)) & 0x09249249u;
+  return v;
+}
+
+__device__ __forceinline__ float decode_ordered(int32_t o) {
+  return __int_as_float(ordered_from_bits(o));
+}
+
+__global__ void __launch_bounds__(kThreads) morton_kernel(const float* __restrict__ xyz, int64_t n,
+                                                          const int32_t* __restrict__ bbox6,
+                                                          uint32_t* __restrict__ keys,
+                                                          uint32_t* __restrict__ vals) {
+  float lo[3], scale[3];
+#pragma unroll
+  for (int d = 0; d < 3; ++d) {
+    const int32_t a = bbox6[d], b = bbox6[3 + d];
+    if (a == INT_MAX || b == INT_MIN) {
+      lo[d] = 0.f;
+      scale[d] = 0.f;
+    } else {
+      lo[d] = decode_ordered(a);
+      const float ext = decode_ordered(b) - lo[d];
+      scale[d] = ext > 0.f ? 1024.f / ext : 0.f;
+    }
+  }
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    uint32_t c[3];
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      float q = (xyz[3 * i + d] - lo[d]) * scale[d];
+      q = fminf(fmaxf(q, 0.f), 1023.f);  // NaN -> 0
+      c[d] = static_cast<uint32_t>(q);
+    }
+    keys[i] = (spread10(c[0]) << 2) | (spread10(c[1]) << 1) | spread10(c[2]);
+    vals[i] = static_cast<uint32_t>(i);
+  }
+}
+
+// ------------------------------------------------------- radix sort -----
+// One 8-bit digit per pass.  Pass = per-tile digit histogram, one exclusive
+// scan over the (digit, tile) matrix in digit-major order, stable scatter.
+// The scatter is stable because ranks follow (round, warp, lane) = position
+// order: a key's destination is its tile's base for the digit, plus the
+// counts of earlier rounds, earlier warps of this round, and earlier lanes of
+// its warp (from __match_any_sync).
+
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+constexpr int kSortItems = 8;
+constexpr int kSortTile = kThreads * kSortItems;
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kThreads) radix_hist_kernel(const uint32_t* __restrict__ keys, int64_t n,
+                                                              int shift, uint32_t* __restrict__ hist,
+                                                              int tiles) {
+  __shared__ uint32_t cnt[kRadix];
+  for (int i = threadIdx.x; i < kRadix; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kSortTile;
+#pragma unroll
+  for (int r = 0; r < kSortItems; ++r) {
+    const int64_t p = base + r * kThreads + threadIdx.x;
+    if (p < n) atomicAdd(&cnt[(keys[p] >> shift) & (kRadix - 1)], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kRadix; i += blockDim.x)
+    hist[static_cast<int64_t>(i) * tiles + blockIdx.x] = cnt[i];
+}
+
+// Exclusive prefix sum of m words in place, one block.
+__global__ void __launch_bounds__(kScanThreads) exclusive_scan_kernel(uint32_t* __restrict__ data, int64_t m) {
+  __shared__ uint32_t warp_sums[kScanThreads / 32];
+  const int t = threadIdx.x;
+  const int64_t chunk = (m + kScanThreads - 1) / kScanThreads;
+  const int64_t beg = t * chunk;
+  const int64_t end = min(m, beg + chunk);
+  uint32_t local = 0;
+  for (int64_t i = beg; i < end; ++i) local += data[i];
+  // inclusive scan of the per-thread sums
+  const int lane = t & 31, warp = t >> 5;
+  uint32_t v = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t u = __shfl_up_sync(kFull, v, off);
+    if (lane >= off) v += u;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t u = __shfl_up_sync(kFull, w, off);
+      if (lane >= off) w += u;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  uint32_t run = v - local + (warp > 0 ? warp_sums[warp - 1] : 0u);
+  for (int64_t i = beg; i < end; ++i) {
+    const uint32_t x = data[i];
+    data[i] = run;
+    run += x;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) radix_scatter_kernel(
+    const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in,
+    uint32_t* __restrict__ keys_out, uint32_t* __restrict__ vals_out, int64_t n, int shift,
+    const uint32_t* __restrict__ offsets, int tiles) {
+  constexpr int kWarps = kThreads / 32;
+  __shared__ uint32_t base[kRadix];
+  __shared__ uint32_t wcount[kWarps][kRadix];
+  const int t = threadIdx.x, warp = t >> 5;
+  for (int i = t; i < kRadix; i += kThreads) base[i] = offsets[static_cast<int64_t>(i) * tiles + blockIdx.x];
+  const int64_t tile0 = static_cast<int64_t>(blockIdx.x) * kSortTile;
+  for (int r = 0; r < kSortItems; ++r) {
+    for (int i = t; i < kWarps * kRadix; i += kThreads) (&wcount[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t p = tile0 + r * kThreads + t;
+    const bool valid = p < n;
+    const uint32_t key = valid ? keys_in[p] : 0u;
+    const uint32_t val = valid ? vals_in[p] : 0u;
+    const uint32_t digit = valid ? ((key >> shift) & (kRadix - 1)) : 0xffffffffu;
+    const uint32_t peers = __match_any_sync(kFull, digit);
+    const uint32_t rank = __popc(peers & lanemask_lt());
+    if (valid && rank == 0) wcount[warp][digit] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      uint32_t off = base[digit] + rank;
+      for (int w = 0; w < warp; ++w) off += wcount[w][digit];
+      keys_out[off] = key;
+      vals_out[off] = val;
+    }
+    __syncthreads();
+    for (int i = t; i < kRadix; i += kThreads) {
+      uint32_t s = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s += wcount[w][i];
+      base[i] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ gather ----
+
+__global__ void __launch_bounds__(kThreads) gather_kernel(const float* __restrict__ xyz, int64_t n,
+                                                          const uint32_t* __restrict__ perm,
+                                                          float4* __restrict__ rec) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t p = perm ? static_cast<int64_t>(perm[i]) : i;
+    rec[i] = make_float4(xyz[3 * p], xyz[3 * p + 1], xyz[3 * p + 2], __int_as_float(static_cast<int32_t>(p)));
+  }
+}
+
+// ------------------------------------------------------------ search ----
+
+struct TreeView {
+  const uint2* __restrict__ nodes;   // heap, 1-based
+  const float4* __restrict__ pts;    // leaf-ordered records
+  const uint2* smem;                 // copy of heap slots [0, smem_slots)
+  uint32_t smem_slots;
+};
+
+struct Best {
+  float d2;
+  int32_t idx;
+  float x, y, z;
+};
+
+__device__ __forceinline__ uint2 load_node(const TreeView& tv, uint32_t i) {
+  return i < tv.smem_slots ? tv.smem[i] : __ldg(&tv.nodes[i]);
+}
+
+__device__ __forceinline__ float dist2(const float4& r, float qx, float qy, float qz) {
+  const float dx = __fsub_rn(r.x, qx);
+  const float dy = __fsub_rn(r.y, qy);
+  const float dz = __fsub_rn(r.z, qz);
+  return __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)), __fmul_rn(dz, dz));
+}
+
+__device__ __forceinline__ void consider(const float4& r, float qx, float qy, float qz, Best& b) {
+  const float d = dist2(r, qx, qy, qz);
+  const int32_t id = __float_as_int(r.w);
+  if (d < b.d2 || (d == b.d2 && id < b.idx)) {
+    b.d2 = d;
+    b.idx = id;
+    b.x = r.x;
+    b.y = r.y;
+    b.z = r.z;
+  }
+}
+
+// Exact nearest neighbour of a finite query point.
+__device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, float qz, Best& b) {
+  uint32_t st_node[kStack];
+  float st_lb[kStack];
+  int sp = 0;
+  uint32_t node = 1;
+  uint2 nd = load_node(tv, node);
+  for (;;) {
+    while ((nd.y & 3u) != kLeafTag) {
+      const uint32_t dim = nd.y;
+      const float split = __uint_as_float(nd.x);
+      const float qd = dim == 0 ? qx : (dim == 1 ? qy : qz);
+      const float delta = __fsub_rn(qd, split);
+      const float lb = __fmul_rn(delta, delta);
+      const uint32_t near = 2 * node + (qd < split ? 0u : 1u);
+      if (lb <= b.d2) {
+        st_node[sp] = near ^ 1u;
+        st_lb[sp] = lb;
+        ++sp;
+      }
+      node = near;
+      nd = load_node(tv, node);
+    }
+    const uint32_t start = nd.x;
+    const uint32_t count = nd.y >> 2;
+    uint32_t k = 0;
+    for (; k + 4 <= count; k += 4) {
+      const float4 r0 = __ldg(&tv.pts[start + k]);
+      const float4 r1 = __ldg(&tv.pts[start + k + 1]);
+      const float4 r2 = __ldg(&tv.pts[start + k + 2]);
+      const float4 r3 = __ldg(&tv.pts[start + k + 3]);
+      consider(r0, qx, qy, qz, b);
+      consider(r1, qx, qy, qz, b);
+      consider(r2, qx, qy, qz, b);
+      consider(r3, qx, qy, qz, b);
+    }
+    for (; k < count; ++k) consider(__ldg(&tv.pts[start + k]), qx, qy, qz, b);
+    bool more = false;
+    while (sp > 0) {
+      --sp;
+      if (st_lb[sp] <= b.d2) {
+        node = st_node[sp];
+        more = true;
+        break;
+      }
+    }
+    if (!more) break;
+    nd = load_node(tv, node);
+  }
+}
+
+__device__ __forceinline__ void stage_top(const uint2* __restrict__ nodes, uint2* s_nodes, int slots) {
+  const uint4* src = reinterpret_cast<const uint4*>(nodes);
+  uint4* dst = reinterpret_cast<uint4*>(s_nodes);
+  for (int i = threadIdx.x; i < slots / 2; i += blockDim.x) dst[i] = __ldg(src + i);
+  __syncthreads();
+}
+
+// ------------------------------------------------------------ NN query --
+
+__global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ nodes,
+                                                      const float4* __restrict__ pts, int smem_slots,
+                                                      const float4* __restrict__ q, int64_t n,
+                                                      int32_t* __restrict__ out_idx,
+                                                      float* __restrict__ out_d2) {
+  extern __shared__ uint2 s_nodes[];
+  stage_top(nodes, s_nodes, smem_slots);
+  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float4 r = q[i];
+    const int32_t slot = __float_as_int(r.w);
+    if (!finite3(r.x, r.y, r.z)) {
+      out_idx[slot] = -1;
+      out_d2[slot] = __int_as_float(0x7fc00000);
+      continue;
+    }
+    Best b{__int_as_float(0x7f800000), INT_MAX, 0.f, 0.f, 0.f};
+    search(tv, r.x, r.y, r.z, b);
+    out_idx[slot] = b.idx == INT_MAX ? -1 : b.idx;
+    out_d2[slot] = b.d2;
+  }
+}
+
+// ------------------------------------------------------------ ICP pass --
+
+template <bool kPerPoint>
+__global__ void __launch_bounds__(kThreads) icp_pass_kernel(
+    const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
+    const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
+    unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
+    float* __restrict__ out_d2) {
+  extern __shared__ uint2 s_nodes[];
+  __shared__ double s_warp[kThreads / 32][kMomentSlots];
+  __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
+  __shared__ bool s_last;
+  stage_top(nodes, s_nodes, smem_slots);
+  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+
+  float acc[16];
+#pragma unroll
+  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+  uint32_t n_acc = 0, n_bad = 0;
+
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float4 s = src[i];
+    const int32_t slot = __float_as_int(s.w);
+    int32_t idx = -1;
+    float d2 = __int_as_float(0x7fc00000);
+    if (!finite3(s.x, s.y, s.z)) {
+      ++n_bad;
+    } else {
+      // p = R s + t, each row ((R_a0 s_x + R_a1 s_y) + R_a2 s_z) + t_a
+      float q[3];
+#pragma unroll
+      for (int a = 0; a < 3; ++a) {
+        float v = __fadd_rn(__fmul_rn(p.R[3 * a], s.x), __fmul_rn(p.R[3 * a + 1], s.y));
+        v = __fadd_rn(v, __fmul_rn(p.R[3 * a + 2], s.z));
+        q[a] = __fadd_rn(v, p.t[a]);
+      }
+      if (finite3(q[0], q[1], q[2])) {
+        Best b{__int_as_float(0x7f800000), INT_MAX, 0.f, 0.f, 0.f};
+        search(tv, q[0], q[1], q[2], b);
+        idx = b.idx;
+        d2 = b.d2;
+        if (b.d2 <= p.max_d2) {
+          ++n_acc;
+          const float ds[3] = {__fsub_rn(s.x, p.shift_s[0]), __fsub_rn(s.y, p.shift_s[1]),
+                               __fsub_rn(s.z, p.shift_s[2])};
+          const float dq[3] = {__fsub_rn(b.x, p.shift_q[0]), __fsub_rn(b.y, p.shift_q[1]),
+                               __fsub_rn(b.z, p.shift_q[2])};
+#pragma unroll
+          for (int a = 0; a < 3; ++a) {
+            acc[a] = __fadd_rn(acc[a], ds[a]);
+            acc[3 + a] = __fadd_rn(acc[3 + a], dq[a]);
+#pragma unroll
+            for (int c = 0; c < 3; ++c) acc[6 + 3 * a + c] = __fadd_rn(acc[6 + 3 * a + c], __fmul_rn(ds[a], dq[c]));
+          }
+          acc[15] = __fadd_rn(acc[15], b.d2);
+        }
+      }
+    }
+    if (kPerPoint) {
+      out_idx[slot] = idx;
+      out_d2[slot] = d2;
+    }
+  }
+
+  // warp: fixed butterfly; lane 0's association order is the same every run
+#pragma unroll
+  for (int v = 0; v < 16; ++v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[v] = __fadd_rn(acc[v], __shfl_xor_sync(kFull, acc[v], off));
+  }
+  n_acc = __reduce_add_sync(kFull, n_acc);
+  n_bad = __reduce_add_sync(kFull, n_bad);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    s_warp[warp][0] = static_cast<double>(n_acc);
+    s_warp[warp][1] = static_cast<double>(n_bad);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = static_cast<double>(acc[v]);
+  }
+  __syncthreads();
+  // block: warps in order
+  if (threadIdx.x < kMomentSlots) {
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
+    partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // grid: the last block to finish sums all block partials in block order
+  constexpr int kGroups = kThreads / kMomentSlots;
+  if (threadIdx.x < kGroups * kMomentSlots) {
+    const int g = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
+    double s = 0.0;
+    for (int b = g; b < static_cast<int>(gridDim.x); b += kGroups)
+      s += __ldcg(&partials[static_cast<int64_t>(b) * kMomentSlots + v]);
+    s_fin[g][v] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < kMomentSlots) {
+    double s = 0.0;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) s += s_fin[g][threadIdx.x];
+    out[threadIdx.x] = s;
+  }
+  if (threadIdx.x == 0) *counter = 0u;
+}
+
+inline int smem_slots_for(const icpnn_tree& t) {
+  return static_cast<int>(std::min<int64_t>(t.heap_slots, kSmemSlots));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ launchers --
+
+void decode_bbox(const int32_t bbox6[6], float lo[3], float hi[3]) {
+  for (int d = 0; d < 3; ++d) {
+    const int32_t a = ordered_from_bits(bbox6[d]);
+    const int32_t b = ordered_from_bits(bbox6[3 + d]);
+    std::memcpy(&lo[d], &a, sizeof(float));
+    std::memcpy(&hi[d], &b, sizeof(float));
+    if (bbox6[d] == INT_MAX || bbox6[3 + d] == INT_MIN) lo[d] = hi[d] = 0.f;
+  }
+}
+
+cudaError_t launch_bbox(const float* xyz, int64_t n, int32_t* bbox6, cudaStream_t s) {
+  bbox_init_kernel<<<1, 32, 0, s>>>(bbox6);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  if (n > 0) {
+    bbox_kernel<<<blocks_for(n, kThreads, 4 * num_sms()), kThreads, 0, s>>>(xyz, n, bbox6);
+    g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_morton(const float* xyz, int64_t n, const int32_t* bbox6, uint32_t* keys,
+                          uint32_t* vals, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  morton_kernel<<<blocks_for(n, kThreads, 8 * num_sms()), kThreads, 0, s>>>(xyz, n, bbox6, keys, vals);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+int64_t radix_temp_words(int64_t n) {
+  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
+  return std::max<int64_t>(1, tiles) * kRadix;
+}
+
+cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                       uint32_t* temp, int64_t n, int bits, cudaStream_t s, uint32_t** sorted_vals) {
+  *sorted_vals = vals;
+  if (n <= 1) return cudaSuccess;
+  const int tiles = static_cast<int>((n + kSortTile - 1) / kSortTile);
+  uint32_t *ki = keys, *vi = vals, *ko = keys_alt, *vo = vals_alt;
+  for (int shift = 0; shift < bits; shift += kRadixBits) {
+    radix_hist_kernel<<<tiles, kThreads, 0, s>>>(ki, n, shift, temp, tiles);
+    exclusive_scan_kernel<<<1, kScanThreads, 0, s>>>(temp, static_cast<int64_t>(tiles) * kRadix);
+    radix_scatter_kernel<<<tiles, kThreads, 0, s>>>(ki, vi, ko, vo, n, shift, temp, tiles);
+    g_launch_count.fetch_add(3, std::memory_order_relaxed);
+    std::swap(ki, ko);
+    std::swap(vi, vo);
+  }
+  *sorted_vals = vi;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const float* xyz, int64_t n, const uint32_t* perm, float4* records,
+                          cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  gather_kernel<<<blocks_for(n, kThreads, 8 * num_sms()), kThreads, 0, s>>>(xyz, n, perm, records);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int32_t* idx,
+                      float* dist2, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int slots = smem_slots_for(t);
+  const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nn_kernel, kThreads, smem);
+  const int grid = blocks_for(n, kThreads, std::max(1, per_sm) * num_sms());
+  nn_kernel<<<grid, kThreads, smem, s>>>(reinterpret_cast<const uint2*>(t.dev.nodes),
+                                          reinterpret_cast<const float4*>(t.dev.points), slots,
+                                          queries, n, idx, dist2);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+int icp_pass_grid(const icpnn_tree& t, int64_t n) {
+  const size_t smem = static_cast<size_t>(smem_slots_for(t)) * sizeof(uint2);
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, icp_pass_kernel<false>, kThreads, smem);
+  return blocks_for(n, kThreads, std::max(1, per_sm) * num_sms());
+}
+
+cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
+                            const IcpPassParams& p, double* partials, uint32_t* counter,
+                            double* out, int32_t* idx, float* dist2, int grid, cudaStream_t s) {
+  const int slots = smem_slots_for(t);
+  const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
+  const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
+  const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
+  if (idx != nullptr || dist2 != nullptr)
+    icp_pass_kernel<true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+                                                        counter, out, idx, dist2);
+  else
+    icp_pass_kernel<false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+                                                         counter, out, nullptr, nullptr);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+}  // namespace icpnn

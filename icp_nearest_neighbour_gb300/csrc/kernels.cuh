@@ -1,0 +1,64 @@
+// Launch interface of the device code (kernels.cu) used by the C ABI (api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "icpnn_internal.h"
+
+namespace icpnn {
+
+// Number of leading heap slots (top tree levels) staged in shared memory by
+// the search kernels: 4096 slots = levels 0..11, 32 KB.
+constexpr int kSmemSlots = 4096;
+
+// ICP pass result: 18 doubles.
+//   [0] accepted pairs, [1] non-finite source points,
+//   [2..4]  sum (s - c_s), [5..7] sum (q - c_q),
+//   [8..16] sum (s - c_s)_a (q - c_q)_b at 8 + 3a + b, [17] sum d2.
+constexpr int kMomentSlots = 18;
+
+struct IcpPassParams {
+  float R[9];
+  float t[3];
+  float shift_s[3];   // c_s
+  float shift_q[3];   // c_q
+  float max_d2;       // accept iff d2 <= max_d2 (float threshold equivalent to the double test)
+};
+
+// Bounding box of n points as order-preserving int encodings
+// (lo x, lo y, lo z, hi x, hi y, hi z); non-finite points are skipped.
+cudaError_t launch_bbox(const float* xyz, int64_t n, int32_t* bbox6, cudaStream_t s);
+void decode_bbox(const int32_t bbox6[6], float lo[3], float hi[3]);
+
+// 30-bit Morton code of every point over the box in bbox6; vals = 0..n-1.
+cudaError_t launch_morton(const float* xyz, int64_t n, const int32_t* bbox6, uint32_t* keys,
+                          uint32_t* vals, cudaStream_t s);
+
+// Stable LSD radix sort of (key, value) pairs on the low `bits` key bits.
+// Buffers: keys/vals (input), keys_alt/vals_alt (same size), temp of
+// radix_temp_words(n) words.  *sorted_vals receives whichever value buffer
+// holds the result.
+int64_t radix_temp_words(int64_t n);
+cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
+                       uint32_t* temp, int64_t n, int bits, cudaStream_t s,
+                       uint32_t** sorted_vals);
+
+// records[i] = (xyz[perm[i]], perm[i]) as float4; perm == nullptr -> identity.
+cudaError_t launch_gather(const float* xyz, int64_t n, const uint32_t* perm, float4* records,
+                          cudaStream_t s);
+
+// Exact 1-NN of every record; writes idx/dist2 at the record's original slot.
+cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int32_t* idx,
+                      float* dist2, cudaStream_t s);
+
+// One fused ICP pass: transform, search, reject, reduce.  `partials` holds
+// grid * kMomentSlots doubles, `counter` one zeroed word (left zeroed), `out`
+// kMomentSlots doubles (may be host-mapped).  idx/dist2 optional.
+int icp_pass_grid(const icpnn_tree& t, int64_t n);
+cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
+                            const IcpPassParams& p, double* partials, uint32_t* counter,
+                            double* out, int32_t* idx, float* dist2, int grid, cudaStream_t s);
+
+}  // namespace icpnn

@@ -1,0 +1,215 @@
+"""GPU parity of the fused ICP pass (icpnn_icp_step) and of the whole
+registration (icpnn_icp_align) against the oracle.
+
+"Implementing ICP with CUDA-KDTree" (pwwt.cn/news/5235220): section 2.1
+(objective and SVD step), 3.3 (loop on the original source with the
+accumulated transform), 4.4 (maximum correspondence distance), 4.6 (stopping
+rule).
+
+Tolerances:
+  * per-point indices and squared distances: bit-identical;
+  * accepted-pair counts: identical (the accept test is an exact float
+    comparison on bit-identical distances);
+  * mse: 1e-6 relative (float32 partial sums per warp, double above);
+  * centroids: 1e-5 of max(|mu|, scene extent); H: 1e-5 relative in the
+    Frobenius norm;
+  * transforms: 1e-4 rad rotation and 1e-5 * scene extent translation.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ROT_TOL = 1e-4
+TRANS_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def nn():
+    import torch
+    import icp_nearest_neighbour_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    m.load(build_if_missing=True)
+    return m
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+def rot_angle(Ra, Rb):
+    """Angle of Ra^T Rb, robust near zero (from the skew part)."""
+    M = np.asarray(Ra).T @ np.asarray(Rb)
+    s = np.linalg.norm([M[2, 1] - M[1, 2], M[0, 2] - M[2, 0], M[1, 0] - M[0, 1]]) / 2
+    c = (np.trace(M) - 1) / 2
+    return math.atan2(s, c)
+
+
+def check_moments(m, st, extent):
+    assert m["n_accepted"] == st["n_accepted"]
+    if st["n_accepted"] == 0:
+        return
+    assert abs(m["mse"] - st["mse"]) <= 1e-6 * abs(st["mse"]) + 1e-30
+    scale = max(np.abs(st["mu_s"]).max(), np.abs(st["mu_q"]).max(), extent)
+    assert np.abs(m["mu_src"] - st["mu_s"]).max() <= 1e-5 * scale
+    assert np.abs(m["mu_tgt"] - st["mu_q"]).max() <= 1e-5 * scale
+    assert np.linalg.norm(m["H"] - st["H"]) <= 1e-5 * np.linalg.norm(st["H"])
+
+
+def check_transform(Ta, Tb, extent):
+    assert rot_angle(Ta[:3, :3], Tb[:3, :3]) <= ROT_TOL
+    assert np.linalg.norm(Ta[:3, 3] - Tb[:3, 3]) <= TRANS_TOL * extent
+
+
+def lib_step(nn, tree, src, T, dmax):
+    import torch
+    R32 = np.asarray(T)[:3, :3].astype(np.float32)
+    t32 = np.asarray(T)[:3, 3].astype(np.float32)
+    n = len(src)
+    idx = torch.empty(n, dtype=torch.int32, device="cuda")
+    d2 = torch.empty(n, dtype=torch.float32, device="cuda")
+    m = nn.icp_step(tree, dev(src), R32, t32, dmax, idx, d2)
+    return m, idx.cpu().numpy(), d2.cpu().numpy()
+
+
+def setup(nn, oracle_mod, case):
+    t = nn.kdtree_build(case.target, case.leaf_size)
+    nn.kdtree_upload(t)
+    return t, oracle_mod.KDTree(case.target, case.leaf_size)
+
+
+@pytest.mark.parametrize("name", ["tiny", "scene"])
+def test_step_parity(nn, oracle_mod, name):
+    c = W.CASES[name]()
+    t, ot = setup(nn, oracle_mod, c)
+    for T in (np.eye(4), c.T_gt):
+        for dmax in (c.max_corr_dist[0], math.inf, 0.05):
+            m, idx, d2 = lib_step(nn, t, c.source, T, dmax)
+            st = oracle_mod.icp_step(ot, c.source, T, dmax)
+            np.testing.assert_array_equal(idx, st["idx"])
+            np.testing.assert_array_equal(d2.view(np.uint32), st["d2"].view(np.uint32))
+            check_moments(m, st, c.extent)
+            assert m["n_nonfinite"] == 0
+
+
+def test_step_host_source_and_no_per_point_outputs(nn, oracle_mod):
+    c = W.tiny_case()
+    t, ot = setup(nn, oracle_mod, c)
+    R = c.T_gt[:3, :3].astype(np.float32)
+    tt = c.T_gt[:3, 3].astype(np.float32)
+    m_host = nn.icp_step(t, c.source, R, tt, 0.1)
+    m_dev = nn.icp_step(t, dev(c.source), R, tt, 0.1)
+    for k in ("n_accepted", "mse"):
+        assert m_host[k] == m_dev[k]
+    np.testing.assert_array_equal(m_host["H"], m_dev["H"])
+    check_moments(m_dev, oracle_mod.icp_step(ot, c.source, c.T_gt, 0.1), c.extent)
+
+
+@pytest.mark.parametrize("nsrc", [1, 3, 255, 257, 4099])
+def test_step_ragged_sizes(nn, oracle_mod, nsrc):
+    c = W.tiny_case()
+    t, ot = setup(nn, oracle_mod, c)
+    src = np.ascontiguousarray(c.source[:nsrc])
+    m, idx, d2 = lib_step(nn, t, src, c.T_gt, math.inf)
+    st = oracle_mod.icp_step(ot, src, c.T_gt, math.inf)
+    np.testing.assert_array_equal(idx, st["idx"])
+    np.testing.assert_array_equal(d2.view(np.uint32), st["d2"].view(np.uint32))
+    check_moments(m, st, c.extent)
+
+
+def _trace_parity(nn, oracle_mod, c, t, ot, src, dmax, res, sample_iters=None):
+    """Feed each iteration's transform to the oracle: same pairs, same mse,
+    and a solve that lands on the library's next transform."""
+    tr = res["trace"]
+    ks = range(len(tr)) if sample_iters is None else sample_iters
+    for k in ks:
+        st = oracle_mod.icp_step(ot, src, tr[k]["T"], dmax)
+        assert tr[k]["n_accepted"] == st["n_accepted"], k
+        assert abs(tr[k]["mse"] - st["mse"]) <= 1e-6 * st["mse"], k
+        T_next = oracle_mod.solve_from_step(st, src, ot)
+        T_lib = tr[k + 1]["T"] if k + 1 < len(tr) else res["T"]
+        check_transform(T_lib, T_next, c.extent)
+
+
+@pytest.mark.parametrize("name", ["tiny", "scene", "lidar"])
+def test_align_parity(nn, oracle_mod, name):
+    c = W.CASES[name]()
+    t, ot = setup(nn, oracle_mod, c)
+    dmax = c.max_corr_dist[0]
+    res = nn.icp_align(t, dev(c.source), c.max_iter, c.eps, dmax, trace=True)
+    _trace_parity(nn, oracle_mod, c, t, ot, c.source, dmax, res)
+    ref = oracle_mod.icp_align(ot, c.source, c.max_iter, c.eps, dmax)
+    # independent end-to-end runs: the same transform; the iteration count may
+    # differ by one when |delta mse| lands within rounding of eps
+    assert abs(res["iters"] - ref["iters"]) <= 1
+    if res["iters"] == ref["iters"]:
+        check_transform(res["T"], ref["T"], c.extent)
+        assert abs(res["final_mse"] - ref["final_mse"]) <= 1e-6 * ref["final_mse"]
+    R = res["T"][:3, :3]
+    np.testing.assert_allclose(R.T @ R, np.eye(3), atol=1e-12)
+    assert abs(np.linalg.det(R) - 1) < 1e-12
+
+
+def test_tiny_recovers_ground_truth(nn):
+    c = W.tiny_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    res = nn.icp_align(t, dev(c.source), c.max_iter, c.eps, c.max_corr_dist[0])
+    assert res["iters"] < c.max_iter
+    assert rot_angle(res["T"][:3, :3], c.T_gt[:3, :3]) < 3e-4
+    assert np.linalg.norm(res["T"][:3, 3] - c.T_gt[:3, 3]) < 5e-4
+
+
+def test_align_is_deterministic(nn):
+    c = W.scene_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    a = nn.icp_align(t, dev(c.source), 10, 0.0, 1.0, trace=True)
+    b = nn.icp_align(t, dev(c.source), 10, 0.0, 1.0, trace=True)
+    np.testing.assert_array_equal(a["T"], b["T"])
+    assert [r["mse"] for r in a["trace"]] == [r["mse"] for r in b["trace"]]
+
+
+def test_large_coarse_to_fine(nn, oracle_mod):
+    """4M target / 2M source, two stages (2.0 m then 0.3 m): parity of the
+    first and last iteration of each stage against the oracle."""
+    c = W.large_case()
+    t, ot = setup(nn, oracle_mod, c)
+    src_d = dev(c.source)
+    T = None
+    for dmax in c.max_corr_dist:
+        res = nn.icp_align(t, src_d, c.max_iter, c.eps, dmax, init_T=T, trace=True)
+        last = len(res["trace"]) - 1
+        _trace_parity(nn, oracle_mod, c, t, ot, c.source, dmax, res, sample_iters=sorted({0, last}))
+        T = res["T"]
+    R = T[:3, :3]
+    assert abs(np.linalg.det(R) - 1) < 1e-12
+
+
+def test_errors(nn):
+    c = W.tiny_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    far = dev(c.source + np.float32(100.0))
+    with pytest.raises(nn.IcpnnError) as e:
+        nn.icp_align(t, far, 5, 1e-6, 0.1)
+    assert e.value.status == "DEGENERATE"
+    bad = c.source.copy()
+    bad[3, 0] = np.nan
+    with pytest.raises(nn.IcpnnError) as e:
+        nn.icp_align(t, dev(bad), 5, 1e-6, math.inf)
+    assert e.value.status == "NONFINITE"
+    with pytest.raises(nn.IcpnnError) as e:
+        nn.icp_align(t, dev(c.source), 0, 1e-6, math.inf)
+    assert e.value.status == "INVALID_ARG"
+    with pytest.raises(nn.IcpnnError) as e:
+        nn.icp_align(t, dev(c.source), 5, -1.0, math.inf)
+    assert e.value.status == "INVALID_ARG"
+    # a failed call leaves the library usable
+    res = nn.icp_align(t, dev(c.source), 5, 0.0, math.inf)
+    assert res["iters"] == 5
