@@ -21,13 +21,15 @@ from ._build import LIB as _LIB_PATH, build as _build_library
 
 __all__ = [
     "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
-    "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "kabsch", "icp_align",
-    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "MAX_DEPTH",
+    "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
+    "kabsch", "icp_align",
+    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "MAX_DEPTH", "NOALLOC_MAX_POINTS",
 ]
 
 MORTON_SORT = 1
 TRACE_TIMING = 2
 MAX_DEPTH = 20
+NOALLOC_MAX_POINTS = 1 << 20
 
 STATUS = {
     0: "OK", -1: "INVALID_ARG", -2: "NOT_UPLOADED", -3: "CUDA", -4: "DEGENERATE",
@@ -83,6 +85,7 @@ def load(build_if_missing: bool = False):
         "icpnn_kdtree_export": ([P, i64, P, P, P, P, P, P, P], ctypes.c_int),
         "icpnn_nn_query": ([P, P, i64, P, P, u32, P], ctypes.c_int),
         "icpnn_icp_step": ([P, P, i64, P, P, f64, P, P, P, P], ctypes.c_int),
+        "icpnn_icp_step_noalloc": ([P, P, i64, P, P, f64, P, P, P, P], ctypes.c_int),
         "icpnn_kabsch": ([P, P], ctypes.c_int),
         "icpnn_icp_align": ([P, P, i64, i32, f64, f64, P, P, P, P, P, i32, u32, P], ctypes.c_int),
         "icpnn_last_error": ([], ctypes.c_char_p),
@@ -238,6 +241,21 @@ def icp_step(tree: KDTree, src, R, t, max_corr_dist: float = float("inf"), idx=N
                                  ctypes.c_void_p(R32.ctypes.data), ctypes.c_void_p(t32.ctypes.data),
                                  float(max_corr_dist), _ptr(idx, np.int32, None, "idx"),
                                  _ptr(dist2, np.float32, None, "dist2"), ctypes.byref(m), _stream(stream)))
+    return m.as_dict()
+
+
+def icp_step_noalloc(tree: KDTree, src, R, t, max_corr_dist: float = float("inf"), idx=None,
+                     dist2=None, stream=None) -> dict:
+    """The same pass as icp_step without any allocation (device buffers only,
+    at most NOALLOC_MAX_POINTS points); for callers that cannot allocate."""
+    R32 = np.ascontiguousarray(R, dtype=np.float32).reshape(9)
+    t32 = np.ascontiguousarray(t, dtype=np.float32).reshape(3)
+    m = Moments()
+    _check(load().icpnn_icp_step_noalloc(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
+                                         ctypes.c_void_p(R32.ctypes.data), ctypes.c_void_p(t32.ctypes.data),
+                                         float(max_corr_dist), _ptr(idx, np.int32, None, "idx"),
+                                         _ptr(dist2, np.float32, None, "dist2"), ctypes.byref(m),
+                                         _stream(stream)))
     return m.as_dict()
 
 

@@ -483,6 +483,61 @@ int icpnn_icp_step(const icpnn_tree* t, const float* src, int64_t n, const float
   return ICPNN_OK;
 }
 
+// The allocation-free pass: every buffer is the caller's or lives in the
+// library's fixed device scratch array; the few bytes that come back to the
+// host land in stack buffers.  No cudaMalloc / cudaFree / cudaHostAlloc,
+// no stream-ordered pool, no host heap for results.
+int icpnn_icp_step_noalloc(const icpnn_tree* t, const float* src, int64_t n, const float* R,
+                           const float* tr, double max_corr_dist, int32_t* idx, float* dist2,
+                           icpnn_moments* out, void* stream) {
+  clear_error();
+  if (int rc = check_tree_on_device(t)) return rc;
+  if (!src || !R || !tr || !out) return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: NULL pointer");
+  if ((idx == nullptr) != (dist2 == nullptr))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: idx and dist2 must both be given or both NULL");
+  if (n < 1 || n > ICPNN_NOALLOC_MAX_POINTS)
+    return fail(ICPNN_ERR_INVALID_ARG,
+                "icp_step_noalloc: n = " + std::to_string(n) + " is outside [1, " +
+                    std::to_string(ICPNN_NOALLOC_MAX_POINTS) +
+                    "], the most points its fixed scratch array can reduce; use icpnn_icp_step");
+  if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: max_corr_dist is NaN");
+  if (!is_device_pointer(src))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: src must be device memory (a host buffer would "
+                                       "need a staging allocation)");
+  if (idx != nullptr && (!is_device_pointer(idx) || !is_device_pointer(dist2)))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: idx and dist2 must be device memory");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  double* scratch = nullptr;
+  ICPNN_CUDA(noalloc_scratch(&scratch));
+  // the finished-block counter must start at zero; the other words are
+  // written before they are read within this call
+  ICPNN_CUDA(cudaMemsetAsync(scratch + noalloc_counter_offset(), 0, sizeof(double), s));
+  int32_t* bbox6 = reinterpret_cast<int32_t*>(scratch + noalloc_bbox_offset());
+  ICPNN_CUDA(launch_bbox(src, n, bbox6, s));
+  int32_t h6[6];
+  ICPNN_CUDA(cudaMemcpyAsync(h6, bbox6, sizeof(h6), cudaMemcpyDeviceToHost, s));
+  ICPNN_CUDA(cudaStreamSynchronize(s));
+  float lo[3], hi[3];
+  decode_bbox(h6, lo, hi);
+  IcpPassParams p;
+  std::memcpy(p.R, R, sizeof(p.R));
+  std::memcpy(p.t, tr, sizeof(p.t));
+  for (int d = 0; d < 3; ++d) {
+    p.shift_s[d] = 0.5f * (lo[d] + hi[d]);
+    p.shift_q[d] = 0.5f * (t->bbox_lo[d] + t->bbox_hi[d]);
+  }
+  p.max_d2 = rejection_threshold(max_corr_dist);
+  ICPNN_CUDA(launch_icp_pass_inplace(*t, src, n, p, scratch, idx, dist2, s));
+  double raw[kMomentSlots];
+  ICPNN_CUDA(cudaMemcpyAsync(raw, scratch + noalloc_result_offset(), sizeof(raw), cudaMemcpyDeviceToHost, s));
+  ICPNN_CUDA(cudaStreamSynchronize(s));
+  decode_moments(raw, p.shift_s, p.shift_q, out);
+  if (out->n_nonfinite > 0)
+    return fail(ICPNN_ERR_NONFINITE, "icp_step_noalloc: " + std::to_string(out->n_nonfinite) +
+                                         " source points have non-finite coordinates");
+  return ICPNN_OK;
+}
+
 int icpnn_kabsch(const icpnn_moments* m, double* T) {
   clear_error();
   if (m == nullptr || T == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kabsch: NULL pointer");

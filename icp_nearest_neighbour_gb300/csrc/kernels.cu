@@ -29,6 +29,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "kernels.cuh"
 
@@ -610,6 +611,183 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
   else
     icp_pass_kernel<false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
                                                          counter, out, nullptr, nullptr);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------- allocation-free pass --
+// A variant of the fused ICP pass for callers that must not allocate device
+// memory.  Instead of Morton-ordered records in pool memory it reads the
+// caller's n x 3 source in place (one thread per point), and every piece of
+// scratch it needs -- the per-block partial moments, the block counter, the
+// bounding box and the final 18-double result -- lives in one file-scope
+// device array.  That array is allocated when the module is loaded and stays
+// resident on every GPU that loads the library until the process exits.
+//
+// Layout of g_noalloc_scratch, in doubles:
+//   [0, kNoAllocMaxBlocks * kMomentSlots)   partial moments of each block
+//   [kNoAllocResult, + kMomentSlots)         the reduced result
+//   [kNoAllocCounter]                        low 32 bits: finished-block counter
+//   [kNoAllocBbox, + 3)                      six int32 bounding-box words
+constexpr int64_t kNoAllocResult = static_cast<int64_t>(kNoAllocMaxBlocks) * kMomentSlots;
+constexpr int64_t kNoAllocCounter = kNoAllocResult + kMomentSlots;
+constexpr int64_t kNoAllocBbox = kNoAllocCounter + 1;
+constexpr int64_t kNoAllocDoubles = kNoAllocBbox + 3;
+static_assert(static_cast<int64_t>(kNoAllocMaxBlocks) * 256 == ICPNN_NOALLOC_MAX_POINTS,
+              "one thread per point, 256 threads per block");
+static_assert(kNoAllocResult == noalloc_result_offset() && kNoAllocCounter == noalloc_counter_offset() &&
+                  kNoAllocBbox == noalloc_bbox_offset(),
+              "scratch layout shared with the host side");
+
+static __device__ __align__(256) double g_noalloc_scratch[kNoAllocDoubles];
+
+namespace {
+
+template <bool kPerPoint>
+__global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
+    const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
+    const float* __restrict__ xyz, int64_t n, IcpPassParams p, double* __restrict__ scratch,
+    int32_t* __restrict__ out_idx, float* __restrict__ out_d2) {
+  extern __shared__ uint2 s_nodes[];
+  __shared__ double s_warp[kThreads / 32][kMomentSlots];
+  __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
+  __shared__ bool s_last;
+  double* partials = scratch;
+  double* result = scratch + kNoAllocResult;
+  unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kNoAllocCounter);
+  stage_top(nodes, s_nodes, smem_slots);
+  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+
+  float acc[16];
+#pragma unroll
+  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+  uint32_t n_acc = 0, n_bad = 0;
+
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const float sx = xyz[3 * i], sy = xyz[3 * i + 1], sz = xyz[3 * i + 2];
+    int32_t idx = -1;
+    float d2 = __int_as_float(0x7fc00000);
+    if (!finite3(sx, sy, sz)) {
+      ++n_bad;
+    } else {
+      float q[3];
+#pragma unroll
+      for (int a = 0; a < 3; ++a) {
+        float v = __fadd_rn(__fmul_rn(p.R[3 * a], sx), __fmul_rn(p.R[3 * a + 1], sy));
+        v = __fadd_rn(v, __fmul_rn(p.R[3 * a + 2], sz));
+        q[a] = __fadd_rn(v, p.t[a]);
+      }
+      if (finite3(q[0], q[1], q[2])) {
+        Best b{__int_as_float(0x7f800000), INT_MAX, 0.f, 0.f, 0.f};
+        search(tv, q[0], q[1], q[2], b);
+        idx = b.idx;
+        d2 = b.d2;
+        if (b.d2 <= p.max_d2) {
+          ++n_acc;
+          const float ds[3] = {__fsub_rn(sx, p.shift_s[0]), __fsub_rn(sy, p.shift_s[1]),
+                               __fsub_rn(sz, p.shift_s[2])};
+          const float dq[3] = {__fsub_rn(b.x, p.shift_q[0]), __fsub_rn(b.y, p.shift_q[1]),
+                               __fsub_rn(b.z, p.shift_q[2])};
+#pragma unroll
+          for (int a = 0; a < 3; ++a) {
+            acc[a] = ds[a];
+            acc[3 + a] = dq[a];
+#pragma unroll
+            for (int c = 0; c < 3; ++c) acc[6 + 3 * a + c] = __fmul_rn(ds[a], dq[c]);
+          }
+          acc[15] = b.d2;
+        }
+      }
+    }
+    if (kPerPoint) {
+      out_idx[i] = idx;
+      out_d2[i] = d2;
+    }
+  }
+
+#pragma unroll
+  for (int v = 0; v < 16; ++v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[v] = __fadd_rn(acc[v], __shfl_xor_sync(kFull, acc[v], off));
+  }
+  n_acc = __reduce_add_sync(kFull, n_acc);
+  n_bad = __reduce_add_sync(kFull, n_bad);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    s_warp[warp][0] = static_cast<double>(n_acc);
+    s_warp[warp][1] = static_cast<double>(n_bad);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = static_cast<double>(acc[v]);
+  }
+  __syncthreads();
+  if (threadIdx.x < kMomentSlots) {
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
+    partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  constexpr int kGroups = kThreads / kMomentSlots;
+  if (threadIdx.x < kGroups * kMomentSlots) {
+    const int g = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
+    double s = 0.0;
+    for (int b = g; b < static_cast<int>(gridDim.x); b += kGroups)
+      s += __ldcg(&partials[static_cast<int64_t>(b) * kMomentSlots + v]);
+    s_fin[g][v] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < kMomentSlots) {
+    double s = 0.0;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) s += s_fin[g][threadIdx.x];
+    result[threadIdx.x] = s;
+  }
+  if (threadIdx.x == 0) *counter = 0u;
+}
+
+}  // namespace
+
+cudaError_t noalloc_scratch(double** out) {
+  // Host code cannot use the array's name as a device address: it resolves to
+  // a host-side shadow.  Look up the real address once per device, with that
+  // device current.
+  static std::mutex mu;
+  static double* addr[kNoAllocMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<double*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_icp_pass_inplace(const icpnn_tree& t, const float* xyz, int64_t n,
+                                    const IcpPassParams& p, double* scratch, int32_t* idx,
+                                    float* dist2, cudaStream_t s) {
+  const int slots = smem_slots_for(t);
+  const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
+  const int grid = static_cast<int>((n + kThreads - 1) / kThreads);
+  const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
+  const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
+  if (idx != nullptr)
+    icp_pass_inplace_kernel<true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, xyz, n, p, scratch,
+                                                               idx, dist2);
+  else
+    icp_pass_inplace_kernel<false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, xyz, n, p, scratch,
+                                                                nullptr, nullptr);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

@@ -61,4 +61,19 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
                             double* out, int32_t* idx, float* dist2, int grid, cudaStream_t s);
 
+// Allocation-free variant of the ICP pass (reads the caller's n x 3 source in
+// place, one thread per point; all scratch in a file-scope device array of
+// kNoAllocMaxBlocks partial records).  noalloc_scratch() returns that array's
+// device address for the current device (looked up once per device).
+constexpr int kNoAllocMaxBlocks = ICPNN_NOALLOC_MAX_POINTS / 256;
+constexpr int kNoAllocMaxDevices = 64;
+cudaError_t noalloc_scratch(double** out);
+// Scratch offsets (in doubles) of the result record and the bounding box.
+constexpr int64_t noalloc_result_offset() { return static_cast<int64_t>(kNoAllocMaxBlocks) * kMomentSlots; }
+constexpr int64_t noalloc_counter_offset() { return noalloc_result_offset() + kMomentSlots; }
+constexpr int64_t noalloc_bbox_offset() { return noalloc_counter_offset() + 1; }
+cudaError_t launch_icp_pass_inplace(const icpnn_tree& t, const float* xyz, int64_t n,
+                                    const IcpPassParams& p, double* scratch, int32_t* idx,
+                                    float* dist2, cudaStream_t s);
+
 }  // namespace icpnn

@@ -213,6 +213,43 @@ int icpnn_icp_align(const icpnn_tree* target, const float* src, int64_t n_src, i
                     double* final_mse, int32_t* iters, icpnn_iter_record* trace,
                     int32_t trace_cap, uint32_t flags, void* stream);
 
+/* ------------------------------------------------------ no allocation --
+ * icpnn_icp_step_noalloc -- the fused correspondence pass of icpnn_icp_step
+ * for callers that cannot allocate device memory: code embedded in a host
+ * application or framework that owns all device memory and hands out only
+ * its own buffers, processes whose device memory is fully reserved by
+ * another allocator, and real-time loops that cannot afford cudaMalloc /
+ * cudaFree (cudaFree waits for the whole device) or an allocation failure
+ * in the middle of a frame.  The paper has no counterpart: it is an
+ * integration aid, not part of the method.
+ *   The result is the same pass: same per-point idx/dist2 (bit for bit) and
+ *   the same moments up to float rounding order (the points are visited in
+ *   the caller's order, not Morton order, so partial sums associate
+ *   differently).
+ *   src          n x 3 float32, DEVICE memory (host pointers are rejected).
+ *   n            1 .. ICPNN_NOALLOC_MAX_POINTS; larger n is rejected with
+ *                ICPNN_ERR_INVALID_ARG (one thread per point; one partial
+ *                record per 256 points must fit the scratch array).
+ *   R, t, max_corr_dist, out   as for icpnn_icp_step.
+ *   idx, dist2   both NULL or both DEVICE buffers of n entries.
+ * Scratch: a fixed file-scope device array of ICPNN_NOALLOC_MAX_POINTS/256
+ * partial records plus a few words (about 576 KB), created when the library
+ * is loaded and held by every GPU that loads it until the process exits.  No
+ * call allocates or frees memory, host or device (the 18-double result is
+ * copied into the caller's `out` through a stack buffer).
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Sharing: every call on a device uses the same array, and each call leaves
+ * its contents behind (the counter that must start at zero is cleared at the
+ * start of every call).  Calls that overlap on the GPU -- concurrent streams
+ * or threads on one device -- race on the array and give wrong results;
+ * serialise them.  The call synchronises `stream`.
+ * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NONFINITE (as icpnn_icp_step). */
+#define ICPNN_NOALLOC_MAX_POINTS 1048576
+int icpnn_icp_step_noalloc(const icpnn_tree* tree, const float* src, int64_t n, const float* R,
+                           const float* t, double max_corr_dist, int32_t* idx, float* dist2,
+                           icpnn_moments* out, void* stream);
+
 /* ----------------------------------------------------------------- misc -- */
 
 /* Message for the calling thread's most recent failed call ("" if none). */
