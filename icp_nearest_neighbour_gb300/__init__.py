@@ -65,16 +65,18 @@ _lib = None
 
 
 def load(build_if_missing: bool = False):
-    """Load libicpnn.so (building it first only when asked)."""
+    """Load libicpnn.so (building it first only when asked).  The environment
+    variable ICPNN_LIBRARY may name another build of the library to load."""
     global _lib
     if _lib is not None:
         return _lib
-    if build_if_missing:
+    path = os.environ.get("ICPNN_LIBRARY", _LIB_PATH)
+    if build_if_missing and path == _LIB_PATH:
         _build_library()
-    if not os.path.exists(_LIB_PATH):
-        raise RuntimeError(f"libicpnn.so not built ({_LIB_PATH}); run __graft_entry__.build() "
+    if not os.path.exists(path):
+        raise RuntimeError(f"libicpnn.so not built ({path}); run __graft_entry__.build() "
                            "or python -m icp_nearest_neighbour_gb300._build")
-    lib = ctypes.CDLL(_LIB_PATH)
+    lib = ctypes.CDLL(path)
     P, i64, i32, u32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
                              ctypes.c_double)
     sig = {

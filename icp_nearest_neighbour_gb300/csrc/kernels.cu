@@ -285,8 +285,8 @@ struct TreeView {
 
 struct Best {
   float d2;
-  int32_t idx;
-  float x, y, z;
+  int32_t idx;   // original target index (INT_MAX: nothing found)
+  uint32_t slot; // position of that point's record
 };
 
 __device__ __forceinline__ uint2 load_node(const TreeView& tv, uint32_t i) {
@@ -300,39 +300,45 @@ __device__ __forceinline__ float dist2(const float4& r, float qx, float qy, floa
   return __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)), __fmul_rn(dz, dz));
 }
 
-__device__ __forceinline__ void consider(const float4& r, float qx, float qy, float qz, Best& b) {
+__device__ __forceinline__ void consider(const float4& r, uint32_t slot, float qx, float qy, float qz,
+                                         Best& b) {
   const float d = dist2(r, qx, qy, qz);
   const int32_t id = __float_as_int(r.w);
   if (d < b.d2 || (d == b.d2 && id < b.idx)) {
     b.d2 = d;
     b.idx = id;
-    b.x = r.x;
-    b.y = r.y;
-    b.z = r.z;
+    b.slot = slot;
   }
 }
 
-// Exact nearest neighbour of a finite query point.
+__device__ __forceinline__ float plane_bound(uint2 nd, float qx, float qy, float qz) {
+  const float qd = nd.y == 0 ? qx : (nd.y == 1 ? qy : qz);
+  const float delta = __fsub_rn(qd, __uint_as_float(nd.x));
+  return __fmul_rn(delta, delta);
+}
+
+// Exact nearest neighbour of a finite query point, depth first, near child
+// first.  Instead of a stack of pending far children the search keeps a
+// 32-bit trail: bit d is set while the far child at depth d of the current
+// path still has to be visited (at most one per level, depth <= 20).  In the
+// implicit heap the pending node is the sibling of the current path's node at
+// that depth, (node >> (depth - d)) ^ 1, and its bound is recomputed from its
+// parent's splitting plane when it is taken up -- against the best distance
+// of that moment, which has usually shrunk.  All state lives in registers:
+// no local-memory stack.  (A restart trail in the sense of Laine, "Restart
+// trail for stackless BVH traversal", 2010; the heap numbering makes the
+// restart from the root unnecessary.)
 __device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, float qz, Best& b) {
-  uint32_t st_node[kStack];
-  float st_lb[kStack];
-  int sp = 0;
-  uint32_t node = 1;
+  uint32_t node = 1, depth = 0, trail = 0;
   uint2 nd = load_node(tv, node);
   for (;;) {
     while ((nd.y & 3u) != kLeafTag) {
-      const uint32_t dim = nd.y;
+      const float qd = nd.y == 0 ? qx : (nd.y == 1 ? qy : qz);
       const float split = __uint_as_float(nd.x);
-      const float qd = dim == 0 ? qx : (dim == 1 ? qy : qz);
       const float delta = __fsub_rn(qd, split);
-      const float lb = __fmul_rn(delta, delta);
-      const uint32_t near = 2 * node + (qd < split ? 0u : 1u);
-      if (lb <= b.d2) {
-        st_node[sp] = near ^ 1u;
-        st_lb[sp] = lb;
-        ++sp;
-      }
-      node = near;
+      node = 2 * node + (qd < split ? 0u : 1u);
+      ++depth;
+      if (__fmul_rn(delta, delta) <= b.d2) trail |= 1u << depth;
       nd = load_node(tv, node);
     }
     const uint32_t start = nd.x;
@@ -343,23 +349,23 @@ __device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, f
       const float4 r1 = __ldg(&tv.pts[start + k + 1]);
       const float4 r2 = __ldg(&tv.pts[start + k + 2]);
       const float4 r3 = __ldg(&tv.pts[start + k + 3]);
-      consider(r0, qx, qy, qz, b);
-      consider(r1, qx, qy, qz, b);
-      consider(r2, qx, qy, qz, b);
-      consider(r3, qx, qy, qz, b);
+      consider(r0, start + k, qx, qy, qz, b);
+      consider(r1, start + k + 1, qx, qy, qz, b);
+      consider(r2, start + k + 2, qx, qy, qz, b);
+      consider(r3, start + k + 3, qx, qy, qz, b);
     }
-    for (; k < count; ++k) consider(__ldg(&tv.pts[start + k]), qx, qy, qz, b);
-    bool more = false;
-    while (sp > 0) {
-      --sp;
-      if (st_lb[sp] <= b.d2) {
-        node = st_node[sp];
-        more = true;
-        break;
-      }
+    for (; k < count; ++k) consider(__ldg(&tv.pts[start + k]), start + k, qx, qy, qz, b);
+    // take up the deepest pending far child whose plane is still within reach
+    for (;;) {
+      if (trail == 0) return;
+      const uint32_t d = 31u - __clz(trail);
+      trail &= ~(1u << d);
+      node = (node >> (depth - d)) ^ 1u;
+      depth = d;
+      const uint2 parent = load_node(tv, node >> 1);
+      nd = load_node(tv, node);
+      if (plane_bound(parent, qx, qy, qz) <= b.d2) break;
     }
-    if (!more) break;
-    nd = load_node(tv, node);
   }
 }
 
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
       out_d2[slot] = __int_as_float(0x7fc00000);
       continue;
     }
-    Best b{__int_as_float(0x7f800000), INT_MAX, 0.f, 0.f, 0.f};
+    Best b{__int_as_float(0x7f800000), INT_MAX, 0u};
     search(tv, r.x, r.y, r.z, b);
     out_idx[slot] = b.idx == INT_MAX ? -1 : b.idx;
     out_d2[slot] = b.d2;
@@ -434,16 +440,21 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
         q[a] = __fadd_rn(v, p.t[a]);
       }
       if (finite3(q[0], q[1], q[2])) {
-        Best b{__int_as_float(0x7f800000), INT_MAX, 0.f, 0.f, 0.f};
+        // Without per-point outputs only accepted pairs matter, so the search
+        // starts with the rejection radius as its best distance (the page's
+        // section 4.4 fuses max_dist into the tree query): it returns the
+        // exact nearest point when one lies within the radius, else nothing.
+        Best b{kPerPoint ? __int_as_float(0x7f800000) : p.max_d2, INT_MAX, 0u};
         search(tv, q[0], q[1], q[2], b);
-        idx = b.idx;
+        idx = b.idx == INT_MAX ? -1 : b.idx;
         d2 = b.d2;
-        if (b.d2 <= p.max_d2) {
+        if (b.idx != INT_MAX && b.d2 <= p.max_d2) {
           ++n_acc;
           const float ds[3] = {__fsub_rn(s.x, p.shift_s[0]), __fsub_rn(s.y, p.shift_s[1]),
                                __fsub_rn(s.z, p.shift_s[2])};
-          const float dq[3] = {__fsub_rn(b.x, p.shift_q[0]), __fsub_rn(b.y, p.shift_q[1]),
-                               __fsub_rn(b.z, p.shift_q[2])};
+          const float4 qr = __ldg(&pts[b.slot]);
+          const float dq[3] = {__fsub_rn(qr.x, p.shift_q[0]), __fsub_rn(qr.y, p.shift_q[1]),
+                               __fsub_rn(qr.z, p.shift_q[2])};
 #pragma unroll
           for (int a = 0; a < 3; ++a) {
             acc[a] = __fadd_rn(acc[a], ds[a]);
@@ -679,7 +690,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
         q[a] = __fadd_rn(v, p.t[a]);
       }
       if (finite3(q[0], q[1], q[2])) {
-        Best b{__int_as_float(0x7f800000), INT_MAX, 0.f, 0.f, 0.f};
+        Best b{__int_as_float(0x7f800000), INT_MAX, 0u};
         search(tv, q[0], q[1], q[2], b);
         idx = b.idx;
         d2 = b.d2;
@@ -687,8 +698,9 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
           ++n_acc;
           const float ds[3] = {__fsub_rn(sx, p.shift_s[0]), __fsub_rn(sy, p.shift_s[1]),
                                __fsub_rn(sz, p.shift_s[2])};
-          const float dq[3] = {__fsub_rn(b.x, p.shift_q[0]), __fsub_rn(b.y, p.shift_q[1]),
-                               __fsub_rn(b.z, p.shift_q[2])};
+          const float4 qr = __ldg(&pts[b.slot]);
+          const float dq[3] = {__fsub_rn(qr.x, p.shift_q[0]), __fsub_rn(qr.y, p.shift_q[1]),
+                               __fsub_rn(qr.z, p.shift_q[2])};
 #pragma unroll
           for (int a = 0; a < 3; ++a) {
             acc[a] = ds[a];

@@ -110,6 +110,25 @@ def test_step_host_source_and_no_per_point_outputs(nn, oracle_mod):
     check_moments(m_dev, oracle_mod.icp_step(ot, c.source, c.T_gt, 0.1), c.extent)
 
 
+@pytest.mark.parametrize("name", ["scene", "lidar"])
+def test_radius_seeded_pass_gives_identical_moments(nn, oracle_mod, name):
+    """Without per-point outputs the search starts from the rejection radius;
+    the accepted pairs, and so every moment bit, must not change."""
+    c = W.CASES[name]()
+    t, ot = setup(nn, oracle_mod, c)
+    src = dev(c.source)
+    for T in (np.eye(4), c.T_gt):
+        R32 = T[:3, :3].astype(np.float32)
+        t32 = T[:3, 3].astype(np.float32)
+        for dmax in (c.max_corr_dist[0], 0.05, 0.3, math.inf):
+            full, _, _ = lib_step(nn, t, c.source, T, dmax)
+            seeded = nn.icp_step(t, src, R32, t32, dmax)
+            for k in ("n_accepted", "sum_d2", "mse"):
+                assert full[k] == seeded[k] or (math.isnan(full[k]) and math.isnan(seeded[k]))
+            np.testing.assert_array_equal(full["H"], seeded["H"])
+            np.testing.assert_array_equal(full["mu_src"], seeded["mu_src"])
+
+
 @pytest.mark.parametrize("nsrc", [1, 3, 255, 257, 4099])
 def test_step_ragged_sizes(nn, oracle_mod, nsrc):
     c = W.tiny_case()
