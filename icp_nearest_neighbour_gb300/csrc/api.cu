@@ -81,6 +81,7 @@ class Scratch {
 struct MappedBuffer {
   double* host = nullptr;
   double* dev = nullptr;
+  unsigned long long seq = 0;  // last sequence number handed to a pass
 };
 thread_local MappedBuffer tl_mapped;
 constexpr int kMappedDoubles = 64;
@@ -96,6 +97,7 @@ int mapped_buffer(MappedBuffer** out) {
       cudaFreeHost(h);
       return fail(ICPNN_ERR_CUDA, std::string("cudaHostGetDevicePointer: ") + cudaGetErrorString(e));
     }
+    std::memset(h, 0, kMappedDoubles * sizeof(double));
     tl_mapped.host = static_cast<double*>(h);
     tl_mapped.dev = static_cast<double*>(d);
   }
@@ -259,6 +261,23 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, cu
   return ICPNN_OK;
 }
 
+// Wait until the pass with sequence number `seq` has published its result in
+// mapped memory.  Bounded: the stream is queried every few thousand polls, so
+// a failed or finished kernel ends the wait.
+int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s) {
+  for (uint64_t spins = 1;; ++spins) {
+    if (*flag == seq) return ICPNN_OK;
+    if ((spins & 4095u) == 0) {
+      const cudaError_t e = cudaStreamQuery(s);
+      if (e == cudaSuccess) {
+        if (*flag == seq) return ICPNN_OK;
+        return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
+      }
+      if (e != cudaErrorNotReady) return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
+    }
+  }
+}
+
 int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, float* d2,
              cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m, float* ms) {
   IcpPassParams p;
@@ -267,17 +286,24 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
   std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
   std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
   p.max_d2 = ps.max_d2;
+  p.seq = ++ps.mb->seq;
   if (ev0) ICPNN_CUDA(cudaEventRecord(ev0, s));
   ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev,
                              idx, d2, ps.grid, s));
   if (ev1) ICPNN_CUDA(cudaEventRecord(ev1, s));
-  ICPNN_CUDA(cudaStreamSynchronize(s));
+  const volatile unsigned long long* flag =
+      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
+  if (int rc = wait_published(flag, p.seq, s)) return rc;
+  std::atomic_thread_fence(std::memory_order_acquire);
   if (ms != nullptr) {
     *ms = 0.f;
-    if (ev0 && ev1) ICPNN_CUDA(cudaEventElapsedTime(ms, ev0, ev1));
+    if (ev0 && ev1) {
+      ICPNN_CUDA(cudaEventSynchronize(ev1));
+      ICPNN_CUDA(cudaEventElapsedTime(ms, ev0, ev1));
+    }
   }
   double raw[kMomentSlots];
-  std::memcpy(raw, ps.mb->host, sizeof(raw));
+  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
   decode_moments(raw, ps.src.shift, ps.shift_q, m);
   return ICPNN_OK;
 }

@@ -1,8 +1,11 @@
 // Host KD-tree build ("Implementing ICP with CUDA-KDTree", sections 2.2, 2.3,
 // 4.2, 5.1, 5.2): split on the axis of largest variance at the median, stop at
-// leaf_size points or at the depth cap, partition in place with nth_element
-// into one index array reserved up front.  Subtrees near the root are built
-// on separate threads; the result does not depend on the threading.
+// leaf_size points or at the depth cap, partition in place with nth_element.
+// The array partitioned is the 16-byte point records themselves (x, y, z,
+// original index), reserved once up front: every pass over a node reads
+// memory sequentially, and when the build ends the array is already the
+// leaf-ordered record array the device search reads.  Subtrees near the root
+// are built on separate threads; the result does not depend on the threading.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -17,33 +20,44 @@
 namespace icpnn {
 namespace {
 
+struct Rec {
+  float c[3];
+  int32_t idx;
+};
+static_assert(sizeof(Rec) == 16, "record must match the device float4 layout");
+
 struct Builder {
-  const float* xyz = nullptr;
   int32_t leaf_size = 0;
   int32_t max_depth = 0;
-  int32_t* order = nullptr;  // point indices, partitioned in place
+  Rec* recs = nullptr;  // point records, partitioned in place
   Node* heap = nullptr;
   int parallel_depth = 0;
   std::atomic<int64_t> n_nodes{0};
 
-  float coord(int32_t p, int d) const { return xyz[3 * static_cast<int64_t>(p) + d]; }
-
   // Axis of largest population variance; axes within a relative 1e-9 of the
   // largest are tied and the lowest of them wins.
   int split_axis(int64_t lo, int64_t hi) const {
+    // two passes (mean, then squared deviations) with the three axes fused;
+    // each axis still sums its terms in index-array order
     const double cnt = static_cast<double>(hi - lo);
-    double var[3];
-    for (int d = 0; d < 3; ++d) {
-      double sum = 0.0;
-      for (int64_t i = lo; i < hi; ++i) sum += coord(order[i], d);
-      const double mean = sum / cnt;
-      double ss = 0.0;
-      for (int64_t i = lo; i < hi; ++i) {
-        const double e = coord(order[i], d) - mean;
-        ss += e * e;
-      }
-      var[d] = ss / cnt;
+    double sum[3] = {0.0, 0.0, 0.0};
+    for (int64_t i = lo; i < hi; ++i) {
+      const float* p = recs[i].c;
+      sum[0] += p[0];
+      sum[1] += p[1];
+      sum[2] += p[2];
     }
+    const double mean[3] = {sum[0] / cnt, sum[1] / cnt, sum[2] / cnt};
+    double ss[3] = {0.0, 0.0, 0.0};
+    for (int64_t i = lo; i < hi; ++i) {
+      const float* p = recs[i].c;
+      for (int d = 0; d < 3; ++d) {
+        const double e = p[d] - mean[d];
+        ss[d] += e * e;
+      }
+    }
+    double var[3];
+    for (int d = 0; d < 3; ++d) var[d] = ss[d] / cnt;
     const double vmax = std::max(var[0], std::max(var[1], var[2]));
     for (int d = 0; d < 3; ++d)
       if (var[d] >= vmax * (1.0 - 1e-9)) return d;
@@ -60,16 +74,15 @@ struct Builder {
     }
     const int axis = split_axis(lo, hi);
     const int64_t m = count / 2;
-    std::nth_element(order + lo, order + lo + m, order + hi, [this, axis](int32_t a, int32_t b) {
-      const float fa = coord(a, axis), fb = coord(b, axis);
-      return fa < fb || (fa == fb && a < b);
+    std::nth_element(recs + lo, recs + lo + m, recs + hi, [axis](const Rec& a, const Rec& b) {
+      return a.c[axis] < b.c[axis] || (a.c[axis] == b.c[axis] && a.idx < b.idx);
     });
-    const float split = coord(order[lo + m], axis);
+    const float split = recs[lo + m].c[axis];
     uint32_t bits;
     std::memcpy(&bits, &split, sizeof(bits));
     heap[node].a = bits;
     heap[node].meta = static_cast<uint32_t>(axis);
-    if (depth < parallel_depth && count >= (1 << 16)) {
+    if (depth < parallel_depth && count >= (1 << 13)) {
       std::future<void> left;
       try {
         left = std::async(std::launch::async, [=] { build(2 * node, lo, lo + m, depth + 1); });
@@ -118,39 +131,35 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     t->depth = depth;
     t->heap_slots = int64_t{1} << (depth + 1);
     t->nodes.assign(static_cast<size_t>(t->heap_slots), Node{0u, 0u});
-    std::vector<int32_t> order(static_cast<size_t>(n));
-    for (int64_t i = 0; i < n; ++i) order[static_cast<size_t>(i)] = static_cast<int32_t>(i);
-
-    Builder b;
-    b.xyz = xyz;
-    b.leaf_size = leaf_size;
-    b.max_depth = max_depth;
-    b.order = order.data();
-    b.heap = t->nodes.data();
-    const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
-    int pd = 0;
-    while ((1u << pd) < hw && pd < 6) ++pd;
-    b.parallel_depth = pd;
-    b.build(1, 0, n, 0);
-    t->n_nodes = b.n_nodes.load();
-
     t->records.resize(static_cast<size_t>(4 * n));
+    Rec* recs = reinterpret_cast<Rec*>(t->records.data());
     float lo[3] = {INFINITY, INFINITY, INFINITY};
     float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
-    for (int64_t k = 0; k < n; ++k) {
-      const int32_t p = order[static_cast<size_t>(k)];
-      float* r = &t->records[static_cast<size_t>(4 * k)];
+    for (int64_t i = 0; i < n; ++i) {
       for (int d = 0; d < 3; ++d) {
-        r[d] = xyz[3 * static_cast<int64_t>(p) + d];
-        lo[d] = std::min(lo[d], r[d]);
-        hi[d] = std::max(hi[d], r[d]);
+        const float v = xyz[3 * i + d];
+        recs[i].c[d] = v;
+        lo[d] = std::min(lo[d], v);
+        hi[d] = std::max(hi[d], v);
       }
-      std::memcpy(&r[3], &p, sizeof(float));
+      recs[i].idx = static_cast<int32_t>(i);
     }
     for (int d = 0; d < 3; ++d) {
       t->bbox_lo[d] = lo[d];
       t->bbox_hi[d] = hi[d];
     }
+
+    Builder b;
+    b.leaf_size = leaf_size;
+    b.max_depth = max_depth;
+    b.recs = recs;
+    b.heap = t->nodes.data();
+    const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
+    int pd = 0;
+    while ((1u << pd) < 4 * hw && pd < 8) ++pd;
+    b.parallel_depth = pd;
+    b.build(1, 0, n, 0);
+    t->n_nodes = b.n_nodes.load();
   } catch (const std::bad_alloc&) {
     return fail(ICPNN_ERR_NO_MEMORY, "kdtree_build: host allocation failed");
   }

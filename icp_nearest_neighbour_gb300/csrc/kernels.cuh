@@ -25,6 +25,7 @@ struct IcpPassParams {
   float shift_s[3];   // c_s
   float shift_q[3];   // c_q
   float max_d2;       // accept iff d2 <= max_d2 (float threshold equivalent to the double test)
+  unsigned long long seq;  // published after the result, see launch_icp_pass
 };
 
 // Bounding box of n points as order-preserving int encodings
@@ -55,7 +56,10 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
 
 // One fused ICP pass: transform, search, reject, reduce.  `partials` holds
 // grid * kMomentSlots doubles, `counter` one zeroed word (left zeroed), `out`
-// kMomentSlots doubles (may be host-mapped).  idx/dist2 optional.
+// kMomentSlots doubles followed by one 64-bit word (may be host-mapped): once
+// the result is complete and visible system-wide the kernel stores p.seq in
+// that word, so the host can poll it instead of synchronising the stream.
+// idx/dist2 optional.
 int icp_pass_grid(const icpnn_tree& t, int64_t n);
 cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
