@@ -47,6 +47,12 @@ WORKLOAD = ("scene 100k<->100k: ground plane 40x40 m + 20 boxes + 10 cylinders, 
 # (35.85 nodes, 101.24 points per query).
 ICP_BYTES_PER_QUERY = 1922.64
 
+# DRAM bytes (read + write) per launch of icp_pass_kernel on this workload,
+# from ncu captures of the current kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum): 3.18 MB on the first pass, 3.48 MB on a converged
+# pass.  Set to None whenever the kernel changes until it is measured again.
+ICP_PASS_DRAM_BYTES = 3.33e6
+
 SLOWDOWN_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -261,7 +267,8 @@ def run_ours(args):
             "bound": "hbm", "kernel": "icp_pass_kernel",
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": peak_src,
-            "traffic": None,
+            "traffic": ICP_PASS_DRAM_BYTES,
+            "algorithmic_bytes_per_launch": ICP_BYTES_PER_QUERY * n,
             "bytes_per_query": ICP_BYTES_PER_QUERY,
             "avg_kernel_us": avg_kernel_s * 1e6,
         },

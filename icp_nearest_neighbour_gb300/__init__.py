@@ -225,8 +225,13 @@ def kdtree_export(tree: KDTree) -> dict:
 
 # ---------------------------------------------------------------- query / ICP
 
-def nn_query(tree: KDTree, xyz, idx, dist2, flags: int = MORTON_SORT, stream=None):
-    """Fill idx (int32, n) and dist2 (float32, n) with each query's exact nearest target point."""
+def nn_query(tree: KDTree, xyz, idx, dist2, flags: int = 0, stream=None):
+    """Fill idx (int32, n) and dist2 (float32, n) with each query's exact nearest target point.
+
+    flags=MORTON_SORT reorders the queries along a Morton curve first; the
+    results are the same.  The sort costs about as much as it saves for a
+    one-shot query of up to ~1M incoherent points; icp_align always sorts its
+    source once and reuses the order in every pass."""
     n = int(xyz.shape[0])
     _check(load().icpnn_nn_query(tree.handle, _ptr(xyz, np.float32, 3, "xyz"), n,
                                  _ptr(idx, np.int32, None, "idx"), _ptr(dist2, np.float32, None, "dist2"),

@@ -160,7 +160,10 @@ int prepare_source(const float* xyz, int64_t n, bool morton, bool want_shift, cu
     ICPNN_CUDA(sc.alloc(&vals2, n));
     ICPNN_CUDA(sc.alloc(&temp, radix_temp_words(n)));
     ICPNN_CUDA(launch_morton(d_xyz, n, bbox6, keys, vals, s));
-    ICPNN_CUDA(radix_sort(keys, vals, keys2, vals2, temp, n, 30, s, &sorted));
+    // bits 6..29 of the 30-bit code: cells of 1/256 of the box per axis,
+    // ample for warp coherence, in three 8-bit passes (stable, so points of
+    // one cell keep their input order)
+    ICPNN_CUDA(radix_sort(keys, vals, keys2, vals2, temp, n, 6, 30, s, &sorted));
     perm = sorted;
   }
   ICPNN_CUDA(launch_gather(d_xyz, n, perm, out->recs, s));

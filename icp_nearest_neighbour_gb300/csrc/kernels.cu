@@ -156,18 +156,19 @@ __global__ void __launch_bounds__(kThreads) morton_kernel(const float* __restric
 }
 
 // ------------------------------------------------------- radix sort -----
-// One 8-bit digit per pass.  Pass = per-tile digit histogram, one exclusive
-// scan over the (digit, tile) matrix in digit-major order, stable scatter.
-// The scatter is stable because ranks follow (round, warp, lane) = position
-// order: a key's destination is its tile's base for the digit, plus the
-// counts of earlier rounds, earlier warps of this round, and earlier lanes of
-// its warp (from __match_any_sync).
+// One 8-bit digit per pass.  A pass is: per-tile digit histogram
+// (hist[digit][tile]); an exclusive scan of every digit's row of tile counts,
+// one block per digit, which also leaves each digit's total; a stable scatter
+// whose blocks first turn the 256 digit totals into digit offsets.  The
+// scatter is stable because ranks follow (round, warp, lane) = position
+// order: a key's destination is its digit's offset, plus its tile's prefix
+// for the digit, plus the counts of earlier rounds, earlier warps of this
+// round, and earlier lanes of its warp (from __match_any_sync).
 
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kSortItems = 8;
 constexpr int kSortTile = kThreads * kSortItems;
-constexpr int kScanThreads = 1024;
 
 __global__ void __launch_bounds__(kThreads) radix_hist_kernel(const uint32_t* __restrict__ keys, int64_t n,
                                                               int shift, uint32_t* __restrict__ hist,
@@ -186,52 +187,62 @@ __global__ void __launch_bounds__(kThreads) radix_hist_kernel(const uint32_t* __
     hist[static_cast<int64_t>(i) * tiles + blockIdx.x] = cnt[i];
 }
 
-// Exclusive prefix sum of m words in place, one block.
-__global__ void __launch_bounds__(kScanThreads) exclusive_scan_kernel(uint32_t* __restrict__ data, int64_t m) {
-  __shared__ uint32_t warp_sums[kScanThreads / 32];
-  const int t = threadIdx.x;
-  const int64_t chunk = (m + kScanThreads - 1) / kScanThreads;
-  const int64_t beg = t * chunk;
-  const int64_t end = min(m, beg + chunk);
-  uint32_t local = 0;
-  for (int64_t i = beg; i < end; ++i) local += data[i];
-  // inclusive scan of the per-thread sums
-  const int lane = t & 31, warp = t >> 5;
-  uint32_t v = local;
+// Exclusive scan of the block's values (one per thread, blockDim.x == kThreads).
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t u = __shfl_up_sync(kFull, v, off);
-    if (lane >= off) v += u;
+    const uint32_t u = __shfl_up_sync(kFull, x, off);
+    if (lane >= off) x += u;
   }
-  if (lane == 31) warp_sums[warp] = v;
+  if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = warp_sums[lane];
+    uint32_t w = lane < kThreads / 32 ? warp_sums[lane] : 0u;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const uint32_t u = __shfl_up_sync(kFull, w, off);
       if (lane >= off) w += u;
     }
-    warp_sums[lane] = w;
+    if (lane < kThreads / 32) warp_sums[lane] = w;
   }
   __syncthreads();
-  uint32_t run = v - local + (warp > 0 ? warp_sums[warp - 1] : 0u);
-  for (int64_t i = beg; i < end; ++i) {
-    const uint32_t x = data[i];
-    data[i] = run;
-    run += x;
+  const uint32_t excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0u);
+  if (total != nullptr) *total = warp_sums[kThreads / 32 - 1];
+  __syncthreads();
+  return excl;
+}
+
+// Block d: exclusive scan of hist[d][0..tiles) in place; digit_total[d] = row sum.
+__global__ void __launch_bounds__(kThreads) digit_row_scan_kernel(uint32_t* __restrict__ hist, int tiles,
+                                                                  uint32_t* __restrict__ digit_total) {
+  __shared__ uint32_t warp_sums[kThreads / 32];
+  uint32_t* row = hist + static_cast<int64_t>(blockIdx.x) * tiles;
+  uint32_t carry = 0;
+  for (int base = 0; base < tiles; base += kThreads) {
+    const int i = base + threadIdx.x;
+    const uint32_t v = i < tiles ? row[i] : 0u;
+    uint32_t chunk_total;
+    const uint32_t excl = block_exclusive_scan(v, warp_sums, &chunk_total);
+    if (i < tiles) row[i] = carry + excl;
+    carry += chunk_total;
   }
+  if (threadIdx.x == 0) digit_total[blockIdx.x] = carry;
 }
 
 __global__ void __launch_bounds__(kThreads) radix_scatter_kernel(
     const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in,
     uint32_t* __restrict__ keys_out, uint32_t* __restrict__ vals_out, int64_t n, int shift,
-    const uint32_t* __restrict__ offsets, int tiles) {
+    const uint32_t* __restrict__ row_prefix, const uint32_t* __restrict__ digit_total, int tiles) {
+  static_assert(kThreads == kRadix, "one thread per digit when forming offsets");
   constexpr int kWarps = kThreads / 32;
   __shared__ uint32_t base[kRadix];
   __shared__ uint32_t wcount[kWarps][kRadix];
+  __shared__ uint32_t warp_sums[kWarps];
   const int t = threadIdx.x, warp = t >> 5;
-  for (int i = t; i < kRadix; i += kThreads) base[i] = offsets[static_cast<int64_t>(i) * tiles + blockIdx.x];
+  const uint32_t digit_offset = block_exclusive_scan(digit_total[t], warp_sums, nullptr);
+  base[t] = digit_offset + row_prefix[static_cast<int64_t>(t) * tiles + blockIdx.x];
   const int64_t tile0 = static_cast<int64_t>(blockIdx.x) * kSortTile;
   for (int r = 0; r < kSortItems; ++r) {
     for (int i = t; i < kWarps * kRadix; i += kThreads) (&wcount[0][0])[i] = 0;
@@ -252,12 +263,10 @@ __global__ void __launch_bounds__(kThreads) radix_scatter_kernel(
       vals_out[off] = val;
     }
     __syncthreads();
-    for (int i = t; i < kRadix; i += kThreads) {
-      uint32_t s = 0;
+    uint32_t sum = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += wcount[w][i];
-      base[i] += s;
-    }
+    for (int w = 0; w < kWarps; ++w) sum += wcount[w][t];
+    base[t] += sum;
     __syncthreads();
   }
 }
@@ -581,19 +590,22 @@ cudaError_t launch_morton(const float* xyz, int64_t n, const int32_t* bbox6, uin
 
 int64_t radix_temp_words(int64_t n) {
   const int64_t tiles = (n + kSortTile - 1) / kSortTile;
-  return std::max<int64_t>(1, tiles) * kRadix;
+  return std::max<int64_t>(1, tiles) * kRadix + kRadix;
 }
 
 cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
-                       uint32_t* temp, int64_t n, int bits, cudaStream_t s, uint32_t** sorted_vals) {
+                       uint32_t* temp, int64_t n, int lo_bit, int hi_bit, cudaStream_t s,
+                       uint32_t** sorted_vals) {
   *sorted_vals = vals;
   if (n <= 1) return cudaSuccess;
   const int tiles = static_cast<int>((n + kSortTile - 1) / kSortTile);
+  uint32_t* hist = temp;
+  uint32_t* digit_total = temp + static_cast<int64_t>(tiles) * kRadix;
   uint32_t *ki = keys, *vi = vals, *ko = keys_alt, *vo = vals_alt;
-  for (int shift = 0; shift < bits; shift += kRadixBits) {
-    radix_hist_kernel<<<tiles, kThreads, 0, s>>>(ki, n, shift, temp, tiles);
-    exclusive_scan_kernel<<<1, kScanThreads, 0, s>>>(temp, static_cast<int64_t>(tiles) * kRadix);
-    radix_scatter_kernel<<<tiles, kThreads, 0, s>>>(ki, vi, ko, vo, n, shift, temp, tiles);
+  for (int shift = lo_bit; shift < hi_bit; shift += kRadixBits) {
+    radix_hist_kernel<<<tiles, kThreads, 0, s>>>(ki, n, shift, hist, tiles);
+    digit_row_scan_kernel<<<kRadix, kThreads, 0, s>>>(hist, tiles, digit_total);
+    radix_scatter_kernel<<<tiles, kThreads, 0, s>>>(ki, vi, ko, vo, n, shift, hist, digit_total, tiles);
     g_launch_count.fetch_add(3, std::memory_order_relaxed);
     std::swap(ki, ko);
     std::swap(vi, vo);

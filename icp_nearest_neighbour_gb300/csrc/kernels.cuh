@@ -37,13 +37,13 @@ void decode_bbox(const int32_t bbox6[6], float lo[3], float hi[3]);
 cudaError_t launch_morton(const float* xyz, int64_t n, const int32_t* bbox6, uint32_t* keys,
                           uint32_t* vals, cudaStream_t s);
 
-// Stable LSD radix sort of (key, value) pairs on the low `bits` key bits.
-// Buffers: keys/vals (input), keys_alt/vals_alt (same size), temp of
-// radix_temp_words(n) words.  *sorted_vals receives whichever value buffer
-// holds the result.
+// Stable LSD radix sort of (key, value) pairs on key bits [lo_bit, hi_bit)
+// (8 bits per pass).  Buffers: keys/vals (input), keys_alt/vals_alt (same
+// size), temp of radix_temp_words(n) words.  *sorted_vals receives whichever
+// value buffer holds the result.
 int64_t radix_temp_words(int64_t n);
 cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
-                       uint32_t* temp, int64_t n, int bits, cudaStream_t s,
+                       uint32_t* temp, int64_t n, int lo_bit, int hi_bit, cudaStream_t s,
                        uint32_t** sorted_vals);
 
 // records[i] = (xyz[perm[i]], perm[i]) as float4; perm == nullptr -> identity.
