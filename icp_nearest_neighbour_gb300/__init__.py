@@ -23,11 +23,12 @@ __all__ = [
     "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
     "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
     "kabsch", "icp_align",
-    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "MAX_DEPTH", "NOALLOC_MAX_POINTS",
+    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "MAX_DEPTH", "NOALLOC_MAX_POINTS",
 ]
 
 MORTON_SORT = 1
 TRACE_TIMING = 2
+RESIDUAL_REJECT = 4
 MAX_DEPTH = 20
 NOALLOC_MAX_POINTS = 1 << 20
 
@@ -57,8 +58,8 @@ class Moments(ctypes.Structure):
 
 class IterRecord(ctypes.Structure):
     _fields_ = [("iter", ctypes.c_int32), ("flags", ctypes.c_int32), ("n_accepted", ctypes.c_int64),
-                ("mse", ctypes.c_double), ("T", ctypes.c_double * 16), ("kernel_ms", ctypes.c_float),
-                ("reserved", ctypes.c_float)]
+                ("n_inliers", ctypes.c_int64), ("mse", ctypes.c_double), ("sigma2", ctypes.c_double),
+                ("T", ctypes.c_double * 16), ("kernel_ms", ctypes.c_float), ("reserved", ctypes.c_float)]
 
 
 _lib = None
@@ -280,8 +281,10 @@ def kabsch(moments: dict) -> np.ndarray:
 
 
 def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
-              init_T=None, trace: bool = False, timing: bool = False, stream=None) -> dict:
-    """Register src onto the tree's points; returns dict(T, final_mse, iters, trace)."""
+              init_T=None, trace: bool = False, timing: bool = False, residual_reject: bool = False,
+              stream=None) -> dict:
+    """Register src onto the tree's points; returns dict(T, final_mse, iters, trace).
+    residual_reject adds the 3-sigma residual rejection and re-solve to every iteration."""
     T = np.zeros(16)
     fmse = ctypes.c_double()
     iters = ctypes.c_int32()
@@ -291,7 +294,7 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
         init = ctypes.c_void_p(init_arr.ctypes.data)
     cap = int(max_iter) if (trace or timing) else 0
     recs = (IterRecord * max(cap, 1))()
-    flags = TRACE_TIMING if timing else 0
+    flags = (TRACE_TIMING if timing else 0) | (RESIDUAL_REJECT if residual_reject else 0)
     _check(load().icpnn_icp_align(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
                                   int(max_iter), float(eps), float(max_corr_dist), init,
                                   ctypes.c_void_p(T.ctypes.data), ctypes.byref(fmse), ctypes.byref(iters),
@@ -299,7 +302,8 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
                                   _stream(stream)))
     out = {"T": T.reshape(4, 4), "final_mse": fmse.value, "iters": iters.value}
     if cap:
-        out["trace"] = [{"iter": r.iter, "n_accepted": r.n_accepted, "mse": r.mse,
-                         "T": np.array(r.T[:]).reshape(4, 4), "kernel_ms": r.kernel_ms}
+        out["trace"] = [{"iter": r.iter, "n_accepted": r.n_accepted, "n_inliers": r.n_inliers,
+                         "mse": r.mse, "sigma2": r.sigma2, "T": np.array(r.T[:]).reshape(4, 4),
+                         "kernel_ms": r.kernel_ms}
                         for r in recs[:min(iters.value, cap)]]
     return out

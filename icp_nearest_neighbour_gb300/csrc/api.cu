@@ -117,15 +117,20 @@ int check_tree_on_device(const icpnn_tree* t) {
 }
 
 // Largest float f such that, for every float d, d <= f exactly when
-// double(d) <= dmax^2.  No rejection -> +inf.
+// double(d) <= limit (limit >= 0; +inf -> +inf).
+float float_threshold(double limit) {
+  if (std::isinf(limit)) return INFINITY;
+  if (limit >= static_cast<double>(FLT_MAX)) return FLT_MAX;
+  float f = static_cast<float>(limit);
+  if (static_cast<double>(f) > limit) f = std::nextafter(f, -INFINITY);
+  return f;
+}
+
+// Threshold for the maximum-correspondence-distance test: accept iff
+// double(d2) <= dmax^2.  No rejection (dmax <= 0 or infinite) -> +inf.
 float rejection_threshold(double dmax) {
   if (!(dmax > 0.0) || std::isinf(dmax)) return INFINITY;
-  const double d2 = dmax * dmax;
-  if (std::isinf(d2)) return INFINITY;
-  if (d2 >= static_cast<double>(FLT_MAX)) return FLT_MAX;
-  float f = static_cast<float>(d2);
-  if (static_cast<double>(f) > d2) f = std::nextafter(f, -INFINITY);
-  return f;
+  return float_threshold(dmax * dmax);
 }
 
 // The source in Morton order as float4 records, plus the float32 centre of
@@ -245,14 +250,16 @@ struct Pass {
   double* partials = nullptr;
   uint32_t* counter = nullptr;
   MappedBuffer* mb = nullptr;
+  int32_t* slot_of = nullptr;  // per Morton-ordered source record: matched slot or -1
   float shift_q[3] = {0, 0, 0};
   float max_d2 = INFINITY;
 };
 
-int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, cudaStream_t s,
-               Scratch& sc, Pass* ps) {
+int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bool want_slots,
+               cudaStream_t s, Scratch& sc, Pass* ps) {
   ps->tree = t;
   ps->n = n;
+  if (want_slots) ICPNN_CUDA(sc.alloc(&ps->slot_of, n));
   if (int rc = prepare_source(src, n, true, true, s, sc, &ps->src)) return rc;
   ps->grid = icp_pass_grid(*t, n);
   ICPNN_CUDA(sc.alloc(&ps->partials, static_cast<int64_t>(ps->grid) * kMomentSlots));
@@ -292,7 +299,7 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
   p.seq = ++ps.mb->seq;
   if (ev0) ICPNN_CUDA(cudaEventRecord(ev0, s));
   ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev,
-                             idx, d2, ps.grid, s));
+                             idx, d2, ps.slot_of, ps.grid, s));
   if (ev1) ICPNN_CUDA(cudaEventRecord(ev1, s));
   const volatile unsigned long long* flag =
       reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
@@ -308,6 +315,35 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
   double raw[kMomentSlots];
   std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
   decode_moments(raw, ps.src.shift, ps.shift_q, m);
+  return ICPNN_OK;
+}
+
+// One residual pass (see launch_residual_pass) under float32 (R, t): returns
+// the number of matched pairs, the sum of their squared residuals, and the
+// moments of the pairs with e2 <= thr.
+int residual_run(const Pass& ps, const float R[9], const float tr[3], float thr, cudaStream_t s,
+                 double* pairs, double* sum_e2, icpnn_moments* kept) {
+  IcpPassParams p;
+  std::memcpy(p.R, R, sizeof(p.R));
+  std::memcpy(p.t, tr, sizeof(p.t));
+  std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
+  std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
+  p.max_d2 = thr;
+  p.seq = ++ps.mb->seq;
+  ICPNN_CUDA(launch_residual_pass(*ps.tree, ps.src.recs, ps.slot_of, ps.n, p, ps.partials, ps.counter,
+                                  ps.mb->dev, ps.grid, s));
+  const volatile unsigned long long* flag =
+      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
+  if (int rc = wait_published(flag, p.seq, s)) return rc;
+  std::atomic_thread_fence(std::memory_order_acquire);
+  double raw[kMomentSlots];
+  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
+  *pairs = raw[1];
+  *sum_e2 = raw[17];
+  decode_moments(raw, ps.src.shift, ps.shift_q, kept);
+  kept->n_nonfinite = 0;
+  kept->sum_d2 = 0.0;
+  kept->mse = NAN;
   return ICPNN_OK;
 }
 
@@ -501,7 +537,7 @@ int icpnn_icp_step(const icpnn_tree* t, const float* src, int64_t n, const float
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Scratch sc(s);
   Pass ps;
-  if (int rc = pass_setup(t, src, n, max_corr_dist, s, sc, &ps)) return rc;
+  if (int rc = pass_setup(t, src, n, max_corr_dist, false, s, sc, &ps)) return rc;
   PointOutputs po;
   if (int rc = bind_point_outputs(idx, dist2, n, sc, &po)) return rc;
   if (int rc = pass_run(ps, R, tr, po.idx, po.d2, s, nullptr, nullptr, out, nullptr)) return rc;
@@ -588,7 +624,9 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: max_corr_dist is NaN");
   if (trace_cap < 0 || (trace_cap > 0 && trace == nullptr))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_align: bad trace buffer");
-  if (flags & ~ICPNN_TRACE_TIMING) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: unknown flag");
+  if (flags & ~(ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_align: unknown flag");
+  const bool residual = (flags & ICPNN_RESIDUAL_REJECT) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   double T[16];
@@ -604,7 +642,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   }
   Scratch sc(s);
   Pass ps;
-  if (int rc = pass_setup(t, src, n_src, max_corr_dist, s, sc, &ps)) return rc;
+  if (int rc = pass_setup(t, src, n_src, max_corr_dist, residual, s, sc, &ps)) return rc;
 
   double mse_hist[3] = {0, 0, 0};
   int32_t done = 0;
@@ -620,20 +658,39 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     if (m.n_accepted < 3)
       return fail(ICPNN_ERR_DEGENERATE, "icp_align: fewer than 3 correspondences accepted at iteration " +
                                             std::to_string(k));
+    double Tn[16];
+    if (kabsch_solve(m, Tn) != ICPNN_OK)
+      return fail(ICPNN_ERR_DEGENERATE, "icp_align: rank-deficient cross-covariance at iteration " +
+                                            std::to_string(k));
+    int64_t n_inliers = m.n_accepted;
+    double sigma2 = 0.0;
+    if (residual) {
+      // page section 4.4: residuals under the first solve, 3-sigma rule, re-solve
+      float R1[9], t1[3];
+      transform_to_f32(Tn, R1, t1);
+      double pairs = 0.0, sum_e2 = 0.0;
+      icpnn_moments kept;
+      if (int rc = residual_run(ps, R1, t1, INFINITY, s, &pairs, &sum_e2, &kept)) return rc;
+      sigma2 = pairs > 0.0 ? sum_e2 / pairs : 0.0;
+      if (int rc = residual_run(ps, R1, t1, float_threshold(9.0 * sigma2), s, &pairs, &sum_e2, &kept))
+        return rc;
+      n_inliers = kept.n_accepted;
+      if (n_inliers < 3 || kabsch_solve(kept, Tn) != ICPNN_OK)
+        return fail(ICPNN_ERR_DEGENERATE, "icp_align: residual rejection left a degenerate pair set at "
+                                          "iteration " + std::to_string(k));
+    }
     if (k < trace_cap) {
       icpnn_iter_record& r = trace[k];
       r.iter = k;
       r.flags = 0;
       r.n_accepted = m.n_accepted;
+      r.n_inliers = n_inliers;
       r.mse = m.mse;
+      r.sigma2 = sigma2;
       std::memcpy(r.T, T, sizeof(T));
       r.kernel_ms = ms;
       r.reserved = 0.f;
     }
-    double Tn[16];
-    if (kabsch_solve(m, Tn) != ICPNN_OK)
-      return fail(ICPNN_ERR_DEGENERATE, "icp_align: rank-deficient cross-covariance at iteration " +
-                                            std::to_string(k));
     std::memcpy(T, Tn, sizeof(T));
     mse_hist[0] = mse_hist[1];
     mse_hist[1] = mse_hist[2];

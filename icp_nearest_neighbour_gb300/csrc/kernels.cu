@@ -39,7 +39,6 @@ std::atomic<int64_t> g_launch_count{0};
 
 namespace {
 
-constexpr int kStack = ICPNN_MAX_DEPTH + 1;  // at most one pending far child per level
 constexpr int kThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -429,92 +428,35 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
 
 // ------------------------------------------------------------ ICP pass --
 
-template <bool kPerPoint>
-__global__ void __launch_bounds__(kThreads) icp_pass_kernel(
-    const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
-    const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
-    unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
-    float* __restrict__ out_d2) {
-  extern __shared__ uint2 s_nodes[];
+// Reduction of the per-thread moments of a pass, in a fixed order: warp
+// butterfly in float (lane 0's association order is the same every run),
+// warps of a block in order in double, then the last block to finish sums
+// the block partials in block order.  out[0] = c0, out[1] = c1 (counts),
+// out[2 + v] = acc[v].  With kPublish the last block then publishes `seq`
+// in the word after the result, once the result is visible system-wide.
+template <bool kPublish>
+__device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
+                                               double* __restrict__ partials,
+                                               unsigned int* __restrict__ counter, double* out,
+                                               unsigned long long seq) {
   __shared__ double s_warp[kThreads / 32][kMomentSlots];
   __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
   __shared__ bool s_last;
-  stage_top(nodes, s_nodes, smem_slots);
-  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
-
-  float acc[16];
-#pragma unroll
-  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
-  uint32_t n_acc = 0, n_bad = 0;
-
-  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
-    const int64_t i = c * 32 + (threadIdx.x & 31);
-    if (i >= n) continue;
-    const float4 s = src[i];
-    const int32_t slot = __float_as_int(s.w);
-    int32_t idx = -1;
-    float d2 = __int_as_float(0x7fc00000);
-    if (!finite3(s.x, s.y, s.z)) {
-      ++n_bad;
-    } else {
-      // p = R s + t, each row ((R_a0 s_x + R_a1 s_y) + R_a2 s_z) + t_a
-      float q[3];
-#pragma unroll
-      for (int a = 0; a < 3; ++a) {
-        float v = __fadd_rn(__fmul_rn(p.R[3 * a], s.x), __fmul_rn(p.R[3 * a + 1], s.y));
-        v = __fadd_rn(v, __fmul_rn(p.R[3 * a + 2], s.z));
-        q[a] = __fadd_rn(v, p.t[a]);
-      }
-      if (finite3(q[0], q[1], q[2])) {
-        // Without per-point outputs only accepted pairs matter, so the search
-        // starts with the rejection radius as its best distance (the page's
-        // section 4.4 fuses max_dist into the tree query): it returns the
-        // exact nearest point when one lies within the radius, else nothing.
-        Best b{kPerPoint ? __int_as_float(0x7f800000) : p.max_d2, INT_MAX, 0u};
-        search(tv, q[0], q[1], q[2], b);
-        idx = b.idx == INT_MAX ? -1 : b.idx;
-        d2 = b.d2;
-        if (b.idx != INT_MAX && b.d2 <= p.max_d2) {
-          ++n_acc;
-          const float ds[3] = {__fsub_rn(s.x, p.shift_s[0]), __fsub_rn(s.y, p.shift_s[1]),
-                               __fsub_rn(s.z, p.shift_s[2])};
-          const float4 qr = __ldg(&pts[b.slot]);
-          const float dq[3] = {__fsub_rn(qr.x, p.shift_q[0]), __fsub_rn(qr.y, p.shift_q[1]),
-                               __fsub_rn(qr.z, p.shift_q[2])};
-#pragma unroll
-          for (int a = 0; a < 3; ++a) {
-            acc[a] = __fadd_rn(acc[a], ds[a]);
-            acc[3 + a] = __fadd_rn(acc[3 + a], dq[a]);
-#pragma unroll
-            for (int c = 0; c < 3; ++c) acc[6 + 3 * a + c] = __fadd_rn(acc[6 + 3 * a + c], __fmul_rn(ds[a], dq[c]));
-          }
-          acc[15] = __fadd_rn(acc[15], b.d2);
-        }
-      }
-    }
-    if (kPerPoint) {
-      out_idx[slot] = idx;
-      out_d2[slot] = d2;
-    }
-  }
-
-  // warp: fixed butterfly; lane 0's association order is the same every run
 #pragma unroll
   for (int v = 0; v < 16; ++v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc[v] = __fadd_rn(acc[v], __shfl_xor_sync(kFull, acc[v], off));
   }
-  n_acc = __reduce_add_sync(kFull, n_acc);
-  n_bad = __reduce_add_sync(kFull, n_bad);
+  c0 = __reduce_add_sync(kFull, c0);
+  c1 = __reduce_add_sync(kFull, c1);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
-    s_warp[warp][0] = static_cast<double>(n_acc);
-    s_warp[warp][1] = static_cast<double>(n_bad);
+    s_warp[warp][0] = static_cast<double>(c0);
+    s_warp[warp][1] = static_cast<double>(c1);
 #pragma unroll
     for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = static_cast<double>(acc[v]);
   }
   __syncthreads();
-  // block: warps in order
   if (threadIdx.x < kMomentSlots) {
     double s = 0.0;
 #pragma unroll
@@ -527,7 +469,6 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // grid: the last block to finish sums all block partials in block order
   constexpr int kGroups = kThreads / kMomentSlots;
   if (threadIdx.x < kGroups * kMomentSlots) {
     const int g = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
@@ -542,14 +483,130 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) s += s_fin[g][threadIdx.x];
     out[threadIdx.x] = s;
-    __threadfence_system();
+    if (kPublish) __threadfence_system();
   }
   if (threadIdx.x == 0) *counter = 0u;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence_system();
-    *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = p.seq;
+  if (kPublish) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence_system();
+      *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq;
+    }
   }
+}
+
+// Accumulate one accepted pair (original source s, matched target q).
+__device__ __forceinline__ void add_pair(float (&acc)[16], float sx, float sy, float sz,
+                                         const float4& qr, float d2, const IcpPassParams& p) {
+  const float ds[3] = {__fsub_rn(sx, p.shift_s[0]), __fsub_rn(sy, p.shift_s[1]),
+                       __fsub_rn(sz, p.shift_s[2])};
+  const float dq[3] = {__fsub_rn(qr.x, p.shift_q[0]), __fsub_rn(qr.y, p.shift_q[1]),
+                       __fsub_rn(qr.z, p.shift_q[2])};
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    acc[a] = __fadd_rn(acc[a], ds[a]);
+    acc[3 + a] = __fadd_rn(acc[3 + a], dq[a]);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) acc[6 + 3 * a + c] = __fadd_rn(acc[6 + 3 * a + c], __fmul_rn(ds[a], dq[c]));
+  }
+  acc[15] = __fadd_rn(acc[15], d2);
+}
+
+// p = R s + t, each row ((R_a0 s_x + R_a1 s_y) + R_a2 s_z) + t_a
+__device__ __forceinline__ void transform_point(const IcpPassParams& p, float sx, float sy, float sz,
+                                                float (&q)[3]) {
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    float v = __fadd_rn(__fmul_rn(p.R[3 * a], sx), __fmul_rn(p.R[3 * a + 1], sy));
+    v = __fadd_rn(v, __fmul_rn(p.R[3 * a + 2], sz));
+    q[a] = __fadd_rn(v, p.t[a]);
+  }
+}
+
+template <bool kPerPoint, bool kSlot>
+__global__ void __launch_bounds__(kThreads) icp_pass_kernel(
+    const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
+    const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
+    unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
+    float* __restrict__ out_d2, int32_t* __restrict__ slot_of) {
+  extern __shared__ uint2 s_nodes[];
+  stage_top(nodes, s_nodes, smem_slots);
+  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+
+  float acc[16];
+#pragma unroll
+  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+  uint32_t n_acc = 0, n_bad = 0;
+
+  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
+    const int64_t i = c * 32 + (threadIdx.x & 31);
+    if (i >= n) continue;
+    const float4 s = src[i];
+    const int32_t slot = __float_as_int(s.w);
+    int32_t idx = -1, matched = -1;
+    float d2 = __int_as_float(0x7fc00000);
+    if (!finite3(s.x, s.y, s.z)) {
+      ++n_bad;
+    } else {
+      float q[3];
+      transform_point(p, s.x, s.y, s.z, q);
+      if (finite3(q[0], q[1], q[2])) {
+        // Without per-point outputs only accepted pairs matter, so the search
+        // starts with the rejection radius as its best distance (the page's
+        // section 4.4 fuses max_dist into the tree query): it returns the
+        // exact nearest point when one lies within the radius, else nothing.
+        Best b{kPerPoint ? __int_as_float(0x7f800000) : p.max_d2, INT_MAX, 0u};
+        search(tv, q[0], q[1], q[2], b);
+        idx = b.idx == INT_MAX ? -1 : b.idx;
+        d2 = b.d2;
+        if (b.idx != INT_MAX && b.d2 <= p.max_d2) {
+          ++n_acc;
+          matched = static_cast<int32_t>(b.slot);
+          add_pair(acc, s.x, s.y, s.z, __ldg(&pts[b.slot]), b.d2, p);
+        }
+      }
+    }
+    if (kPerPoint) {
+      out_idx[slot] = idx;
+      out_d2[slot] = d2;
+    }
+    if (kSlot) slot_of[i] = matched;
+  }
+  reduce_moments<true>(acc, n_acc, n_bad, partials, counter, out, p.seq);
+}
+
+// Residual pass of the section 4.4 rejection: for every source record with a
+// match from the last correspondence pass (slot_of >= 0), the squared residual
+// e2 of the pair under the transform in p (same float arithmetic as the search
+// distance).  Counts every pair in c1 and sums its e2 in acc[15]; pairs with
+// e2 <= p.max_d2 are counted in c0 and their moments accumulated in acc[0..14].
+__global__ void __launch_bounds__(kThreads) residual_pass_kernel(
+    const float4* __restrict__ pts, const float4* __restrict__ src, const int32_t* __restrict__ slot_of,
+    int64_t n, IcpPassParams p, double* __restrict__ partials, unsigned int* __restrict__ counter,
+    double* out) {
+  float acc[16];
+#pragma unroll
+  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+  uint32_t n_keep = 0, n_pair = 0;
+  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
+    const int64_t i = c * 32 + (threadIdx.x & 31);
+    if (i >= n) continue;
+    const int32_t sl = slot_of[i];
+    if (sl < 0) continue;
+    const float4 s = src[i];
+    const float4 r = __ldg(&pts[sl]);
+    float q[3];
+    transform_point(p, s.x, s.y, s.z, q);
+    const float e2 = dist2(r, q[0], q[1], q[2]);
+    ++n_pair;
+    const float sum_e2 = __fadd_rn(acc[15], e2);
+    if (e2 <= p.max_d2) {
+      ++n_keep;
+      add_pair(acc, s.x, s.y, s.z, r, 0.f, p);
+    }
+    acc[15] = sum_e2;
+  }
+  reduce_moments<true>(acc, n_keep, n_pair, partials, counter, out, p.seq);
 }
 
 inline int smem_slots_for(const icpnn_tree& t) {
@@ -640,23 +697,40 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
 int icp_pass_grid(const icpnn_tree& t, int64_t n) {
   const size_t smem = static_cast<size_t>(smem_slots_for(t)) * sizeof(uint2);
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, icp_pass_kernel<false>, kThreads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, icp_pass_kernel<false, false>, kThreads, smem);
   return blocks_for(n, kThreads, std::max(1, per_sm) * num_sms());
 }
 
 cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
-                            double* out, int32_t* idx, float* dist2, int grid, cudaStream_t s) {
+                            double* out, int32_t* idx, float* dist2, int32_t* slot_of, int grid,
+                            cudaStream_t s) {
   const int slots = smem_slots_for(t);
   const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
   const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
-  if (idx != nullptr || dist2 != nullptr)
-    icp_pass_kernel<true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
-                                                        counter, out, idx, dist2);
+  const bool per_point = idx != nullptr || dist2 != nullptr;
+  if (per_point && slot_of != nullptr)
+    icp_pass_kernel<true, true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+                                                              counter, out, idx, dist2, slot_of);
+  else if (per_point)
+    icp_pass_kernel<true, false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+                                                               counter, out, idx, dist2, nullptr);
+  else if (slot_of != nullptr)
+    icp_pass_kernel<false, true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+                                                               counter, out, nullptr, nullptr, slot_of);
   else
-    icp_pass_kernel<false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
-                                                         counter, out, nullptr, nullptr);
+    icp_pass_kernel<false, false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+                                                                counter, out, nullptr, nullptr, nullptr);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,
+                                 int64_t n, const IcpPassParams& p, double* partials,
+                                 uint32_t* counter, double* out, int grid, cudaStream_t s) {
+  residual_pass_kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(t.dev.points), src,
+                                                 slot_of, n, p, partials, counter, out);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }
@@ -695,9 +769,6 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
     const float* __restrict__ xyz, int64_t n, IcpPassParams p, double* __restrict__ scratch,
     int32_t* __restrict__ out_idx, float* __restrict__ out_d2) {
   extern __shared__ uint2 s_nodes[];
-  __shared__ double s_warp[kThreads / 32][kMomentSlots];
-  __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
-  __shared__ bool s_last;
   double* partials = scratch;
   double* result = scratch + kNoAllocResult;
   unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kNoAllocCounter);
@@ -718,12 +789,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
       ++n_bad;
     } else {
       float q[3];
-#pragma unroll
-      for (int a = 0; a < 3; ++a) {
-        float v = __fadd_rn(__fmul_rn(p.R[3 * a], sx), __fmul_rn(p.R[3 * a + 1], sy));
-        v = __fadd_rn(v, __fmul_rn(p.R[3 * a + 2], sz));
-        q[a] = __fadd_rn(v, p.t[a]);
-      }
+      transform_point(p, sx, sy, sz, q);
       if (finite3(q[0], q[1], q[2])) {
         Best b{__int_as_float(0x7f800000), INT_MAX, 0u};
         search(tv, q[0], q[1], q[2], b);
@@ -731,19 +797,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
         d2 = b.d2;
         if (b.d2 <= p.max_d2) {
           ++n_acc;
-          const float ds[3] = {__fsub_rn(sx, p.shift_s[0]), __fsub_rn(sy, p.shift_s[1]),
-                               __fsub_rn(sz, p.shift_s[2])};
-          const float4 qr = __ldg(&pts[b.slot]);
-          const float dq[3] = {__fsub_rn(qr.x, p.shift_q[0]), __fsub_rn(qr.y, p.shift_q[1]),
-                               __fsub_rn(qr.z, p.shift_q[2])};
-#pragma unroll
-          for (int a = 0; a < 3; ++a) {
-            acc[a] = ds[a];
-            acc[3 + a] = dq[a];
-#pragma unroll
-            for (int c = 0; c < 3; ++c) acc[6 + 3 * a + c] = __fmul_rn(ds[a], dq[c]);
-          }
-          acc[15] = b.d2;
+          add_pair(acc, sx, sy, sz, __ldg(&pts[b.slot]), b.d2, p);
         }
       }
     }
@@ -752,50 +806,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
       out_d2[i] = d2;
     }
   }
-
-#pragma unroll
-  for (int v = 0; v < 16; ++v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[v] = __fadd_rn(acc[v], __shfl_xor_sync(kFull, acc[v], off));
-  }
-  n_acc = __reduce_add_sync(kFull, n_acc);
-  n_bad = __reduce_add_sync(kFull, n_bad);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) {
-    s_warp[warp][0] = static_cast<double>(n_acc);
-    s_warp[warp][1] = static_cast<double>(n_bad);
-#pragma unroll
-    for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = static_cast<double>(acc[v]);
-  }
-  __syncthreads();
-  if (threadIdx.x < kMomentSlots) {
-    double s = 0.0;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
-    partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  constexpr int kGroups = kThreads / kMomentSlots;
-  if (threadIdx.x < kGroups * kMomentSlots) {
-    const int g = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
-    double s = 0.0;
-    for (int b = g; b < static_cast<int>(gridDim.x); b += kGroups)
-      s += __ldcg(&partials[static_cast<int64_t>(b) * kMomentSlots + v]);
-    s_fin[g][v] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x < kMomentSlots) {
-    double s = 0.0;
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) s += s_fin[g][threadIdx.x];
-    result[threadIdx.x] = s;
-  }
-  if (threadIdx.x == 0) *counter = 0u;
+  reduce_moments<false>(acc, n_acc, n_bad, partials, counter, result, 0ull);
 }
 
 }  // namespace

@@ -61,9 +61,20 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
 // that word, so the host can poll it instead of synchronising the stream.
 // idx/dist2 optional.
 int icp_pass_grid(const icpnn_tree& t, int64_t n);
+// slot_of (optional): per source record, the record slot of its accepted
+// match, or -1.
 cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
-                            double* out, int32_t* idx, float* dist2, int grid, cudaStream_t s);
+                            double* out, int32_t* idx, float* dist2, int32_t* slot_of, int grid,
+                            cudaStream_t s);
+
+// Residual pass of the residual rejection (same grid, partials, counter and
+// published result layout as the ICP pass): out[0] = pairs with
+// e2 <= p.max_d2, out[1] = pairs with a match, out[2..16] = moments of the
+// kept pairs, out[17] = sum of e2 over all matched pairs.
+cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,
+                                 int64_t n, const IcpPassParams& p, double* partials,
+                                 uint32_t* counter, double* out, int grid, cudaStream_t s);
 
 // Allocation-free variant of the ICP pass (reads the caller's n x 3 source in
 // place, one thread per point; all scratch in a file-scope device array of

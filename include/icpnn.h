@@ -68,7 +68,9 @@ typedef enum icpnn_status {
 #define ICPNN_MORTON_SORT 1u /* reorder queries along a 30-bit Morton curve first */
 
 /* icp_align flags */
-#define ICPNN_TRACE_TIMING 2u /* fill icpnn_iter_record.kernel_ms (CUDA events) */
+#define ICPNN_TRACE_TIMING 2u     /* fill icpnn_iter_record.kernel_ms (CUDA events) */
+#define ICPNN_RESIDUAL_REJECT 4u  /* page section 4.4: after each solve drop pairs whose
+                                     residual exceeds 3 sigma and solve again */
 
 typedef struct icpnn_tree icpnn_tree; /* opaque; owned by the library */
 
@@ -160,8 +162,12 @@ typedef struct icpnn_moments {
 typedef struct icpnn_iter_record {
     int32_t iter;        /* 0-based */
     int32_t flags;       /* reserved, 0 */
-    int64_t n_accepted;  /* pairs accepted in this pass */
-    double mse;          /* mean squared distance of those pairs */
+    int64_t n_accepted;  /* pairs accepted by the distance test in this pass */
+    int64_t n_inliers;   /* pairs the final solve used (= n_accepted without
+                            ICPNN_RESIDUAL_REJECT) */
+    double mse;          /* mean squared distance of the accepted pairs */
+    double sigma2;       /* mean squared residual under the first solve (residual
+                            rejection only, else 0) */
     double T[16];        /* row-major transform this pass used (before the solve) */
     float kernel_ms;     /* device time of the pass (with ICPNN_TRACE_TIMING), else 0 */
     float reserved;
@@ -196,6 +202,12 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   with DEGENERATE if fewer than 3 pairs are accepted, mse_k, T_{k+1} =
  *   icpnn_kabsch; stop after the solve once k >= 2 and
  *   |mse_{k-1} - mse_k| < eps and |mse_{k-2} - mse_{k-1}| < eps.
+ *   With ICPNN_RESIDUAL_REJECT (page section 4.4) each iteration's first
+ *   solve T' is followed by: e_i^2 = squared residual of every accepted pair
+ *   under float32(T') (the search's float arithmetic), sigma^2 = mean e_i^2,
+ *   keep the pairs with double(e_i^2) <= 9 sigma^2, T_{k+1} = solve over the
+ *   kept pairs (DEGENERATE if fewer than 3 remain).  The stopping rule still
+ *   uses mse_k of the correspondence pass.
  *   Then one more pass (no solve) under the returned transform.
  *   src          n_src x 3 float32 (device, or host: copied in once).
  *   max_iter     >= 1.  eps >= 0 (0: run max_iter iterations).
@@ -204,7 +216,7 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   iters        host: number of solves performed.
  *   trace        optional host array of trace_cap records (one per
  *                iteration, up to trace_cap).
- *   flags        ICPNN_TRACE_TIMING or 0.
+ *   flags        ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT, or 0.
  * Synchronises `stream` once per iteration; scratch comes from the
  * stream-ordered allocator and is returned before the call ends.
  * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY, NONFINITE, DEGENERATE. */

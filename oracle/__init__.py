@@ -26,6 +26,11 @@ Source: "Implementing ICP with CUDA-KDTree" (pwwt.cn/news/5235220).
                   change of the mean squared correspondence distance has
                   stayed below eps for two consecutive iterations, or at
                   max_iter.
+* ``residual_reject`` -- section 4.4's second defence against outliers:
+                  after the solve, compute every accepted pair's residual,
+                  drop pairs beyond n_sigma standard deviations and solve
+                  once more (the page recommends 3 sigma, combined with the
+                  maximum correspondence distance).
 
 Readings (the page is silent or loose on these):
   - eps is absolute, on mse_k = (sum of accepted d2) / (number accepted);
@@ -39,7 +44,15 @@ Readings (the page is silent or loose on these):
   - fewer than 3 accepted pairs, or H of rank < 2 (sigma_2 <= 1e-12 sigma_1),
     is degenerate;
   - the reported error is the mse under the returned transform (one extra
-    correspondence pass, no solve).
+    correspondence pass, no solve);
+  - residual rejection: residual e_i = |R' s_i + t' - q_i| of each accepted
+    pair under the first solve (R', t') of the iteration, evaluated like the
+    search (float32 transform of the original s_i with float32(R', t'),
+    float32 squared distance); sigma^2 = mean of e_i^2 over the accepted pairs
+    (the residual vectors of a least-squares rigid fit have zero mean, so
+    this is their variance); keep pairs with e_i^2 <= (n_sigma sigma)^2,
+    compared in double; the iteration's transform is the solve over the kept
+    pairs; the stopping rule still uses the mse of the correspondence pass.
 
 Parity pins (tests/test_oracle.py): hand-derived NN fixture, scipy cKDTree
 cross-check, tree search == brute force on tie-heavy clouds, tree
@@ -114,6 +127,8 @@ def _load():
     lib.orc_tree_export.restype = None
     lib.orc_tree_nn.argtypes = [P, P, i64, P, P, P, P]
     lib.orc_tree_nn.restype = None
+    lib.orc_pair_dist2.argtypes = [P, P, i64, P]
+    lib.orc_pair_dist2.restype = None
     _lib = lib
     return lib
 
@@ -137,6 +152,16 @@ def nn_brute(reference, queries):
     d2 = np.empty(len(q), np.float32)
     lib.orc_nn_brute(_ptr(ref), len(ref), _ptr(q), len(q), _ptr(idx), _ptr(d2))
     return idx, d2
+
+
+def pair_dist2(q, p) -> np.ndarray:
+    """float32 squared distance of each pair (q_i, p_i), search arithmetic."""
+    lib = _load()
+    q = _f32(q)
+    p = _f32(p)
+    out = np.empty(len(q), np.float32)
+    lib.orc_pair_dist2(_ptr(q), _ptr(p), len(q), _ptr(out))
+    return out
 
 
 def transform(R, t, source) -> np.ndarray:
@@ -278,12 +303,36 @@ def solve_from_step(step, source, tree: KDTree):
     return T
 
 
+def residual_reject(step, source, tree: KDTree, T1, n_sigma: float):
+    """Residuals of the accepted pairs under the first solve T1, the sigma
+    rule, and the solve over the kept pairs.  Returns dict(T, kept (mask over
+    the source), n_kept, sigma2, e2 (per accepted pair))."""
+    acc = step["accepted"]
+    src = _f32(source)
+    S = src[acc]
+    Q = tree.points[step["idx"][acc]]
+    R32, t32 = as_kernel_rt(T1)
+    e2 = pair_dist2(Q, transform(R32, t32, S))
+    sigma2 = float(np.sum(e2.astype(np.float64)) / len(e2))
+    keep_acc = e2.astype(np.float64) <= (n_sigma * n_sigma) * sigma2
+    kept = np.zeros(len(src), bool)
+    kept[np.flatnonzero(acc)[keep_acc]] = True
+    if keep_acc.sum() < 3:
+        raise DegenerateError("fewer than 3 pairs left after residual rejection")
+    R, t, _ = kabsch(S[keep_acc], Q[keep_acc])
+    T = np.eye(4)
+    T[:3, :3] = R
+    T[:3, 3] = t
+    return {"T": T, "kept": kept, "n_kept": int(keep_acc.sum()), "sigma2": sigma2, "e2": e2}
+
+
 def icp_align(tree: KDTree, source, max_iter: int, eps: float, max_corr_dist,
-              init_T=None):
-    """Section 3.3 loop with the section 4.6 stopping rule.
+              init_T=None, residual_sigma: float = 0.0):
+    """Section 3.3 loop with the section 4.6 stopping rule; residual_sigma > 0
+    adds the section 4.4 residual rejection and re-solve to every iteration.
 
     Returns dict(T, iters, final_mse, trace) where trace[k] = dict(T (used for
-    pass k), mse, n_accepted)."""
+    pass k), mse, n_accepted, n_inliers)."""
     T = np.eye(4) if init_T is None else np.asarray(init_T, np.float64).copy()
     trace = []
     mses = []
@@ -293,7 +342,13 @@ def icp_align(tree: KDTree, source, max_iter: int, eps: float, max_corr_dist,
         if st["n_accepted"] < 3:
             raise DegenerateError("fewer than 3 accepted correspondences")
         T_next = solve_from_step(st, source, tree)
-        trace.append({"T": T.copy(), "mse": st["mse"], "n_accepted": st["n_accepted"]})
+        n_in = st["n_accepted"]
+        if residual_sigma > 0:
+            rr = residual_reject(st, source, tree, T_next, residual_sigma)
+            T_next = rr["T"]
+            n_in = rr["n_kept"]
+        trace.append({"T": T.copy(), "mse": st["mse"], "n_accepted": st["n_accepted"],
+                      "n_inliers": n_in})
         mses.append(st["mse"])
         T = T_next
         iters = k + 1

@@ -28,6 +28,9 @@
  *            than the best distance so far.
  *   transform -- p = R*s + t of section 2.1 applied to the original source
  *            coordinates (section 3.3), float32.
+ *   pair_dist2 -- squared distance of given pairs (q_i, p_i) with the same
+ *            float32 arithmetic as the search: the residual of a pair under a
+ *            transform, for the residual rejection of section 4.4.
  *
  * Readings where the page is silent or loose (each also listed in the
  * design notes):
@@ -120,6 +123,16 @@ void orc_transform(const float *R, const float *t, const float *s, int64_t n, fl
             out[3 * i + a] = acc;
         }
     }
+}
+
+/* ------------------------------------------------------------- residuals */
+
+/* out[i] = d2 between target point q_i and point p_i, in the search's order
+ * of operations (dx = q.x - p.x, ...). */
+void orc_pair_dist2(const float *q, const float *p, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_dist2(q + 3 * i, p[3 * i], p[3 * i + 1], p[3 * i + 2]);
 }
 
 /* ------------------------------------------------------------------- tree */

@@ -174,6 +174,44 @@ def test_align_parity(nn, oracle_mod, name):
     assert abs(np.linalg.det(R) - 1) < 1e-12
 
 
+def _residual_case(name):
+    if name == "tiny_outliers":
+        c = W.tiny_case()
+        src, _ = W.with_outliers(c.source, 0.05, 0.15, 11)
+        return c, src, math.inf
+    c = W.CASES[name]()
+    return c, c.source, c.max_corr_dist[0]
+
+
+@pytest.mark.parametrize("name", ["tiny_outliers", "scene"])
+def test_residual_rejection_parity(nn, oracle_mod, name):
+    """Section 4.4 residual rejection: each iteration's transform fed to the
+    oracle reproduces the correspondence pass exactly, the residual variance
+    to 1e-5, the kept set up to pairs whose residual sits within rounding of
+    the 3-sigma threshold (the two sides sum the residuals in different
+    orders), and the re-solve lands on the library's next transform."""
+    c, src, dmax = _residual_case(name)
+    t, ot = setup(nn, oracle_mod, c)
+    res = nn.icp_align(t, dev(src), c.max_iter, c.eps, dmax, trace=True, residual_reject=True)
+    tr = res["trace"]
+    ks = range(len(tr)) if name == "tiny_outliers" else sorted({0, 1, 5, len(tr) // 2, len(tr) - 1})
+    for k in ks:
+        st = oracle_mod.icp_step(ot, src, tr[k]["T"], dmax)
+        assert tr[k]["n_accepted"] == st["n_accepted"], k
+        assert abs(tr[k]["mse"] - st["mse"]) <= 1e-6 * st["mse"], k
+        T1 = oracle_mod.solve_from_step(st, src, ot)
+        rr = oracle_mod.residual_reject(st, src, ot, T1, 3.0)
+        assert abs(tr[k]["sigma2"] - rr["sigma2"]) <= 1e-5 * rr["sigma2"], k
+        assert abs(tr[k]["n_inliers"] - rr["n_kept"]) <= 2, k
+        if name == "tiny_outliers":
+            assert tr[k]["n_inliers"] < tr[k]["n_accepted"], k
+        T_lib = tr[k + 1]["T"] if k + 1 < len(tr) else res["T"]
+        check_transform(T_lib, rr["T"], c.extent)
+    if name == "tiny_outliers":
+        plain = nn.icp_align(t, dev(src), c.max_iter, c.eps, dmax)
+        assert rot_angle(res["T"][:3, :3], c.T_gt[:3, :3]) < rot_angle(plain["T"][:3, :3], c.T_gt[:3, :3])
+
+
 def test_tiny_recovers_ground_truth(nn):
     c = W.tiny_case()
     t = nn.kdtree_build(c.target, c.leaf_size)

@@ -364,3 +364,61 @@ def test_rotation_error_formula():
     import oracle
     R = W.axis_angle_matrix([0, 0, 1], 0.25)
     assert abs(oracle.rotation_error(R, np.eye(3)) - 0.25) < 1e-12
+
+
+# ------------------------------------------------------------ residual rejection
+
+def _with_outliers(c, frac=0.03, seed=4):
+    return W.with_outliers(c.source, frac, 0.15, seed)
+
+
+def test_residual_rejection_drops_planted_outliers(oracle_mod):
+    """Section 4.4: pairs beyond 3 sigma after the solve are dropped and the
+    solve repeated.  Points displaced by 0.15 m in a cloud aligned to 0.002 m
+    must be the ones dropped, and the recovered motion must improve."""
+    c = W.tiny_case()
+    src, bad = _with_outliers(c)
+    tree = oracle_mod.KDTree(c.target, c.leaf_size)
+    st = oracle_mod.icp_step(tree, src, c.T_gt, math.inf)
+    T1 = oracle_mod.solve_from_step(st, src, tree)
+    rr = oracle_mod.residual_reject(st, src, tree, T1, 3.0)
+    dropped = np.flatnonzero(st["accepted"] & ~rr["kept"])
+    assert len(dropped) > 0
+    assert np.isin(dropped, bad).mean() > 0.95            # what it drops are outliers
+    assert rr["n_kept"] + len(dropped) == st["n_accepted"]
+    e_all = oracle_mod.rotation_error(T1[:3, :3], c.T_gt[:3, :3])
+    e_rej = oracle_mod.rotation_error(rr["T"][:3, :3], c.T_gt[:3, :3])
+    assert e_rej < 0.5 * e_all
+    assert np.linalg.norm(rr["T"][:3, 3] - c.T_gt[:3, 3]) < np.linalg.norm(T1[:3, 3] - c.T_gt[:3, 3])
+
+
+def test_residual_rule_and_sigma(oracle_mod):
+    """sigma^2 is the mean squared residual of the accepted pairs under the
+    first solve, recomputed here in double from the pairs themselves; the kept
+    set is exactly the pairs within 3 sigma."""
+    c = W.tiny_case()
+    src, _ = _with_outliers(c, 0.02, 9)
+    tree = oracle_mod.KDTree(c.target, c.leaf_size)
+    st = oracle_mod.icp_step(tree, src, np.eye(4), math.inf)
+    T1 = oracle_mod.solve_from_step(st, src, tree)
+    rr = oracle_mod.residual_reject(st, src, tree, T1, 3.0)
+    acc = st["accepted"]
+    S = src[acc].astype(np.float64)
+    Q = c.target[st["idx"][acc]].astype(np.float64)
+    res = S @ T1[:3, :3].T + T1[:3, 3] - Q
+    e2 = np.sum(res * res, axis=1)
+    assert abs(rr["sigma2"] - e2.mean()) <= 1e-5 * e2.mean()
+    near = np.abs(e2 - 9 * e2.mean()) < 1e-5 * e2.mean()
+    np.testing.assert_array_equal(rr["kept"][acc][~near], (e2 <= 9 * e2.mean())[~near])
+
+
+def test_icp_with_residual_rejection_recovers_through_outliers(oracle_mod):
+    c = W.tiny_case()
+    src, _ = _with_outliers(c, 0.05, 11)
+    tree = oracle_mod.KDTree(c.target, c.leaf_size)
+    plain = oracle_mod.icp_align(tree, src, c.max_iter, c.eps, math.inf)
+    robust = oracle_mod.icp_align(tree, src, c.max_iter, c.eps, math.inf, residual_sigma=3.0)
+    e_plain = oracle_mod.rotation_error(plain["T"][:3, :3], c.T_gt[:3, :3])
+    e_rob = oracle_mod.rotation_error(robust["T"][:3, :3], c.T_gt[:3, :3])
+    assert e_rob < e_plain
+    assert all(r["n_inliers"] < r["n_accepted"] for r in robust["trace"])

@@ -144,6 +144,17 @@ def gaussian_mixture(n: int, rng, centres: np.ndarray, sigmas: np.ndarray) -> np
     return _f32(pts)
 
 
+def with_outliers(points: np.ndarray, frac: float, sigma: float, seed: int):
+    """Copy of a cloud with a fraction of its points displaced by N(0, sigma)
+    per coordinate (gross outliers for the residual rejection); returns
+    (cloud, indices of the displaced points)."""
+    rng = np.random.default_rng(seed)
+    pts = np.array(points, dtype=np.float32, copy=True)
+    bad = rng.choice(len(pts), int(frac * len(pts)), replace=False)
+    pts[bad] += rng.normal(0.0, sigma, size=(len(bad), 3)).astype(np.float32)
+    return pts, bad
+
+
 # --------------------------------------------------------------------------
 # case 1: tiny uniform cube
 # --------------------------------------------------------------------------
