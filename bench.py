@@ -226,6 +226,21 @@ def run_ours(args):
         rr_ms.append(a.elapsed_time(b))
         rr_iters += r["iters"]
 
+    # ---- several frames in flight: 8 sources of the same scene, one tree
+    _, frame_srcs, _ = workloads.scene_frames(8)
+    frame_dev = [torch.from_numpy(f).cuda() for f in frame_srcs]
+    multi = {}
+    for mc in (1, 4):
+        nn.icp_align_batch(tree, frame_dev, case.max_iter, case.eps, dmax, max_concurrent=mc, stream=stream)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        b = nn.icp_align_batch(tree, frame_dev, case.max_iter, case.eps, dmax, max_concurrent=mc,
+                               stream=stream)
+        torch.cuda.synchronize()
+        secs = time.perf_counter() - t0
+        multi[f"frames_in_flight_{mc}"] = {"value": float(b["iters"].sum()) / secs, "unit": UNIT,
+                                           "ms_per_frame": secs * 1e3 / len(frame_dev)}
+
     # ---- end to end from host buffers: build + upload + registration
     pinned_src = torch.from_numpy(case.source).pin_memory()
     pinned_tgt = case.target
@@ -290,6 +305,8 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "once_per_target_ms": {"kdtree_build": build_ms, "kdtree_upload": upload_ms},
+        "multi_frame_8": dict(multi, note="8 independent 100k sources of the scene against one "
+                                          "resident tree, icpnn_icp_align_batch, wall clock"),
         "with_residual_rejection": {"value": rr_iters / (sum(rr_ms) / 1e3), "unit": UNIT,
                                     "ms_per_step": statistics.mean(rr_ms),
                                     "iters_per_step": rr_iters // args.steps,

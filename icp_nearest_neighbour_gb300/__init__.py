@@ -22,7 +22,7 @@ from ._build import LIB as _LIB_PATH, build as _build_library
 __all__ = [
     "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
     "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
-    "kabsch", "icp_align",
+    "kabsch", "icp_align", "icp_align_batch",
     "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "MAX_DEPTH", "NOALLOC_MAX_POINTS",
 ]
 
@@ -91,6 +91,7 @@ def load(build_if_missing: bool = False):
         "icpnn_icp_step_noalloc": ([P, P, i64, P, P, f64, P, P, P, P], ctypes.c_int),
         "icpnn_kabsch": ([P, P], ctypes.c_int),
         "icpnn_icp_align": ([P, P, i64, i32, f64, f64, P, P, P, P, P, i32, u32, P], ctypes.c_int),
+        "icpnn_icp_align_batch": ([P, i32, P, P, i32, f64, f64, P, P, P, P, P, u32, i32, P], ctypes.c_int),
         "icpnn_last_error": ([], ctypes.c_char_p),
         "icpnn_launch_count": ([], i64),
         "icpnn_version": ([], i32),
@@ -306,4 +307,36 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
                          "mse": r.mse, "sigma2": r.sigma2, "T": np.array(r.T[:]).reshape(4, 4),
                          "kernel_ms": r.kernel_ms}
                         for r in recs[:min(iters.value, cap)]]
+    return out
+
+
+def icp_align_batch(tree: KDTree, srcs, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
+                    init_T=None, residual_reject: bool = False, max_concurrent: int = 4,
+                    stream=None) -> dict:
+    """Register several sources against one tree, several frames in flight.
+
+    Returns dict(T (n, 4, 4), final_mse (n,), iters (n,), status (n,))."""
+    n = len(srcs)
+    ptrs = (ctypes.c_void_p * n)(*[_ptr(x, np.float32, 3, f"srcs[{i}]").value for i, x in enumerate(srcs)])
+    counts = np.ascontiguousarray([int(x.shape[0]) for x in srcs], dtype=np.int64)
+    T = np.zeros((n, 16))
+    fmse = np.zeros(n)
+    iters = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    init = None
+    if init_T is not None:
+        init_arr = np.ascontiguousarray(init_T, dtype=np.float64).reshape(n * 16)
+        init = ctypes.c_void_p(init_arr.ctypes.data)
+    rc = load().icpnn_icp_align_batch(tree.handle, n, ctypes.cast(ptrs, ctypes.c_void_p),
+                                      ctypes.c_void_p(counts.ctypes.data), int(max_iter), float(eps),
+                                      float(max_corr_dist), init, ctypes.c_void_p(T.ctypes.data),
+                                      ctypes.c_void_p(fmse.ctypes.data), ctypes.c_void_p(iters.ctypes.data),
+                                      ctypes.c_void_p(status.ctypes.data),
+                                      RESIDUAL_REJECT if residual_reject else 0, int(max_concurrent),
+                                      _stream(stream))
+    out = {"T": T.reshape(n, 4, 4), "final_mse": fmse, "iters": iters, "status": status}
+    if rc != 0:
+        err = IcpnnError(rc, last_error())
+        err.result = out
+        raise err
     return out

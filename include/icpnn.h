@@ -225,6 +225,31 @@ int icpnn_icp_align(const icpnn_tree* target, const float* src, int64_t n_src, i
                     double* final_mse, int32_t* iters, icpnn_iter_record* trace,
                     int32_t trace_cap, uint32_t flags, void* stream);
 
+/* icpnn_icp_align_batch -- register n_frames sources against one resident
+ * target (page section 3.4: several frames in flight so that one frame's
+ * queries overlap another frame's result transfer and solve).  Each frame is
+ * an icpnn_icp_align run by a library worker thread on a stream of its own,
+ * with up to max_concurrent frames in flight (<= 0: 4); frames are handed out
+ * in order as workers free up.  Every frame's result is bit-identical to a
+ * single-frame icpnn_icp_align of it.
+ *   srcs, n_src   n_frames source pointers (n x 3 float32, device or host)
+ *                 and point counts.
+ *   init_T        NULL or n_frames row-major 4x4 initial transforms.
+ *   out_T, final_mse, iters, status   per-frame outputs (host arrays of
+ *                 16*n_frames, n_frames, n_frames, n_frames); status[f] is
+ *                 frame f's icpnn_status.
+ *   flags         ICPNN_RESIDUAL_REJECT or 0.
+ *   stream        the frames start after work already enqueued on it; all
+ *                 their work is complete when the call returns.
+ * Returns ICPNN_OK if every frame succeeded, else the first failing frame's
+ * status (icpnn_last_error names the frame).  The caller's current device must
+ * be the tree's.  Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY,
+ * NONFINITE, DEGENERATE. */
+int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames, const float* const* srcs,
+                          const int64_t* n_src, int32_t max_iter, double eps, double max_corr_dist,
+                          const double* init_T, double* out_T, double* final_mse, int32_t* iters,
+                          int32_t* status, uint32_t flags, int32_t max_concurrent, void* stream);
+
 /* ------------------------------------------------------ no allocation --
  * icpnn_icp_step_noalloc -- the fused correspondence pass of icpnn_icp_step
  * for callers that cannot allocate device memory: code embedded in a host

@@ -291,6 +291,28 @@ def scene_case(n_target: int = 100_000, n_source: int = 100_000) -> Registration
                             info={"angle_deg": math.degrees(angle), "t_norm": float(np.linalg.norm(t))})
 
 
+def scene_frames(n_frames: int, n_target: int = 100_000, n_source: int = 100_000):
+    """The scene of case 2 (same target) with n_frames independent sources:
+    frame 0 is case 2's own source, frame k > 0 an independent resample of the
+    same surfaces under its own offset (<= 15 deg, <= 1 m), drawn from the
+    sub-stream ``SeedSequence(1002).spawn(4 + k)[-1]``.  Returns (case, [frame
+    sources], [frame ground truths])."""
+    case = scene_case(n_target, n_source)
+    r_scene = _rngs(2, 4)[0]
+    scene = make_scene(r_scene)
+    srcs, gts = [case.source], [case.T_gt]
+    for k in range(1, n_frames):
+        rng = np.random.default_rng(np.random.SeedSequence(SEED_BASE + 2).spawn(4 + k)[-1])
+        world = sample_scene_surfaces(scene, n_source, rng, 0.01)
+        angle = math.radians(rng.uniform(0.0, 15.0))
+        R = axis_angle_matrix(random_unit_vector(rng), angle)
+        t = random_unit_vector(rng) * rng.uniform(0.0, 1.0)
+        T = rigid(R, t)
+        srcs.append(_f32(_apply_inverse(T, world)))
+        gts.append(T)
+    return case, srcs, gts
+
+
 def large_case(n_target: int = 4_000_000, n_source: int = 2_000_000) -> RegistrationCase:
     r_scene, r_tgt, r_src, r_pose = _rngs(5, 4)
     scene = make_scene(r_scene)
