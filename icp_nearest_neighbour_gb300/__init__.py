@@ -22,7 +22,7 @@ from ._build import LIB as _LIB_PATH, build as _build_library
 __all__ = [
     "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
     "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
-    "kabsch", "icp_align", "icp_align_batch",
+    "kabsch", "icp_align", "icp_align_batch", "voxel_downsample",
     "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "MAX_DEPTH", "NOALLOC_MAX_POINTS",
 ]
 
@@ -92,6 +92,7 @@ def load(build_if_missing: bool = False):
         "icpnn_kabsch": ([P, P], ctypes.c_int),
         "icpnn_icp_align": ([P, P, i64, i32, f64, f64, P, P, P, P, P, i32, u32, P], ctypes.c_int),
         "icpnn_icp_align_batch": ([P, i32, P, P, i32, f64, f64, P, P, P, P, P, u32, i32, P], ctypes.c_int),
+        "icpnn_voxel_downsample": ([P, i64, ctypes.c_float, P, P, P], ctypes.c_int),
         "icpnn_last_error": ([], ctypes.c_char_p),
         "icpnn_launch_count": ([], i64),
         "icpnn_version": ([], i32),
@@ -340,3 +341,18 @@ def icp_align_batch(tree: KDTree, srcs, max_iter: int, eps: float, max_corr_dist
         err.result = out
         raise err
     return out
+
+
+def voxel_downsample(xyz, voxel_size: float, stream=None):
+    """Voxel-grid filter (centroid per occupied voxel).  A CUDA tensor in gives
+    a CUDA tensor out, a NumPy array gives a NumPy array; shape (m, 3)."""
+    n = int(xyz.shape[0])
+    if _is_torch(xyz) and xyz.is_cuda:
+        import torch
+        out = torch.empty((max(n, 1), 3), dtype=torch.float32, device=xyz.device)
+    else:
+        out = np.empty((max(n, 1), 3), np.float32)
+    m = ctypes.c_int64()
+    _check(load().icpnn_voxel_downsample(_ptr(xyz, np.float32, 3, "xyz"), n, float(voxel_size),
+                                         _ptr(out, np.float32, 3, "out"), ctypes.byref(m), _stream(stream)))
+    return out[:m.value]

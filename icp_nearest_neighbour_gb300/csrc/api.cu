@@ -709,6 +709,53 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   return ICPNN_OK;
 }
 
+int icpnn_voxel_downsample(const float* xyz, int64_t n, float voxel_size, float* out_xyz, int64_t* out_n,
+                           void* stream) {
+  clear_error();
+  if (out_n == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "voxel_downsample: out_n is NULL");
+  *out_n = 0;
+  if (n < 0 || n > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "voxel_downsample: n out of range");
+  if (!(voxel_size > 0.0f) || std::isinf(voxel_size))
+    return fail(ICPNN_ERR_INVALID_ARG, "voxel_downsample: voxel_size must be positive and finite");
+  if (n == 0) return ICPNN_OK;
+  if (!xyz || !out_xyz) return fail(ICPNN_ERR_INVALID_ARG, "voxel_downsample: NULL pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t count = 0;
+  {
+    Scratch sc(s);
+    const float* d_xyz = xyz;
+    if (!is_device_pointer(xyz)) {
+      float* tmp = nullptr;
+      ICPNN_CUDA(sc.alloc(&tmp, 3 * n));
+      ICPNN_CUDA(cudaMemcpyAsync(tmp, xyz, static_cast<size_t>(n) * 3 * sizeof(float), cudaMemcpyHostToDevice, s));
+      d_xyz = tmp;
+    }
+    const bool host_out = !is_device_pointer(out_xyz);
+    float* d_out = out_xyz;
+    if (host_out) ICPNN_CUDA(sc.alloc(&d_out, 3 * n));
+    uint32_t* scratch = nullptr;
+    long long* bounds = nullptr;
+    unsigned long long* total = nullptr;
+    ICPNN_CUDA(sc.alloc(&scratch, voxel_scratch_words(n)));
+    ICPNN_CUDA(sc.alloc(&bounds, 8));
+    ICPNN_CUDA(sc.alloc(&total, 1));
+    long long host_bounds[8];
+    cudaError_t err = cudaSuccess;
+    const int rc = voxel_downsample(d_xyz, n, voxel_size, d_out, &count, scratch, bounds, total, host_bounds, s, &err);
+    if (err != cudaSuccess) return fail(ICPNN_ERR_CUDA, std::string("voxel_downsample: ") + cudaGetErrorString(err));
+    if (rc < 0)
+      return fail(ICPNN_ERR_INVALID_ARG, "voxel_downsample: a voxel index exceeds 2^40 (coordinates too large "
+                                         "for this voxel size)");
+    if (host_out && count > 0) {
+      ICPNN_CUDA(cudaMemcpyAsync(out_xyz, d_out, static_cast<size_t>(count) * 3 * sizeof(float),
+                                 cudaMemcpyDeviceToHost, s));
+      ICPNN_CUDA(cudaStreamSynchronize(s));
+    }
+  }
+  *out_n = count;
+  return ICPNN_OK;
+}
+
 const char* icpnn_last_error(void) { return tl_error.c_str(); }
 
 int64_t icpnn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }

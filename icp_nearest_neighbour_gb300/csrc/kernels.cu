@@ -270,6 +270,186 @@ __global__ void __launch_bounds__(kThreads) radix_scatter_kernel(
   }
 }
 
+// ------------------------------------------------------------ voxels ----
+// Voxel-grid downsampling ("Implementing ICP with CUDA-KDTree", section 4.3):
+// voxel index floor(x / v) per axis (float32 division, grid anchored at the
+// origin), one output point per occupied voxel, the centroid of its points
+// summed in input order in double and rounded to float32, voxels ordered by
+// (ix, iy, iz).  Non-finite points are dropped.
+
+constexpr double kVoxelIndexLimit = 1099511627776.0;  // 2^40
+
+__device__ __forceinline__ bool voxel_index(const float* __restrict__ xyz, int64_t i, float v,
+                                            long long (&k)[3]) {
+  const float x = xyz[3 * i], y = xyz[3 * i + 1], z = xyz[3 * i + 2];
+  if (!finite3(x, y, z)) return false;
+  k[0] = static_cast<long long>(floorf(__fdiv_rn(x, v)));
+  k[1] = static_cast<long long>(floorf(__fdiv_rn(y, v)));
+  k[2] = static_cast<long long>(floorf(__fdiv_rn(z, v)));
+  return true;
+}
+
+// bounds: lo[3], hi[3] (int64 voxel indices), [6] finite points, [7] out-of-range flag
+__global__ void voxel_bounds_init_kernel(long long* bounds) {
+  const int i = threadIdx.x;
+  if (i < 3) bounds[i] = LLONG_MAX;
+  else if (i < 6) bounds[i] = LLONG_MIN;
+  else if (i < 8) bounds[i] = 0;
+}
+
+__global__ void __launch_bounds__(kThreads) voxel_bounds_kernel(const float* __restrict__ xyz, int64_t n,
+                                                                float v, long long* __restrict__ bounds) {
+  long long lo[3] = {LLONG_MAX, LLONG_MAX, LLONG_MAX}, hi[3] = {LLONG_MIN, LLONG_MIN, LLONG_MIN};
+  unsigned long long cnt = 0, bad = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float x = xyz[3 * i], y = xyz[3 * i + 1], z = xyz[3 * i + 2];
+    if (!finite3(x, y, z)) continue;
+    const float q[3] = {floorf(__fdiv_rn(x, v)), floorf(__fdiv_rn(y, v)), floorf(__fdiv_rn(z, v))};
+    bool ok = true;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) ok = ok && fabsf(q[d]) < static_cast<float>(kVoxelIndexLimit);
+    if (!ok) {
+      ++bad;
+      continue;
+    }
+    ++cnt;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      const long long k = static_cast<long long>(q[d]);
+      lo[d] = min(lo[d], k);
+      hi[d] = max(hi[d], k);
+    }
+  }
+#pragma unroll
+  for (int d = 0; d < 3; ++d) {
+    for (int off = 16; off > 0; off >>= 1) {
+      lo[d] = min(lo[d], __shfl_xor_sync(kFull, lo[d], off));
+      hi[d] = max(hi[d], __shfl_xor_sync(kFull, hi[d], off));
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    cnt += __shfl_xor_sync(kFull, cnt, off);
+    bad += __shfl_xor_sync(kFull, bad, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      if (lo[d] != LLONG_MAX) atomicMin(&bounds[d], lo[d]);
+      if (hi[d] != LLONG_MIN) atomicMax(&bounds[3 + d], hi[d]);
+    }
+    if (cnt) atomicAdd(reinterpret_cast<unsigned long long*>(&bounds[6]), cnt);
+    if (bad) atomicAdd(reinterpret_cast<unsigned long long*>(&bounds[7]), bad);
+  }
+}
+
+struct VoxelGrid {
+  float v;
+  long long lo[3];
+  unsigned long long ry, rz;      // index ranges of y and z
+  unsigned long long sentinel;    // key of a dropped point: sorts after every voxel
+};
+
+__device__ __forceinline__ unsigned long long voxel_key(const float* __restrict__ xyz, int64_t i,
+                                                        const VoxelGrid& g) {
+  long long k[3];
+  if (!voxel_index(xyz, i, g.v, k)) return g.sentinel;
+  return (static_cast<unsigned long long>(k[0] - g.lo[0]) * g.ry + static_cast<unsigned long long>(k[1] - g.lo[1])) *
+             g.rz +
+         static_cast<unsigned long long>(k[2] - g.lo[2]);
+}
+
+__global__ void __launch_bounds__(kThreads) voxel_keys_kernel(const float* __restrict__ xyz, int64_t n,
+                                                              VoxelGrid g, uint32_t* __restrict__ key_lo,
+                                                              uint32_t* __restrict__ key_hi,
+                                                              uint32_t* __restrict__ vals) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const unsigned long long k = voxel_key(xyz, i, g);
+    key_lo[i] = static_cast<uint32_t>(k);
+    if (key_hi) key_hi[i] = static_cast<uint32_t>(k >> 32);
+    vals[i] = static_cast<uint32_t>(i);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) gather_u32_kernel(const uint32_t* __restrict__ src,
+                                                              const uint32_t* __restrict__ perm, int64_t n,
+                                                              uint32_t* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = src[perm[i]];
+}
+
+__device__ __forceinline__ bool voxel_head(const float* __restrict__ xyz, const uint32_t* __restrict__ order,
+                                           int64_t i, int64_t m, const VoxelGrid& g) {
+  if (i >= m) return false;
+  if (i == 0) return true;
+  return voxel_key(xyz, order[i], g) != voxel_key(xyz, order[i - 1], g);
+}
+
+// per block of kThreads sorted positions: number of voxel heads
+__global__ void __launch_bounds__(kThreads) voxel_head_count_kernel(const float* __restrict__ xyz,
+                                                                    const uint32_t* __restrict__ order,
+                                                                    int64_t m, VoxelGrid g,
+                                                                    uint32_t* __restrict__ block_heads) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const uint32_t h = voxel_head(xyz, order, i, m, g) ? 1u : 0u;
+  const uint32_t c = __reduce_add_sync(kFull, h);
+  __shared__ uint32_t warp_c[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) warp_c[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < kThreads / 32; ++w) t += warp_c[w];
+    block_heads[blockIdx.x] = t;
+  }
+}
+
+// exclusive scan of `count` words in place by one block; total to *total
+__global__ void __launch_bounds__(kThreads) scan_one_block_kernel(uint32_t* __restrict__ data, int64_t count,
+                                                                  unsigned long long* __restrict__ total) {
+  __shared__ uint32_t warp_sums[kThreads / 32];
+  uint32_t carry = 0;
+  for (int64_t base = 0; base < count; base += kThreads) {
+    const int64_t i = base + threadIdx.x;
+    const uint32_t v = i < count ? data[i] : 0u;
+    uint32_t chunk_total;
+    const uint32_t excl = block_exclusive_scan(v, warp_sums, &chunk_total);
+    if (i < count) data[i] = carry + excl;
+    carry += chunk_total;
+  }
+  if (threadIdx.x == 0) *total = carry;
+}
+
+// every voxel head: its ordinal (block offset + rank in block), then the
+// centroid of its run of equal keys, summed in sorted (= input) order
+__global__ void __launch_bounds__(kThreads) voxel_emit_kernel(const float* __restrict__ xyz,
+                                                              const uint32_t* __restrict__ order, int64_t m,
+                                                              VoxelGrid g,
+                                                              const uint32_t* __restrict__ block_offset,
+                                                              float* __restrict__ out) {
+  __shared__ uint32_t warp_sums[kThreads / 32];
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const bool head = voxel_head(xyz, order, i, m, g);
+  const uint32_t rank = block_exclusive_scan(head ? 1u : 0u, warp_sums, nullptr);
+  if (!head) return;
+  const int64_t ord = static_cast<int64_t>(block_offset[blockIdx.x]) + rank;
+  const unsigned long long key = voxel_key(xyz, order[i], g);
+  double sx = 0.0, sy = 0.0, sz = 0.0;
+  int64_t j = i;
+  for (; j < m; ++j) {
+    const uint32_t p = order[j];
+    if (j > i && voxel_key(xyz, p, g) != key) break;
+    sx += static_cast<double>(xyz[3 * static_cast<int64_t>(p)]);
+    sy += static_cast<double>(xyz[3 * static_cast<int64_t>(p) + 1]);
+    sz += static_cast<double>(xyz[3 * static_cast<int64_t>(p) + 2]);
+  }
+  const double cnt = static_cast<double>(j - i);
+  out[3 * ord] = static_cast<float>(sx / cnt);
+  out[3 * ord + 1] = static_cast<float>(sy / cnt);
+  out[3 * ord + 2] = static_cast<float>(sz / cnt);
+}
+
 // ------------------------------------------------------------ gather ----
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const float* __restrict__ xyz, int64_t n,
@@ -733,6 +913,78 @@ cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const i
                                                  slot_of, n, p, partials, counter, out);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
+}
+
+int64_t voxel_scratch_words(int64_t n) {
+  // key_lo, key_hi, vals, alt keys, alt vals, gathered hi, radix temp, block heads
+  const int64_t blocks = (n + kThreads - 1) / kThreads;
+  return 6 * std::max<int64_t>(n, 1) + radix_temp_words(n) + std::max<int64_t>(blocks, 1) + 64;
+}
+
+int voxel_downsample(const float* xyz, int64_t n, float v, float* out, int64_t* out_n, uint32_t* scratch,
+                     long long* bounds, unsigned long long* total, long long* host_bounds, cudaStream_t s,
+                     cudaError_t* err) {
+  *err = cudaSuccess;
+  *out_n = 0;
+  if (n <= 0) return 0;
+  const int grid = blocks_for(n, kThreads, 8 * num_sms());
+  voxel_bounds_init_kernel<<<1, 32, 0, s>>>(bounds);
+  voxel_bounds_kernel<<<grid, kThreads, 0, s>>>(xyz, n, v, bounds);
+  g_launch_count.fetch_add(2, std::memory_order_relaxed);
+  if ((*err = cudaMemcpyAsync(host_bounds, bounds, 8 * sizeof(long long), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return 0;
+  if ((*err = cudaStreamSynchronize(s)) != cudaSuccess) return 0;
+  if (host_bounds[7] != 0) return -1;  // an index beyond +-2^40
+  const int64_t m = host_bounds[6];
+  if (m == 0) return 0;
+  VoxelGrid g;
+  g.v = v;
+  unsigned long long r[3];
+  for (int d = 0; d < 3; ++d) {
+    g.lo[d] = host_bounds[d];
+    r[d] = static_cast<unsigned long long>(host_bounds[3 + d] - host_bounds[d]) + 1ull;
+  }
+  g.ry = r[1];
+  g.rz = r[2];
+  // r < 2^41 per axis; the product must stay below 2^63 (it does unless the
+  // occupied index box is astronomically large)
+  const long double total_keys = static_cast<long double>(r[0]) * r[1] * r[2];
+  if (total_keys >= 9.2e18L) return -1;
+  g.sentinel = r[0] * r[1] * r[2];
+  int bits = 0;
+  while (bits < 64 && (g.sentinel >> bits) != 0) ++bits;
+  uint32_t* key_lo = scratch;
+  uint32_t* key_hi = scratch + n;
+  uint32_t* vals = scratch + 2 * n;
+  uint32_t* alt_k = scratch + 3 * n;
+  uint32_t* alt_v = scratch + 4 * n;
+  uint32_t* gath = scratch + 5 * n;
+  uint32_t* temp = scratch + 6 * n;
+  uint32_t* block_heads = temp + radix_temp_words(n);
+  voxel_keys_kernel<<<grid, kThreads, 0, s>>>(xyz, n, g, key_lo, bits > 32 ? key_hi : nullptr, vals);
+  g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  uint32_t* order = nullptr;
+  if ((*err = radix_sort(key_lo, vals, alt_k, alt_v, temp, n, 0, std::min(bits, 32), s, &order)) != cudaSuccess)
+    return 0;
+  if (bits > 32) {
+    // stable LSD over the high word: sort (hi key in the current order, order)
+    gather_u32_kernel<<<grid, kThreads, 0, s>>>(key_hi, order, n, gath);
+    g_launch_count.fetch_add(1, std::memory_order_relaxed);
+    uint32_t* other_v = order == vals ? alt_v : vals;
+    uint32_t* other_k = key_lo;  // free now
+    if ((*err = radix_sort(gath, order, other_k, other_v, temp, n, 0, bits - 32, s, &order)) != cudaSuccess)
+      return 0;
+  }
+  const int blocks = static_cast<int>((m + kThreads - 1) / kThreads);
+  voxel_head_count_kernel<<<blocks, kThreads, 0, s>>>(xyz, order, m, g, block_heads);
+  scan_one_block_kernel<<<1, kThreads, 0, s>>>(block_heads, blocks, total);
+  voxel_emit_kernel<<<blocks, kThreads, 0, s>>>(xyz, order, m, g, block_heads, out);
+  g_launch_count.fetch_add(3, std::memory_order_relaxed);
+  if ((*err = cudaGetLastError()) != cudaSuccess) return 0;
+  unsigned long long h_total = 0;
+  if ((*err = cudaMemcpyAsync(&h_total, total, sizeof(h_total), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return 0;
+  if ((*err = cudaStreamSynchronize(s)) != cudaSuccess) return 0;
+  *out_n = static_cast<int64_t>(h_total);
+  return 0;
 }
 
 // ------------------------------------------------- allocation-free pass --

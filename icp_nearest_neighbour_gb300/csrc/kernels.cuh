@@ -76,6 +76,16 @@ cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const i
                                  int64_t n, const IcpPassParams& p, double* partials,
                                  uint32_t* counter, double* out, int grid, cudaStream_t s);
 
+// Voxel-grid downsampling of n points (device xyz) into out (device, capacity
+// n x 3); *out_n = occupied voxels.  scratch: voxel_scratch_words(n) words;
+// bounds: 8 device words; total: 1 device word; host_bounds: 8 host words.
+// Returns 0, or -1 when a voxel index would exceed +-2^40 (or the occupied
+// index box 2^63 keys); CUDA errors in *err.
+int64_t voxel_scratch_words(int64_t n);
+int voxel_downsample(const float* xyz, int64_t n, float v, float* out, int64_t* out_n, uint32_t* scratch,
+                     long long* bounds, unsigned long long* total, long long* host_bounds, cudaStream_t s,
+                     cudaError_t* err);
+
 // Allocation-free variant of the ICP pass (reads the caller's n x 3 source in
 // place, one thread per point; all scratch in a file-scope device array of
 // kNoAllocMaxBlocks partial records).  noalloc_scratch() returns that array's

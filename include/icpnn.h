@@ -139,7 +139,24 @@ int icpnn_kdtree_export(const icpnn_tree* tree, int64_t node_capacity, float* sp
 int icpnn_nn_query(const icpnn_tree* tree, const float* xyz, int64_t n, int32_t* idx,
                    float* dist2, uint32_t flags, void* stream);
 
-/* ------------------------------------------------------------------ ICP --
+/* icpnn_voxel_downsample -- the voxel-grid filter of page section 4.3 (run
+ * before the tree is built): one output point per occupied voxel of side
+ * voxel_size, the centroid of the points in it.
+ *   Voxel of a point: (floor(x / v), floor(y / v), floor(z / v)) with
+ *   float32 division (the grid is anchored at the coordinate origin); the
+ *   centroid sums its points in input order in double and rounds the mean
+ *   to float32; output voxels are ordered by (ix, iy, iz); points with a
+ *   non-finite coordinate are dropped.  The result is exact: it equals any
+ *   implementation of that definition bit for bit.
+ *   xyz        n x 3 float32, device or host.
+ *   out_xyz    capacity n x 3 float32, device or host.
+ *   out_n      host: number of voxels written.
+ * Synchronises `stream`.  Errors: INVALID_ARG (voxel_size <= 0 or not
+ * finite, a voxel index beyond 2^40), CUDA, NO_MEMORY. */
+int icpnn_voxel_downsample(const float* xyz, int64_t n, float voxel_size, float* out_xyz, int64_t* out_n,
+                           void* stream);
+
+/* ------------------------------------------------------------------ ICP --/* ------------------------------------------------------------------ ICP --
  * Moments of one correspondence pass (page sections 2.1, 3.3, 4.4): the
  * original source points s_i whose transformed image R s_i + t has a nearest
  * target point q_i within the maximum distance are "accepted";

@@ -26,6 +26,8 @@ Source: "Implementing ICP with CUDA-KDTree" (pwwt.cn/news/5235220).
                   change of the mean squared correspondence distance has
                   stayed below eps for two consecutive iterations, or at
                   max_iter.
+* ``voxel_downsample`` -- section 4.3: one centroid per occupied voxel,
+                  applied before the tree is built.
 * ``residual_reject`` -- section 4.4's second defence against outliers:
                   after the solve, compute every accepted pair's residual,
                   drop pairs beyond n_sigma standard deviations and solve
@@ -129,6 +131,8 @@ def _load():
     lib.orc_tree_nn.restype = None
     lib.orc_pair_dist2.argtypes = [P, P, i64, P]
     lib.orc_pair_dist2.restype = None
+    lib.orc_voxel_downsample.argtypes = [P, i64, ctypes.c_float, P]
+    lib.orc_voxel_downsample.restype = i64
     _lib = lib
     return lib
 
@@ -162,6 +166,18 @@ def pair_dist2(q, p) -> np.ndarray:
     out = np.empty(len(q), np.float32)
     lib.orc_pair_dist2(_ptr(q), _ptr(p), len(q), _ptr(out))
     return out
+
+
+def voxel_downsample(points, voxel: float) -> np.ndarray:
+    """Section 4.3 voxel-grid filter: centroids of the occupied voxels of side
+    `voxel` (float32), ordered by voxel index (see icp_oracle.c)."""
+    lib = _load()
+    pts = _f32(points)
+    out = np.empty((max(len(pts), 1), 3), np.float32)
+    m = lib.orc_voxel_downsample(_ptr(pts), len(pts), float(np.float32(voxel)), _ptr(out))
+    if m < 0:
+        raise ValueError("oracle voxel downsampling failed")
+    return out[:m].copy()
 
 
 def transform(R, t, source) -> np.ndarray:

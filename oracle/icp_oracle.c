@@ -31,6 +31,13 @@
  *   pair_dist2 -- squared distance of given pairs (q_i, p_i) with the same
  *            float32 arithmetic as the search: the residual of a pair under a
  *            transform, for the residual rejection of section 4.4.
+ *   voxel -- the voxel-grid downsampling of section 4.3 (done before the
+ *            tree is built): one point per occupied voxel, the centroid of the
+ *            points in it.  Readings: voxel index floor(x / v) per axis in
+ *            float32 (the grid is anchored at the coordinate origin); the
+ *            centroid sums the voxel's points in input order in double and
+ *            rounds the mean to float32; output voxels ordered by
+ *            (ix, iy, iz); points with a non-finite coordinate are dropped.
  *
  * Readings where the page is silent or loose (each also listed in the
  * design notes):
@@ -133,6 +140,60 @@ void orc_pair_dist2(const float *q, const float *p, int64_t n, float *out)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = orc_dist2(q + 3 * i, p[3 * i], p[3 * i + 1], p[3 * i + 2]);
+}
+
+/* ----------------------------------------------------------------- voxel */
+
+typedef struct {
+    int64_t k[3];
+    int64_t idx;
+} orc_vkey;
+
+static int orc_vkey_cmp(const void *pa, const void *pb)
+{
+    const orc_vkey *a = (const orc_vkey *)pa, *b = (const orc_vkey *)pb;
+    for (int d = 0; d < 3; ++d) {
+        if (a->k[d] < b->k[d]) return -1;
+        if (a->k[d] > b->k[d]) return 1;
+    }
+    return (a->idx > b->idx) - (a->idx < b->idx);
+}
+
+/* out receives up to n centroids (3 floats each); returns the number of
+ * occupied voxels, or -1 on bad arguments / allocation failure. */
+int64_t orc_voxel_downsample(const float *xyz, int64_t n, float v, float *out)
+{
+    if (!(v > 0.0f) || n < 0) return -1;
+    orc_vkey *keys = (orc_vkey *)malloc((size_t)(n > 0 ? n : 1) * sizeof(orc_vkey));
+    if (!keys) return -1;
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const float *p = xyz + 3 * i;
+        if (!orc_finite3(p)) continue;
+        for (int d = 0; d < 3; ++d) keys[m].k[d] = (int64_t)floorf(p[d] / v);
+        keys[m].idx = i;
+        ++m;
+    }
+    qsort(keys, (size_t)m, sizeof(orc_vkey), orc_vkey_cmp);
+    int64_t nv = 0;
+    for (int64_t a = 0; a < m;) {
+        int64_t b = a;
+        double sum[3] = {0.0, 0.0, 0.0};
+        while (b < m && keys[b].k[0] == keys[a].k[0] && keys[b].k[1] == keys[a].k[1] &&
+               keys[b].k[2] == keys[a].k[2]) {
+            const float *p = xyz + 3 * keys[b].idx;
+            sum[0] += p[0];
+            sum[1] += p[1];
+            sum[2] += p[2];
+            ++b;
+        }
+        const double cnt = (double)(b - a);
+        for (int d = 0; d < 3; ++d) out[3 * nv + d] = (float)(sum[d] / cnt);
+        ++nv;
+        a = b;
+    }
+    free(keys);
+    return nv;
 }
 
 /* ------------------------------------------------------------------- tree */

@@ -422,3 +422,46 @@ def test_icp_with_residual_rejection_recovers_through_outliers(oracle_mod):
     e_rob = oracle_mod.rotation_error(robust["T"][:3, :3], c.T_gt[:3, :3])
     assert e_rob < e_plain
     assert all(r["n_inliers"] < r["n_accepted"] for r in robust["trace"])
+
+
+# ------------------------------------------------------------ voxel grid
+
+def _hand_voxel():
+    from conftest import read_fixture
+    rows = read_fixture("voxel_hand.txt")
+    pts = np.array([[float(v) for v in r[1:4]] for r in rows if r[0] == "point"], np.float32)
+    exp = np.array([[float(v) for v in r[1:4]] for r in rows if r[0] == "expect"], np.float64)
+    return pts, exp.astype(np.float32)
+
+
+def test_voxel_hand_fixture(oracle_mod):
+    pts, exp = _hand_voxel()
+    np.testing.assert_array_equal(oracle_mod.voxel_downsample(pts, 0.5), exp)
+
+
+@pytest.mark.parametrize("v", [0.05, 0.1, 0.37])
+def test_voxel_against_numpy_grouping(oracle_mod, v):
+    """Voxel membership and order from numpy's float32 floor and unique; means
+    from numpy in double (summation order may differ: within 1 float ulp)."""
+    rng = np.random.default_rng(17)
+    pts = (rng.normal(size=(20000, 3)) * np.array([2.0, 1.0, 0.5])).astype(np.float32)
+    pts[::97] = pts[1::97]                                   # duplicates
+    got = oracle_mod.voxel_downsample(pts, v)
+    keys = np.floor(pts / np.float32(v)).astype(np.int64)
+    uniq, inv = np.unique(keys, axis=0, return_inverse=True)
+    inv = inv.reshape(-1)
+    sums = np.zeros((len(uniq), 3))
+    np.add.at(sums, inv, pts.astype(np.float64))
+    means = (sums / np.bincount(inv)[:, None]).astype(np.float32)
+    assert got.shape == means.shape
+    np.testing.assert_array_almost_equal_nulp(got, means, nulp=1)
+
+
+def test_voxel_degenerate_inputs(oracle_mod):
+    assert oracle_mod.voxel_downsample(np.zeros((0, 3), np.float32), 0.1).shape == (0, 3)
+    one = np.array([[1.5, -2.5, 3.25]], np.float32)
+    np.testing.assert_array_equal(oracle_mod.voxel_downsample(one, 0.1), one)
+    same = np.tile(np.array([[0.01, 0.02, 0.03]], np.float32), (1000, 1))
+    assert oracle_mod.voxel_downsample(same, 1.0).shape == (1, 3)
+    allnan = np.full((5, 3), np.nan, np.float32)
+    assert oracle_mod.voxel_downsample(allnan, 1.0).shape == (0, 3)
