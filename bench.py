@@ -241,6 +241,38 @@ def run_ours(args):
         multi[f"frames_in_flight_{mc}"] = {"value": float(b["iters"].sum()) / secs, "unit": UNIT,
                                            "ms_per_frame": secs * 1e3 / len(frame_dev)}
 
+    # ---- the page's section 6 regression timing point: 200k <-> 200k, 30 iterations
+    # (tree build included, as in the page's comparison), and the section 4.2
+    # split-rule comparison: mean fused-pass time with each axis rule
+    u = workloads.uniform200k_case()
+    u_src = torch.from_numpy(u.source).cuda()
+    u_ms = []
+    for rep in range(4):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ut = nn.kdtree_build(u.target, u.leaf_size)
+        nn.kdtree_upload(ut, stream=stream)
+        nn.icp_align(ut, u_src, u.max_iter, u.eps, math.inf, stream=stream)
+        torch.cuda.synchronize()
+        if rep:
+            u_ms.append((time.perf_counter() - t0) * 1e3)
+        ut.free()
+    split_cmp = {}
+    lid = workloads.lidar_case()
+    for cname, cc in (("lidar", lid), ("uniform200k", u)):
+        csrc = torch.from_numpy(cc.source).cuda()
+        row = {}
+        for rule in (False, True):
+            ct = nn.kdtree_build(cc.target, cc.leaf_size, round_robin=rule)
+            nn.kdtree_upload(ct, stream=stream)
+            nn.icp_align(ct, csrc, cc.max_iter, cc.eps, cc.max_corr_dist[0], stream=stream)
+            r = nn.icp_align(ct, csrc, cc.max_iter, cc.eps, cc.max_corr_dist[0], timing=True, stream=stream)
+            row["round_robin_pass_us" if rule else "max_variance_pass_us"] = \
+                1e3 * statistics.mean(x["kernel_ms"] for x in r["trace"])
+            ct.free()
+        split_cmp[cname] = row
+    del u_src
+
     # ---- voxel-grid downsampling of the 4M-point large-case target (0.1 m)
     big = torch.from_numpy(workloads.large_case().target).cuda()
     nn.voxel_downsample(big, 0.1, stream=stream)
@@ -322,6 +354,10 @@ def run_ours(args):
         "multi_frame_8": dict(multi, note="8 independent 100k sources of the scene against one "
                                           "resident tree, icpnn_icp_align_batch, wall clock"),
         "voxel_downsample_4M": voxel,
+        "uniform200k_30_iterations_ms": {"value": statistics.median(u_ms),
+                                         "note": "section 6 regression, 200k<->200k, 30 iterations, "
+                                                 "host tree build + upload + registration, wall clock"},
+        "split_rule_mean_pass_us": split_cmp,
         "with_residual_rejection": {"value": rr_iters / (sum(rr_ms) / 1e3), "unit": UNIT,
                                     "ms_per_step": statistics.mean(rr_ms),
                                     "iters_per_step": rr_iters // args.steps,

@@ -29,6 +29,7 @@ __all__ = [
 MORTON_SORT = 1
 TRACE_TIMING = 2
 RESIDUAL_REJECT = 4
+SPLIT_ROUND_ROBIN = 8
 MAX_DEPTH = 20
 NOALLOC_MAX_POINTS = 1 << 20
 
@@ -81,7 +82,7 @@ def load(build_if_missing: bool = False):
     P, i64, i32, u32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
                              ctypes.c_double)
     sig = {
-        "icpnn_kdtree_build": ([P, i64, i32, i32, ctypes.POINTER(P)], ctypes.c_int),
+        "icpnn_kdtree_build": ([P, i64, i32, i32, u32, ctypes.POINTER(P)], ctypes.c_int),
         "icpnn_kdtree_upload": ([P, P], ctypes.c_int),
         "icpnn_kdtree_free": ([P], None),
         "icpnn_kdtree_info": ([P, P, P, P, P, P], ctypes.c_int),
@@ -186,12 +187,13 @@ class KDTree:
         return kdtree_info(self)
 
 
-def kdtree_build(points, leaf_size: int, max_depth: int = -1) -> KDTree:
+def kdtree_build(points, leaf_size: int, max_depth: int = -1, round_robin: bool = False) -> KDTree:
+    """Host build of the target tree; round_robin picks the x, y, z, ... axis rule."""
     pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
     lib = load()
     h = ctypes.c_void_p()
     _check(lib.icpnn_kdtree_build(_ptr(pts, np.float32, 3, "points"), len(pts), int(leaf_size),
-                                  int(max_depth), ctypes.byref(h)))
+                                  int(max_depth), SPLIT_ROUND_ROBIN if round_robin else 0, ctypes.byref(h)))
     return KDTree(h)
 
 

@@ -370,7 +370,7 @@ using namespace icpnn;
 extern "C" {
 
 int icpnn_kdtree_build(const float* xyz_host, int64_t n, int32_t leaf_size, int32_t max_depth,
-                       icpnn_tree** out) {
+                       uint32_t flags, icpnn_tree** out) {
   clear_error();
   if (out == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: out is NULL");
   *out = nullptr;
@@ -381,9 +381,10 @@ int icpnn_kdtree_build(const float* xyz_host, int64_t n, int32_t leaf_size, int3
   if (max_depth == -1) max_depth = ICPNN_MAX_DEPTH;
   if (max_depth < 0 || max_depth > ICPNN_MAX_DEPTH)
     return fail(ICPNN_ERR_TREE_DEPTH, "kdtree_build: max_depth must be in [0, 20] or -1");
+  if (flags & ~ICPNN_SPLIT_ROUND_ROBIN) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: unknown flag");
   icpnn_tree* t = new (std::nothrow) icpnn_tree();
   if (t == nullptr) return fail(ICPNN_ERR_NO_MEMORY, "kdtree_build: host allocation failed");
-  const int rc = build_tree(xyz_host, n, leaf_size, max_depth, t);
+  const int rc = build_tree(xyz_host, n, leaf_size, max_depth, (flags & ICPNN_SPLIT_ROUND_ROBIN) != 0, t);
   if (rc != ICPNN_OK) {
     delete t;
     return rc;

@@ -53,6 +53,7 @@ struct icpnn_tree {
   int32_t leaf_size = 0;
   int32_t max_depth = 0;
   int32_t depth = 0;          // deepest level holding a node (root = 0)
+  bool round_robin = false;   // split axis = depth mod 3 (else largest variance)
   int64_t n_nodes = 0;        // nodes in use
   int64_t heap_slots = 0;     // 2^(depth+1)
   float bbox_lo[3] = {0, 0, 0};
@@ -69,7 +70,7 @@ int fail(int code, const std::string& msg);
 void clear_error();
 
 // Host tree build (kdtree_build.cpp).
-int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth,
+int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t);
 
 // Host Kabsch solve (kabsch.cpp).  Returns ICPNN_OK or ICPNN_ERR_DEGENERATE.

@@ -1,5 +1,6 @@
 // Host KD-tree build ("Implementing ICP with CUDA-KDTree", sections 2.2, 2.3,
-// 4.2, 5.1, 5.2): split on the axis of largest variance at the median, stop at
+// 4.2, 5.1, 5.2): split on the axis of largest variance (or, as the section
+// 4.2 alternative, round robin x, y, z by depth) at the median, stop at
 // leaf_size points or at the depth cap, partition in place with nth_element.
 // The array partitioned is the 16-byte point records themselves (x, y, z,
 // original index), reserved once up front: every pass over a node reads
@@ -32,6 +33,7 @@ struct Builder {
   Rec* recs = nullptr;  // point records, partitioned in place
   Node* heap = nullptr;
   int parallel_depth = 0;
+  bool round_robin = false;  // axis = depth mod 3 instead of largest variance
   std::atomic<int64_t> n_nodes{0};
 
   // Axis of largest population variance; axes within a relative 1e-9 of the
@@ -72,7 +74,7 @@ struct Builder {
       heap[node].meta = kLeafTag | (static_cast<uint32_t>(count) << 2);
       return;
     }
-    const int axis = split_axis(lo, hi);
+    const int axis = round_robin ? depth % 3 : split_axis(lo, hi);
     const int64_t m = count / 2;
     std::nth_element(recs + lo, recs + lo + m, recs + hi, [axis](const Rec& a, const Rec& b) {
       return a.c[axis] < b.c[axis] || (a.c[axis] == b.c[axis] && a.idx < b.idx);
@@ -115,7 +117,8 @@ int32_t tree_depth(int64_t n, int32_t leaf_size, int32_t max_depth) {
 
 }  // namespace
 
-int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, icpnn_tree* t) {
+int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
+               icpnn_tree* t) {
   for (int64_t i = 0; i < 3 * n; ++i)
     if (!std::isfinite(xyz[i]))
       return fail(ICPNN_ERR_NONFINITE, "kdtree_build: non-finite coordinate at point " +
@@ -128,6 +131,7 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     t->n = n;
     t->leaf_size = leaf_size;
     t->max_depth = max_depth;
+    t->round_robin = round_robin;
     t->depth = depth;
     t->heap_slots = int64_t{1} << (depth + 1);
     t->nodes.assign(static_cast<size_t>(t->heap_slots), Node{0u, 0u});
@@ -154,6 +158,7 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     b.max_depth = max_depth;
     b.recs = recs;
     b.heap = t->nodes.data();
+    b.round_robin = round_robin;
     const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
     int pd = 0;
     while ((1u << pd) < 4 * hw && pd < 8) ++pd;

@@ -64,6 +64,9 @@ typedef enum icpnn_status {
 #define ICPNN_MAX_DEPTH 20
 #define ICPNN_MAX_LEAF_SIZE 64
 
+/* kdtree_build flags */
+#define ICPNN_SPLIT_ROUND_ROBIN 8u /* split axis x, y, z, x, ... by depth (page section 4.2) */
+
 /* nn_query flags */
 #define ICPNN_MORTON_SORT 1u /* reorder queries along a 30-bit Morton curve first */
 
@@ -84,16 +87,19 @@ typedef struct icpnn_tree icpnn_tree; /* opaque; owned by the library */
  *              points is a leaf (the page recommends 8 to 16).
  *   max_depth  0 .. ICPNN_MAX_DEPTH, or -1 for the page's 20; a node at this
  *              depth is a leaf whatever its size.
+ *   flags      0, or ICPNN_SPLIT_ROUND_ROBIN for the page's alternative axis
+ *              rule (section 4.2): x, y, z, x, ... by depth.
  *   out        receives the new tree; free it with icpnn_kdtree_free.
  * Split rule: axis of largest population variance (computed in double; axes
  * within a relative 1e-9 of the largest count as tied, the lowest wins),
  * median split: left holds the floor(count/2) smallest points ordered by
  * (coordinate, point index), right the rest, split value = the coordinate of
- * the smallest right point.
+ * the smallest right point.  Nearest-neighbour results never depend on the
+ * rule; only the search cost does.
  * Errors: INVALID_ARG, TREE_DEPTH, NONFINITE (any coordinate NaN/Inf),
  * NO_MEMORY.  Host only; needs no GPU. */
 int icpnn_kdtree_build(const float* xyz_host, int64_t n, int32_t leaf_size, int32_t max_depth,
-                       icpnn_tree** out);
+                       uint32_t flags, icpnn_tree** out);
 
 /* icpnn_kdtree_upload -- copy the tree (node array and leaf-ordered point
  * records) to the current device, enqueued on `stream`, which is then

@@ -117,7 +117,7 @@ def _load():
     lib.orc_nn_brute.restype = None
     lib.orc_transform.argtypes = [P, P, P, i64, P]
     lib.orc_transform.restype = None
-    lib.orc_tree_build.argtypes = [P, i64, i32, i32, ctypes.POINTER(P)]
+    lib.orc_tree_build.argtypes = [P, i64, i32, i32, i32, ctypes.POINTER(P)]
     lib.orc_tree_build.restype = ctypes.c_int
     lib.orc_tree_free.argtypes = [P]
     lib.orc_tree_free.restype = None
@@ -194,14 +194,15 @@ def transform(R, t, source) -> np.ndarray:
 class KDTree:
     """The oracle's own KD-tree (page layout: 24-byte nodes in preorder)."""
 
-    def __init__(self, points, leaf_size: int, max_depth: int = DEPTH_CAP):
+    def __init__(self, points, leaf_size: int, max_depth: int = DEPTH_CAP, round_robin: bool = False):
         lib = _load()
         self.points = _f32(points)
         self.leaf_size = int(leaf_size)
         self.max_depth = int(max_depth)
+        self.round_robin = bool(round_robin)
         h = ctypes.c_void_p()
         rc = lib.orc_tree_build(_ptr(self.points), len(self.points), self.leaf_size,
-                                self.max_depth, ctypes.byref(h))
+                                self.max_depth, int(self.round_robin), ctypes.byref(h))
         if rc != 0:
             raise ValueError(f"oracle tree build failed ({rc})")
         self._h = h

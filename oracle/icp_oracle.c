@@ -22,7 +22,8 @@
  *            table.  Split axis = the axis of largest variance (section 4.2),
  *            split at the median (section 2.2), leaf when the node holds at
  *            most leaf_size points (8-16, section 4.1) or sits at the depth
- *            cap (20, section 5.2).
+ *            cap (20, section 5.2).  The round-robin rule of section 4.2
+ *            (axis = depth mod 3: x, y, z, x, ...) is the alternative split.
  *   search-- the tree search of section 2.2: walk to the near child first,
  *            then visit the far child unless the splitting plane is farther
  *            than the best distance so far.
@@ -214,6 +215,7 @@ typedef struct {
     int64_t n_nodes, cap;
     int32_t *leaf_index; /* leaf slot -> reference point index */
     int32_t leaf_size, max_depth, depth;
+    int32_t round_robin; /* 0: axis of largest variance, 1: depth mod 3 */
 } orc_tree;
 
 static int orc_key_less(const float *pts, int dim, int32_t a, int32_t b)
@@ -309,7 +311,7 @@ static int orc_build_rec(orc_tree *t, int64_t lo, int64_t hi, int depth, int32_t
         return 0;
     }
     int32_t *a = t->leaf_index + lo;
-    int dim = orc_split_axis(t->pts, a, count);
+    int dim = t->round_robin ? depth % 3 : orc_split_axis(t->pts, a, count);
     int64_t m = count / 2;
     orc_select(t->pts, dim, a, count, m);
     float split = t->pts[3 * (int64_t)a[m] + dim];
@@ -338,7 +340,7 @@ void orc_tree_free(orc_tree *t)
 /* Returns 0 on success, -1 on bad arguments or non-finite input, -2 on
  * allocation failure. */
 int orc_tree_build(const float *pts, int64_t n, int32_t leaf_size, int32_t max_depth,
-                   orc_tree **out)
+                   int32_t round_robin, orc_tree **out)
 {
     *out = NULL;
     if (!pts || n < 1 || n > INT32_MAX || leaf_size < 1 || max_depth < 0) return -1;
@@ -349,6 +351,7 @@ int orc_tree_build(const float *pts, int64_t n, int32_t leaf_size, int32_t max_d
     t->n = n;
     t->leaf_size = leaf_size;
     t->max_depth = max_depth;
+    t->round_robin = round_robin ? 1 : 0;
     t->pts = (float *)malloc((size_t)n * 3 * sizeof(float));
     t->leaf_index = (int32_t *)malloc((size_t)n * sizeof(int32_t));
     if (!t->pts || !t->leaf_index) {

@@ -279,3 +279,36 @@ def test_errors(nn):
     # a failed call leaves the library usable
     res = nn.icp_align(t, dev(c.source), 5, 0.0, math.inf)
     assert res["iters"] == 5
+
+
+def test_round_robin_tree_gives_the_same_registration(nn, oracle_mod):
+    """Section 4.2's alternative axis rule changes the tree, not the nearest
+    neighbours nor the reduction order: the registration is bit-identical."""
+    c = W.lidar_case()
+    src = dev(c.source)
+    trees = []
+    for rr in (False, True):
+        t = nn.kdtree_build(c.target, c.leaf_size, round_robin=rr)
+        nn.kdtree_upload(t)
+        trees.append(t)
+    a = nn.icp_align(trees[0], src, c.max_iter, c.eps, c.max_corr_dist[0])
+    b = nn.icp_align(trees[1], src, c.max_iter, c.eps, c.max_corr_dist[0])
+    np.testing.assert_array_equal(a["T"], b["T"])
+    assert a["iters"] == b["iters"] and a["final_mse"] == b["final_mse"]
+
+
+def test_section6_uniform200k_regression(nn, oracle_mod):
+    """The page's simulation regression (section 6) at its full 200k size:
+    parity with the oracle, and the convergence curve it describes (a large
+    first error, a steep drop, then a jump-free approach to the noise floor)."""
+    c = W.uniform200k_case()
+    t, ot = setup(nn, oracle_mod, c)
+    res = nn.icp_align(t, dev(c.source), c.max_iter, c.eps, math.inf, trace=True)
+    _trace_parity(nn, oracle_mod, c, t, ot, c.source, math.inf, res, sample_iters=[0, 3, 6, 29])
+    Ts = [r["T"] for r in res["trace"]] + [res["T"]]
+    rot = np.array([rot_angle(T[:3, :3], c.T_gt[:3, :3]) for T in Ts])
+    tra = np.array([np.linalg.norm(T[:3, 3] - c.T_gt[:3, 3]) for T in Ts])
+    assert rot[8] < 0.01 * rot[0] and tra[8] < 0.01 * tra[0]
+    for k in range(8, len(rot) - 1):
+        assert rot[k + 1] <= rot[k] * 1.05 + 1e-6
+    assert rot[-1] < 1e-4 and tra[-1] < 1e-3

@@ -194,3 +194,11 @@ def test_large_workload_sampled(nn, oracle_mod):
     i_o, d_o = ot.query(c.source[sample])
     assert_nn_equal(idx[sample], d2[sample], i_o, d_o)
     assert (idx >= 0).all() and np.isfinite(d2).all()
+
+
+@pytest.mark.parametrize("name", ["grid", "clustered", "line"])
+def test_round_robin_trees_match_brute_force(nn, oracle_mod, name):
+    ref, q = _clouds()[name]
+    t = nn.kdtree_build(ref, 4, round_robin=True)
+    nn.kdtree_upload(t)
+    assert_nn_equal(*gpu_nn(nn, t, q, 0), *oracle_mod.nn_brute(ref, q))

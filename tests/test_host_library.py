@@ -66,6 +66,17 @@ def test_tree_matches_oracle_tree(lib, oracle_mod, name):
     assert sorted(ex["leaf_index"].tolist()) == list(range(len(pts)))
 
 
+@pytest.mark.parametrize("name", ["uniform", "grid_ties", "flat", "scene"])
+def test_round_robin_tree_matches_oracle_tree(lib, oracle_mod, name):
+    pts, leaf = _tree_clouds()[name]
+    t = lib.kdtree_build(pts, leaf, round_robin=True)
+    o = oracle_mod.KDTree(pts, leaf, round_robin=True)
+    ex, oex = lib.kdtree_export(t), o.export()
+    for k in ("split_val", "split_dim", "left", "right", "start", "end"):
+        np.testing.assert_array_equal(ex[k], oex[k], err_msg=k)
+    assert _leaf_sets(ex) == _leaf_sets(oex)
+
+
 def test_tree_depth_cap(lib, oracle_mod):
     pts = W.uniform_cloud(3000, 4)
     t = lib.kdtree_build(pts, 1, max_depth=5)

@@ -141,7 +141,7 @@ def test_tie_fixture_needs_far_side_equal_distance(oracle_mod):
 
 # ------------------------------------------------------------ tree --------
 
-def _check_tree(ref, leaf, max_depth, ex, depth_reported):
+def _check_tree(ref, leaf, max_depth, ex, depth_reported, round_robin=False):
     n = len(ref)
     assert sorted(ex["leaf_index"].tolist()) == list(range(n))
     covered = np.zeros(n, int)
@@ -162,8 +162,11 @@ def _check_tree(ref, leaf, max_depth, ex, depth_reported):
         d = ex["split_dim"][node]
         s = ex["split_val"][node]
         pts = ref[members].astype(np.float64)
-        var = pts.var(axis=0)                                    # numpy population variance
-        assert d == int(np.flatnonzero(var >= var.max() * (1 - 1e-9))[0])
+        if round_robin:
+            assert d == depth % 3                                # section 4.2 alternative
+        else:
+            var = pts.var(axis=0)                                # numpy population variance
+            assert d == int(np.flatnonzero(var >= var.max() * (1 - 1e-9))[0])
         m = count // 2
         keys_l = [(ref[p, d], p) for p in members[:m]]
         keys_r = [(ref[p, d], p) for p in members[m:]]
@@ -465,3 +468,33 @@ def test_voxel_degenerate_inputs(oracle_mod):
     assert oracle_mod.voxel_downsample(same, 1.0).shape == (1, 3)
     allnan = np.full((5, 3), np.nan, np.float32)
     assert oracle_mod.voxel_downsample(allnan, 1.0).shape == (0, 3)
+
+
+# ------------------------------------------------------------ round robin, section 6
+
+@pytest.mark.parametrize("name", ["grid", "clustered", "flat", "line"])
+def test_round_robin_tree_invariants_and_search(oracle_mod, name):
+    ref, q = _tie_clouds()[name]
+    tree = oracle_mod.KDTree(ref, 4, round_robin=True)
+    _check_tree(ref, 4, oracle_mod.DEPTH_CAP, tree.export(), tree.depth, round_robin=True)
+    i_t, d_t = tree.query(q)
+    i_b, d_b = oracle_mod.nn_brute(ref, q)
+    np.testing.assert_array_equal(i_t, i_b)
+    np.testing.assert_array_equal(d_t.view(np.uint32), d_b.view(np.uint32))
+
+
+def test_section6_regression_curve(oracle_mod):
+    """The page's simulation regression (section 6), at 40k points: a large
+    error on the first iteration, a steep drop within five, then a slow,
+    jump-free approach to the noise floor; the final motion near the truth."""
+    c = W.uniform200k_case(40_000)
+    tree = oracle_mod.KDTree(c.target, c.leaf_size)
+    r = oracle_mod.icp_align(tree, c.source, c.max_iter, c.eps, math.inf)
+    Ts = [x["T"] for x in r["trace"]] + [r["T"]]
+    rot = np.array([oracle_mod.rotation_error(T[:3, :3], c.T_gt[:3, :3]) for T in Ts])
+    tra = np.array([np.linalg.norm(T[:3, 3] - c.T_gt[:3, 3]) for T in Ts])
+    assert rot[5] < 0.1 * rot[0] and tra[5] < 0.2 * tra[0]
+    for k in range(5, len(rot) - 1):
+        assert rot[k + 1] <= rot[k] * 1.05 + 1e-6
+        assert tra[k + 1] <= tra[k] * 1.05 + 1e-6
+    assert rot[-1] < 1e-4 and tra[-1] < 1e-3

@@ -31,6 +31,12 @@ small parity tests while keeping the structure):
 5. ``large``    4M-point target, 2M-point source on the scene surfaces,
                 20 deg / 3 m offset, leaf 16, max correspondence 2.0 m then
                 0.3 m, 60 iterations per stage.
+6. ``uniform200k`` the simulation regression of the page's section 6: 200k
+                points uniform in [-25, 25]^3, source = target under a random
+                rigid motion (2 deg about a random axis, |t| = 0.2 m: inside
+                point-to-point ICP's basin for a 0.85 m point spacing) plus
+                N(0, voxel / 10) noise with voxel 0.1 m, leaf 16, 30
+                iterations, no distance rejection.
 """
 from __future__ import annotations
 
@@ -313,6 +319,18 @@ def scene_frames(n_frames: int, n_target: int = 100_000, n_source: int = 100_000
     return case, srcs, gts
 
 
+def uniform200k_case(n: int = 200_000) -> RegistrationCase:
+    r_tgt, r_pose, r_noise = _rngs(6, 3)
+    target = r_tgt.uniform(-25.0, 25.0, size=(n, 3))
+    R = axis_angle_matrix(random_unit_vector(r_pose), math.radians(2.0))
+    t = random_unit_vector(r_pose) * 0.2
+    T_gt = rigid(R, t)
+    src = _apply_inverse(T_gt, target) + r_noise.normal(0.0, 0.1 / 10.0, size=(n, 3))
+    target = _f32(target)
+    return RegistrationCase("uniform200k", target, _f32(src), T_gt, leaf_size=16, max_iter=30,
+                            eps=0.0, max_corr_dist=(math.inf,), extent=bbox_diagonal(target))
+
+
 def large_case(n_target: int = 4_000_000, n_source: int = 2_000_000) -> RegistrationCase:
     r_scene, r_tgt, r_src, r_pose = _rngs(5, 4)
     scene = make_scene(r_scene)
@@ -429,4 +447,5 @@ CASES = {
     "lidar": lidar_case,
     "gmm": gmm_case,
     "large": large_case,
+    "uniform200k": uniform200k_case,
 }
