@@ -289,7 +289,7 @@ int wait_published(const volatile unsigned long long* flag, unsigned long long s
 }
 
 int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, float* d2,
-             cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m, float* ms) {
+             cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m) {
   IcpPassParams p;
   std::memcpy(p.R, R, sizeof(p.R));
   std::memcpy(p.t, tr, sizeof(p.t));
@@ -305,16 +305,24 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
       reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
   if (int rc = wait_published(flag, p.seq, s)) return rc;
   std::atomic_thread_fence(std::memory_order_acquire);
-  if (ms != nullptr) {
-    *ms = 0.f;
-    if (ev0 && ev1) {
-      ICPNN_CUDA(cudaEventSynchronize(ev1));
-      ICPNN_CUDA(cudaEventElapsedTime(ms, ev0, ev1));
-    }
-  }
   double raw[kMomentSlots];
   std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
   decode_moments(raw, ps.src.shift, ps.shift_q, m);
+  return ICPNN_OK;
+}
+
+// Per-thread pool of timing events, created on first use and kept, so that
+// timing a registration costs two event records per pass and nothing else
+// until the elapsed times are read after the loop.
+thread_local std::vector<cudaEvent_t> tl_events;
+
+int timing_events(size_t count, cudaEvent_t** out) {
+  while (tl_events.size() < count) {
+    cudaEvent_t e = nullptr;
+    ICPNN_CUDA(cudaEventCreate(&e));
+    tl_events.push_back(e);
+  }
+  *out = tl_events.data();
   return ICPNN_OK;
 }
 
@@ -353,14 +361,6 @@ void transform_to_f32(const double T[16], float R[9], float t[3]) {
     t[i] = static_cast<float>(T[4 * i + 3]);
   }
 }
-
-struct EventPair {
-  cudaEvent_t a = nullptr, b = nullptr;
-  ~EventPair() {
-    if (a) cudaEventDestroy(a);
-    if (b) cudaEventDestroy(b);
-  }
-};
 
 }  // namespace
 }  // namespace icpnn
@@ -541,7 +541,7 @@ int icpnn_icp_step(const icpnn_tree* t, const float* src, int64_t n, const float
   if (int rc = pass_setup(t, src, n, max_corr_dist, false, s, sc, &ps)) return rc;
   PointOutputs po;
   if (int rc = bind_point_outputs(idx, dist2, n, sc, &po)) return rc;
-  if (int rc = pass_run(ps, R, tr, po.idx, po.d2, s, nullptr, nullptr, out, nullptr)) return rc;
+  if (int rc = pass_run(ps, R, tr, po.idx, po.d2, s, nullptr, nullptr, out)) return rc;
   if (int rc = copy_back(po, n, s)) return rc;
   if (out->n_nonfinite > 0)
     return fail(ICPNN_ERR_NONFINITE, "icp_step: " + std::to_string(out->n_nonfinite) +
@@ -636,11 +636,10 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   } else {
     for (int k = 0; k < 16; ++k) T[k] = (k % 5 == 0) ? 1.0 : 0.0;
   }
-  EventPair ev;
-  if ((flags & ICPNN_TRACE_TIMING) && trace_cap > 0) {
-    ICPNN_CUDA(cudaEventCreate(&ev.a));
-    ICPNN_CUDA(cudaEventCreate(&ev.b));
-  }
+  cudaEvent_t* ev = nullptr;
+  const int32_t timed = (flags & ICPNN_TRACE_TIMING) ? std::min(trace_cap, max_iter) : 0;
+  if (timed > 0)
+    if (int rc = timing_events(2 * static_cast<size_t>(timed), &ev)) return rc;
   Scratch sc(s);
   Pass ps;
   if (int rc = pass_setup(t, src, n_src, max_corr_dist, residual, s, sc, &ps)) return rc;
@@ -651,8 +650,10 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     float R32[9], t32[3];
     transform_to_f32(T, R32, t32);
     icpnn_moments m;
-    float ms = 0.f;
-    if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, ev.a, ev.b, &m, &ms)) return rc;
+    const bool time_it = k < timed;
+    if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, time_it ? ev[2 * k] : nullptr,
+                          time_it ? ev[2 * k + 1] : nullptr, &m))
+      return rc;
     if (m.n_nonfinite > 0)
       return fail(ICPNN_ERR_NONFINITE, "icp_align: " + std::to_string(m.n_nonfinite) +
                                            " source points have non-finite coordinates");
@@ -689,7 +690,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       r.mse = m.mse;
       r.sigma2 = sigma2;
       std::memcpy(r.T, T, sizeof(T));
-      r.kernel_ms = ms;
+      r.kernel_ms = 0.f;
       r.reserved = 0.f;
     }
     std::memcpy(T, Tn, sizeof(T));
@@ -700,10 +701,15 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     if (k >= 2 && std::fabs(mse_hist[1] - mse_hist[2]) < eps && std::fabs(mse_hist[0] - mse_hist[1]) < eps)
       break;
   }
+  if (timed > 0) {
+    const int32_t recorded = std::min(timed, done);
+    ICPNN_CUDA(cudaEventSynchronize(ev[2 * (recorded - 1) + 1]));
+    for (int32_t k = 0; k < recorded; ++k) ICPNN_CUDA(cudaEventElapsedTime(&trace[k].kernel_ms, ev[2 * k], ev[2 * k + 1]));
+  }
   float R32[9], t32[3];
   transform_to_f32(T, R32, t32);
   icpnn_moments fin;
-  if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, &fin, nullptr)) return rc;
+  if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, &fin)) return rc;
   std::memcpy(out_T, T, sizeof(T));
   *final_mse = fin.mse;
   *iters = done;

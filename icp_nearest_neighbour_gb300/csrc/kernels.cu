@@ -471,14 +471,26 @@ struct TreeView {
   uint32_t smem_slots;
 };
 
+// The running best as one 64-bit key (d2 bits << 32) | original index.  d2
+// is a sum of squares, never negative zero or NaN for a finite query, so its
+// IEEE bits order exactly like its values, and one unsigned 64-bit compare is
+// the lexicographic (d2, index) test of the exact-neighbour definition.  The
+// index field starts at INT_MAX, above every real index.
 struct Best {
-  float d2;
-  int32_t idx;   // original target index (INT_MAX: nothing found)
-  uint32_t slot; // position of that point's record
+  unsigned long long key;
+  uint32_t slot;  // position of the best point's record
+  __device__ __forceinline__ float d2() const { return __uint_as_float(static_cast<uint32_t>(key >> 32)); }
+  __device__ __forceinline__ int32_t idx() const { return static_cast<int32_t>(key & 0xffffffffu); }
 };
+__device__ __forceinline__ Best make_best(float d2) {
+  return Best{(static_cast<unsigned long long>(__float_as_uint(d2)) << 32) | 0x7fffffffull, 0u};
+}
 
+// One generic load: the top levels come from the shared-memory copy, the rest
+// from global memory, selected by pointer rather than by branch.
 __device__ __forceinline__ uint2 load_node(const TreeView& tv, uint32_t i) {
-  return i < tv.smem_slots ? tv.smem[i] : __ldg(&tv.nodes[i]);
+  const uint2* p = i < tv.smem_slots ? tv.smem : tv.nodes;
+  return p[i];
 }
 
 __device__ __forceinline__ float dist2(const float4& r, float qx, float qy, float qz) {
@@ -491,10 +503,9 @@ __device__ __forceinline__ float dist2(const float4& r, float qx, float qy, floa
 __device__ __forceinline__ void consider(const float4& r, uint32_t slot, float qx, float qy, float qz,
                                          Best& b) {
   const float d = dist2(r, qx, qy, qz);
-  const int32_t id = __float_as_int(r.w);
-  if (d < b.d2 || (d == b.d2 && id < b.idx)) {
-    b.d2 = d;
-    b.idx = id;
+  const unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d)) << 32) | __float_as_uint(r.w);
+  if (key < b.key) {
+    b.key = key;
     b.slot = slot;
   }
 }
@@ -526,7 +537,7 @@ __device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, f
       const float delta = __fsub_rn(qd, split);
       node = 2 * node + (qd < split ? 0u : 1u);
       ++depth;
-      if (__fmul_rn(delta, delta) <= b.d2) trail |= 1u << depth;
+      if (__fmul_rn(delta, delta) <= b.d2()) trail |= 1u << depth;
       nd = load_node(tv, node);
     }
     const uint32_t start = nd.x;
@@ -552,7 +563,7 @@ __device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, f
       depth = d;
       const uint2 parent = load_node(tv, node >> 1);
       nd = load_node(tv, node);
-      if (plane_bound(parent, qx, qy, qz) <= b.d2) break;
+      if (plane_bound(parent, qx, qy, qz) <= b.d2()) break;
     }
   }
 }
@@ -599,10 +610,10 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
       out_d2[slot] = __int_as_float(0x7fc00000);
       continue;
     }
-    Best b{__int_as_float(0x7f800000), INT_MAX, 0u};
+    Best b = make_best(__int_as_float(0x7f800000));
     search(tv, r.x, r.y, r.z, b);
-    out_idx[slot] = b.idx == INT_MAX ? -1 : b.idx;
-    out_d2[slot] = b.d2;
+    out_idx[slot] = b.idx() == INT_MAX ? -1 : b.idx();
+    out_d2[slot] = b.d2();
   }
 }
 
@@ -735,14 +746,14 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
         // starts with the rejection radius as its best distance (the page's
         // section 4.4 fuses max_dist into the tree query): it returns the
         // exact nearest point when one lies within the radius, else nothing.
-        Best b{kPerPoint ? __int_as_float(0x7f800000) : p.max_d2, INT_MAX, 0u};
+        Best b = make_best(kPerPoint ? __int_as_float(0x7f800000) : p.max_d2);
         search(tv, q[0], q[1], q[2], b);
-        idx = b.idx == INT_MAX ? -1 : b.idx;
-        d2 = b.d2;
-        if (b.idx != INT_MAX && b.d2 <= p.max_d2) {
+        idx = b.idx() == INT_MAX ? -1 : b.idx();
+        d2 = b.d2();
+        if (b.idx() != INT_MAX && b.d2() <= p.max_d2) {
           ++n_acc;
           matched = static_cast<int32_t>(b.slot);
-          add_pair(acc, s.x, s.y, s.z, __ldg(&pts[b.slot]), b.d2, p);
+          add_pair(acc, s.x, s.y, s.z, __ldg(&pts[b.slot]), b.d2(), p);
         }
       }
     }
@@ -1043,13 +1054,13 @@ __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
       float q[3];
       transform_point(p, sx, sy, sz, q);
       if (finite3(q[0], q[1], q[2])) {
-        Best b{__int_as_float(0x7f800000), INT_MAX, 0u};
+        Best b = make_best(__int_as_float(0x7f800000));
         search(tv, q[0], q[1], q[2], b);
-        idx = b.idx;
-        d2 = b.d2;
-        if (b.d2 <= p.max_d2) {
+        idx = b.idx();
+        d2 = b.d2();
+        if (b.d2() <= p.max_d2) {
           ++n_acc;
-          add_pair(acc, sx, sy, sz, __ldg(&pts[b.slot]), b.d2, p);
+          add_pair(acc, sx, sy, sz, __ldg(&pts[b.slot]), b.d2(), p);
         }
       }
     }
