@@ -251,15 +251,20 @@ struct Pass {
   uint32_t* counter = nullptr;
   MappedBuffer* mb = nullptr;
   int32_t* slot_of = nullptr;  // per Morton-ordered source record: matched slot or -1
+  uint32_t* leaf_of = nullptr; // per source record: leaf of the last best match (warm start)
   float shift_q[3] = {0, 0, 0};
   float max_d2 = INFINITY;
 };
 
 int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bool want_slots,
-               cudaStream_t s, Scratch& sc, Pass* ps) {
+               bool warm_start, cudaStream_t s, Scratch& sc, Pass* ps) {
   ps->tree = t;
   ps->n = n;
   if (want_slots) ICPNN_CUDA(sc.alloc(&ps->slot_of, n));
+  if (warm_start) {
+    ICPNN_CUDA(sc.alloc(&ps->leaf_of, n));
+    ICPNN_CUDA(cudaMemsetAsync(ps->leaf_of, 0, static_cast<size_t>(n) * sizeof(uint32_t), s));
+  }
   if (int rc = prepare_source(src, n, true, true, s, sc, &ps->src)) return rc;
   ps->grid = icp_pass_grid(*t, n);
   ICPNN_CUDA(sc.alloc(&ps->partials, static_cast<int64_t>(ps->grid) * kMomentSlots));
@@ -299,7 +304,7 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
   p.seq = ++ps.mb->seq;
   if (ev0) ICPNN_CUDA(cudaEventRecord(ev0, s));
   ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev,
-                             idx, d2, ps.slot_of, ps.grid, s));
+                             idx, d2, ps.slot_of, idx == nullptr ? ps.leaf_of : nullptr, ps.grid, s));
   if (ev1) ICPNN_CUDA(cudaEventRecord(ev1, s));
   const volatile unsigned long long* flag =
       reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
@@ -538,7 +543,7 @@ int icpnn_icp_step(const icpnn_tree* t, const float* src, int64_t n, const float
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Scratch sc(s);
   Pass ps;
-  if (int rc = pass_setup(t, src, n, max_corr_dist, false, s, sc, &ps)) return rc;
+  if (int rc = pass_setup(t, src, n, max_corr_dist, false, false, s, sc, &ps)) return rc;
   PointOutputs po;
   if (int rc = bind_point_outputs(idx, dist2, n, sc, &po)) return rc;
   if (int rc = pass_run(ps, R, tr, po.idx, po.d2, s, nullptr, nullptr, out)) return rc;
@@ -642,7 +647,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     if (int rc = timing_events(2 * static_cast<size_t>(timed), &ev)) return rc;
   Scratch sc(s);
   Pass ps;
-  if (int rc = pass_setup(t, src, n_src, max_corr_dist, residual, s, sc, &ps)) return rc;
+  if (int rc = pass_setup(t, src, n_src, max_corr_dist, residual, true, s, sc, &ps)) return rc;
 
   double mse_hist[3] = {0, 0, 0};
   int32_t done = 0;

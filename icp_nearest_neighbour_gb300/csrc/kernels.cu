@@ -510,12 +510,6 @@ __device__ __forceinline__ void consider(const float4& r, uint32_t slot, float q
   }
 }
 
-__device__ __forceinline__ float plane_bound(uint2 nd, float qx, float qy, float qz) {
-  const float qd = nd.y == 0 ? qx : (nd.y == 1 ? qy : qz);
-  const float delta = __fsub_rn(qd, __uint_as_float(nd.x));
-  return __fmul_rn(delta, delta);
-}
-
 // Exact nearest neighbour of a finite query point, depth first, near child
 // first.  Instead of a stack of pending far children the search keeps a
 // 32-bit trail: bit d is set while the far child at depth d of the current
@@ -527,45 +521,95 @@ __device__ __forceinline__ float plane_bound(uint2 nd, float qx, float qy, float
 // no local-memory stack.  (A restart trail in the sense of Laine, "Restart
 // trail for stackless BVH traversal", 2010; the heap numbering makes the
 // restart from the root unnecessary.)
-__device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, float qz, Best& b) {
-  uint32_t node = 1, depth = 0, trail = 0;
-  uint2 nd = load_node(tv, node);
+__device__ __forceinline__ void scan_leaf(const TreeView& tv, uint2 nd, float qx, float qy, float qz, Best& b) {
+  const uint32_t start = nd.x;
+  const uint32_t count = nd.y >> 2;
+  uint32_t k = 0;
+  for (; k + 4 <= count; k += 4) {
+    const float4 r0 = __ldg(&tv.pts[start + k]);
+    const float4 r1 = __ldg(&tv.pts[start + k + 1]);
+    const float4 r2 = __ldg(&tv.pts[start + k + 2]);
+    const float4 r3 = __ldg(&tv.pts[start + k + 3]);
+    consider(r0, start + k, qx, qy, qz, b);
+    consider(r1, start + k + 1, qx, qy, qz, b);
+    consider(r2, start + k + 2, qx, qy, qz, b);
+    consider(r3, start + k + 3, qx, qy, qz, b);
+  }
+  for (; k < count; ++k) consider(__ldg(&tv.pts[start + k]), start + k, qx, qy, qz, b);
+}
+
+// Lower bound for the subtree of `node` given its parent's record: 0 when the
+// query lies on node's side of the parent's splitting plane, else the squared
+// distance to that plane.
+__device__ __forceinline__ float sibling_bound(uint2 parent, uint32_t node, float qx, float qy, float qz) {
+  const float qd = parent.y == 0 ? qx : (parent.y == 1 ? qy : qz);
+  const float split = __uint_as_float(parent.x);
+  const bool same_side = ((node & 1u) == 0u) == (qd < split);
+  const float delta = __fsub_rn(qd, split);
+  return same_side ? 0.f : __fmul_rn(delta, delta);
+}
+
+// Exact nearest neighbour, optionally warm-started at a leaf (start > 1: the
+// leaf where this query's best point was found in the previous pass).
+// Returns the leaf holding the best point found by this search (0 if none).
+__device__ __forceinline__ uint32_t search_from(const TreeView& tv, float qx, float qy, float qz, Best& b,
+                                                uint32_t start) {
+  uint32_t node = 1, depth = 0, trail = 0, best_leaf = 0;
+  uint2 nd;
+  bool scanned = false;
+  if (start > 1) {
+    // Warm start: scan the leaf, then bound every sibling along its root path
+    // at once (independent loads), keeping the ones still within reach as
+    // pending; with the leaf they cover the whole tree, so the result is the
+    // same exact neighbour from any starting leaf.
+    node = start;
+    depth = 31u - __clz(start);
+    const unsigned long long before = b.key;
+    scan_leaf(tv, load_node(tv, node), qx, qy, qz, b);
+    if (b.key != before) best_leaf = node;
+#pragma unroll
+    for (uint32_t lvl = 1; lvl <= ICPNN_MAX_DEPTH; ++lvl) {
+      if (lvl <= depth) {
+        const uint32_t sib = (node >> (depth - lvl)) ^ 1u;
+        if (sibling_bound(load_node(tv, sib >> 1), sib, qx, qy, qz) <= b.d2()) trail |= 1u << lvl;
+      }
+    }
+    scanned = true;
+  } else {
+    nd = load_node(tv, node);
+  }
   for (;;) {
-    while ((nd.y & 3u) != kLeafTag) {
-      const float qd = nd.y == 0 ? qx : (nd.y == 1 ? qy : qz);
-      const float split = __uint_as_float(nd.x);
-      const float delta = __fsub_rn(qd, split);
-      node = 2 * node + (qd < split ? 0u : 1u);
-      ++depth;
-      if (__fmul_rn(delta, delta) <= b.d2()) trail |= 1u << depth;
-      nd = load_node(tv, node);
+    if (!scanned) {
+      while ((nd.y & 3u) != kLeafTag) {
+        const float qd = nd.y == 0 ? qx : (nd.y == 1 ? qy : qz);
+        const float split = __uint_as_float(nd.x);
+        const float delta = __fsub_rn(qd, split);
+        node = 2 * node + (qd < split ? 0u : 1u);
+        ++depth;
+        if (__fmul_rn(delta, delta) <= b.d2()) trail |= 1u << depth;
+        nd = load_node(tv, node);
+      }
+      const unsigned long long before = b.key;
+      scan_leaf(tv, nd, qx, qy, qz, b);
+      if (b.key != before) best_leaf = node;
     }
-    const uint32_t start = nd.x;
-    const uint32_t count = nd.y >> 2;
-    uint32_t k = 0;
-    for (; k + 4 <= count; k += 4) {
-      const float4 r0 = __ldg(&tv.pts[start + k]);
-      const float4 r1 = __ldg(&tv.pts[start + k + 1]);
-      const float4 r2 = __ldg(&tv.pts[start + k + 2]);
-      const float4 r3 = __ldg(&tv.pts[start + k + 3]);
-      consider(r0, start + k, qx, qy, qz, b);
-      consider(r1, start + k + 1, qx, qy, qz, b);
-      consider(r2, start + k + 2, qx, qy, qz, b);
-      consider(r3, start + k + 3, qx, qy, qz, b);
-    }
-    for (; k < count; ++k) consider(__ldg(&tv.pts[start + k]), start + k, qx, qy, qz, b);
-    // take up the deepest pending far child whose plane is still within reach
+    scanned = false;
+    // take up the deepest pending sibling still within reach of the best
     for (;;) {
-      if (trail == 0) return;
+      if (trail == 0) return best_leaf;
       const uint32_t d = 31u - __clz(trail);
       trail &= ~(1u << d);
       node = (node >> (depth - d)) ^ 1u;
       depth = d;
       const uint2 parent = load_node(tv, node >> 1);
       nd = load_node(tv, node);
-      if (plane_bound(parent, qx, qy, qz) <= b.d2()) break;
+      if (sibling_bound(parent, node, qx, qy, qz) <= b.d2()) break;
     }
   }
+}
+
+__device__ __forceinline__ void search(const TreeView& tv, float qx, float qy, float qz, Best& b) {
+  search_from(tv, qx, qy, qz, b, 1u);
 }
 
 // Work distribution of the search kernels: queries are taken in chunks of 32
@@ -719,7 +763,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
     const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
     const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
     unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
-    float* __restrict__ out_d2, int32_t* __restrict__ slot_of) {
+    float* __restrict__ out_d2, int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of) {
   extern __shared__ uint2 s_nodes[];
   stage_top(nodes, s_nodes, smem_slots);
   const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
@@ -747,7 +791,12 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
         // section 4.4 fuses max_dist into the tree query): it returns the
         // exact nearest point when one lies within the radius, else nothing.
         Best b = make_best(kPerPoint ? __int_as_float(0x7f800000) : p.max_d2);
-        search(tv, q[0], q[1], q[2], b);
+        if (leaf_of != nullptr) {
+          const uint32_t prev = leaf_of[i];
+          leaf_of[i] = search_from(tv, q[0], q[1], q[2], b, prev);
+        } else {
+          search(tv, q[0], q[1], q[2], b);
+        }
         idx = b.idx() == INT_MAX ? -1 : b.idx();
         d2 = b.d2();
         if (b.idx() != INT_MAX && b.d2() <= p.max_d2) {
@@ -894,8 +943,8 @@ int icp_pass_grid(const icpnn_tree& t, int64_t n) {
 
 cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
-                            double* out, int32_t* idx, float* dist2, int32_t* slot_of, int grid,
-                            cudaStream_t s) {
+                            double* out, int32_t* idx, float* dist2, int32_t* slot_of,
+                            uint32_t* leaf_of, int grid, cudaStream_t s) {
   const int slots = smem_slots_for(t);
   const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
@@ -903,16 +952,16 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
   const bool per_point = idx != nullptr || dist2 != nullptr;
   if (per_point && slot_of != nullptr)
     icp_pass_kernel<true, true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
-                                                              counter, out, idx, dist2, slot_of);
+                                                              counter, out, idx, dist2, slot_of, leaf_of);
   else if (per_point)
     icp_pass_kernel<true, false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
-                                                               counter, out, idx, dist2, nullptr);
+                                                               counter, out, idx, dist2, nullptr, leaf_of);
   else if (slot_of != nullptr)
     icp_pass_kernel<false, true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
-                                                               counter, out, nullptr, nullptr, slot_of);
+                                                               counter, out, nullptr, nullptr, slot_of, leaf_of);
   else
     icp_pass_kernel<false, false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
-                                                                counter, out, nullptr, nullptr, nullptr);
+                                                                counter, out, nullptr, nullptr, nullptr, leaf_of);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

@@ -62,11 +62,13 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
 // idx/dist2 optional.
 int icp_pass_grid(const icpnn_tree& t, int64_t n);
 // slot_of (optional): per source record, the record slot of its accepted
-// match, or -1.
+// match, or -1.  leaf_of (optional): per source record, the heap id of the
+// leaf where the previous pass found its best point (0: none); the search
+// starts there and overwrites it.
 cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
-                            double* out, int32_t* idx, float* dist2, int32_t* slot_of, int grid,
-                            cudaStream_t s);
+                            double* out, int32_t* idx, float* dist2, int32_t* slot_of,
+                            uint32_t* leaf_of, int grid, cudaStream_t s);
 
 // Residual pass of the residual rejection (same grid, partials, counter and
 // published result layout as the ICP pass): out[0] = pairs with
