@@ -51,7 +51,7 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
         if verbose_ptxas:
             cmd[1:1] = ["-Xptxas", "-v"]
     else:
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-I", INCLUDE,
+        cmd = ["g++", "-O3", "-std=c++17", "-fPIC", "-ffp-contract=off", "-I", INCLUDE,
                "-I", CSRC, "-I", "/usr/local/cuda/include", "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:

@@ -10,68 +10,22 @@
 // result is bit-identical to a single-frame icpnn_icp_align of it: the same
 // kernels run with the same grids, only their interleaving changes.
 //
-// Workers come from a process-wide pool that is created on first use and
-// never torn down; each worker keeps its own non-blocking stream per device
-// and its own mapped result buffer for the life of the process.
+// Workers come from the library's process-wide host pool; each worker keeps
+// its own non-blocking stream per device and its own mapped result buffer for
+// the life of the process.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <atomic>
 #include <condition_variable>
-#include <deque>
-#include <functional>
 #include <mutex>
 #include <string>
-#include <thread>
 #include <vector>
 
 #include "icpnn_internal.h"
 
 namespace icpnn {
 namespace {
-
-class WorkerPool {
- public:
-  void ensure(int n) {
-    std::lock_guard<std::mutex> lock(mu_);
-    while (threads_ < n) {
-      std::thread([this] { loop(); }).detach();
-      ++threads_;
-    }
-  }
-  void submit(std::function<void()> job) {
-    {
-      std::lock_guard<std::mutex> lock(mu_);
-      queue_.push_back(std::move(job));
-    }
-    cv_.notify_one();
-  }
-
- private:
-  void loop() {
-    for (;;) {
-      std::function<void()> job;
-      {
-        std::unique_lock<std::mutex> lock(mu_);
-        cv_.wait(lock, [this] { return !queue_.empty(); });
-        job = std::move(queue_.front());
-        queue_.pop_front();
-      }
-      job();
-    }
-  }
-  std::mutex mu_;
-  std::condition_variable cv_;
-  std::deque<std::function<void()>> queue_;
-  int threads_ = 0;
-};
-
-// Never destroyed: detached workers may still be parked on its condition
-// variable when the process exits.
-WorkerPool& pool() {
-  static WorkerPool* p = new WorkerPool();
-  return *p;
-}
 
 constexpr int kMaxDevices = 64;
 thread_local cudaStream_t tl_stream[kMaxDevices] = {};
@@ -135,9 +89,8 @@ extern "C" int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames,
   } sh;
   sh.msg.resize(static_cast<size_t>(n_frames));
 
-  pool().ensure(workers);
   for (int w = 0; w < workers; ++w) {
-    pool().submit([&, dev] {
+    pool_submit([&, dev] {
       cudaStream_t ws = nullptr;
       int rc = cudaSetDevice(dev) == cudaSuccess ? worker_stream(dev, &ws)
                                                  : fail(ICPNN_ERR_CUDA, "icp_align_batch: cudaSetDevice failed");
@@ -161,7 +114,7 @@ extern "C" int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames,
         ++sh.done;
       }
       sh.cv.notify_all();
-    });
+    }, workers);
   }
   {
     std::unique_lock<std::mutex> lock(sh.mu);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -72,6 +73,13 @@ void clear_error();
 // Host tree build (kdtree_build.cpp).
 int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t);
+
+// Process-wide host worker pool (host_pool.cpp).  pool_submit queues a job
+// (ensuring at least min_threads workers); parallel_for runs fn(0..tasks-1)
+// on the pool with the caller taking part, so nested use cannot deadlock;
+// the first exception a task throws is rethrown to the caller.
+void pool_submit(std::function<void()> job, int min_threads);
+void parallel_for(int tasks, const std::function<void(int)>& fn);
 
 // Host Kabsch solve (kabsch.cpp).  Returns ICPNN_OK or ICPNN_ERR_DEGENERATE.
 int kabsch_solve(const icpnn_moments& m, double T[16]);

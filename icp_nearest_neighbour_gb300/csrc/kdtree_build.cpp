@@ -1,20 +1,41 @@
 // Host KD-tree build ("Implementing ICP with CUDA-KDTree", sections 2.2, 2.3,
 // 4.2, 5.1, 5.2): split on the axis of largest variance (or, as the section
 // 4.2 alternative, round robin x, y, z by depth) at the median, stop at
-// leaf_size points or at the depth cap, partition in place with nth_element.
+// leaf_size points or at the depth cap.
 // The array partitioned is the 16-byte point records themselves (x, y, z,
-// original index), reserved once up front: every pass over a node reads
-// memory sequentially, and when the build ends the array is already the
-// leaf-ordered record array the device search reads.  Subtrees near the root
-// are built on separate threads; the result does not depend on the threading.
+// original index): every pass over a node reads memory sequentially, and when
+// the build ends the array is already the leaf-ordered record array the device
+// search reads.
+//
+// How a node is split.  The median under the (coordinate, index) order is
+// unique, so which records end up left of it does not depend on how it is
+// found.  A node of kBucketMin records or more finds it with one histogram
+// pass (records binned by where their coordinate falls in mean +- one standard
+// deviation of the node, which always holds the median; outside values clamp
+// to the end bins) and one scatter pass that writes the records below, inside
+// and above the median's bin to the node's range of a second buffer; an
+// nth_element over that bin alone then places the median.  The scatter pass
+// also sums the two children's coordinates and squares, so a child knows its
+// mean and variance without reading its records again.  Smaller nodes use
+// nth_element and one pass for the children's sums.
+//
+// Variance: sums of x - c and (x - c)^2 in double about the parent's mean c,
+// var = q/n - (s/n)^2.  The page fixes no formula; the rounding differs from
+// a two-pass sum by parts in 1e15, far inside the relative 1e-9 within which
+// axes count as tied (the lowest tied axis wins).
+//
+// Parallelism.  The subtrees of nodes near the root are tasks of the library's
+// host pool, and a node of two or more kChunk-record chunks runs its passes
+// chunk-parallel, summing per chunk and adding the chunk sums in chunk order.
+// The chunking depends on the node's size only, so the tree is the same on
+// every machine and thread count.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
-#include <exception>
-#include <future>
 #include <new>
 #include <thread>
+#include <vector>
 
 #include "icpnn_internal.h"
 
@@ -27,78 +48,268 @@ struct Rec {
 };
 static_assert(sizeof(Rec) == 16, "record must match the device float4 layout");
 
+constexpr int64_t kChunk = 16384;    // records per chunk of a parallel node pass
+constexpr int64_t kMaxChunks = 64;
+constexpr int64_t kBucketMin = 32;  // smaller nodes use nth_element
+
+int64_t chunks_for(int64_t count) { return std::min<int64_t>(kMaxChunks, count / kChunk); }
+
+// Sums over a set of records of x - c and (x - c)^2 per axis, c a fixed
+// centre, and the coordinate range per axis.
+struct Sums {
+  double n = 0.0;
+  double s[3] = {0.0, 0.0, 0.0};
+  double q[3] = {0.0, 0.0, 0.0};
+  float mn[3] = {INFINITY, INFINITY, INFINITY};
+  float mx[3] = {-INFINITY, -INFINITY, -INFINITY};
+  void add(const Rec& r, const double c[3]) {
+    n += 1.0;
+    for (int d = 0; d < 3; ++d) {
+      const double x = static_cast<double>(r.c[d]) - c[d];
+      s[d] += x;
+      q[d] += x * x;
+      mn[d] = std::min(mn[d], r.c[d]);
+      mx[d] = std::max(mx[d], r.c[d]);
+    }
+  }
+  void add(const Sums& o) {
+    n += o.n;
+    for (int d = 0; d < 3; ++d) {
+      s[d] += o.s[d];
+      q[d] += o.q[d];
+      mn[d] = std::min(mn[d], o.mn[d]);
+      mx[d] = std::max(mx[d], o.mx[d]);
+    }
+  }
+};
+
+// A node's mean and population variance per axis.  An axis on which all
+// coordinates are equal has variance exactly 0 (as a direct two-pass sum of
+// float coordinates gives), not the rounding left over by q/n - (s/n)^2.
+// `accurate` is false when the subtraction lost too much: the mean of
+// (x - c)^2 is more than 16 times the variance, i.e. c lies far from the
+// records; the caller then sums again about the mean just found.
+struct Moments {
+  double mean[3];
+  double var[3];
+  bool accurate;
+  static Moments from(const Sums& u, const double c[3]) {
+    Moments m;
+    m.accurate = true;
+    for (int d = 0; d < 3; ++d) {
+      const double a = u.s[d] / u.n;
+      const double q = u.q[d] / u.n;
+      m.mean[d] = c[d] + a;
+      m.var[d] = u.mn[d] == u.mx[d] ? 0.0 : std::max(0.0, q - a * a);
+      if (u.mn[d] != u.mx[d] && !(q <= 16.0 * m.var[d])) m.accurate = false;
+    }
+    return m;
+  }
+};
+
+bool rec_less(const Rec& a, const Rec& b, int axis) {
+  return a.c[axis] < b.c[axis] || (a.c[axis] == b.c[axis] && a.idx < b.idx);
+}
+
 struct Builder {
   int32_t leaf_size = 0;
   int32_t max_depth = 0;
-  Rec* recs = nullptr;  // point records, partitioned in place
+  Rec* buf[2] = {nullptr, nullptr};  // records ([0], the output) and scratch
   Node* heap = nullptr;
   int parallel_depth = 0;
   bool round_robin = false;  // axis = depth mod 3 instead of largest variance
   std::atomic<int64_t> n_nodes{0};
 
-  // Axis of largest population variance; axes within a relative 1e-9 of the
-  // largest are tied and the lowest of them wins.
-  int split_axis(int64_t lo, int64_t hi) const {
-    // two passes (mean, then squared deviations) with the three axes fused;
-    // each axis still sums its terms in index-array order
-    const double cnt = static_cast<double>(hi - lo);
-    double sum[3] = {0.0, 0.0, 0.0};
-    for (int64_t i = lo; i < hi; ++i) {
-      const float* p = recs[i].c;
-      sum[0] += p[0];
-      sum[1] += p[1];
-      sum[2] += p[2];
-    }
-    const double mean[3] = {sum[0] / cnt, sum[1] / cnt, sum[2] / cnt};
-    double ss[3] = {0.0, 0.0, 0.0};
-    for (int64_t i = lo; i < hi; ++i) {
-      const float* p = recs[i].c;
-      for (int d = 0; d < 3; ++d) {
-        const double e = p[d] - mean[d];
-        ss[d] += e * e;
-      }
-    }
-    double var[3];
-    for (int d = 0; d < 3; ++d) var[d] = ss[d] / cnt;
-    const double vmax = std::max(var[0], std::max(var[1], var[2]));
+  bool is_leaf(int64_t count, int depth) const { return count <= leaf_size || depth >= max_depth; }
+
+  // Axis of largest variance; axes within a relative 1e-9 of the largest are
+  // tied and the lowest of them wins.
+  static int widest_axis(const Moments& mo) {
+    const double vmax = std::max(mo.var[0], std::max(mo.var[1], mo.var[2]));
     for (int d = 0; d < 3; ++d)
-      if (var[d] >= vmax * (1.0 - 1e-9)) return d;
+      if (mo.var[d] >= vmax * (1.0 - 1e-9)) return d;
     return 0;
   }
 
-  void build(uint64_t node, int64_t lo, int64_t hi, int depth) {
+  // Splits node [lo, hi) of buf[b] at rank m on `axis`; returns the buffer
+  // that now holds the node (records of rank < m first, rank m at lo + m).
+  int split(int b, int64_t lo, int64_t hi, int64_t m, int axis, const Moments& mo) {
+    const int64_t count = hi - lo;
+    Rec* src = buf[b];
+    if (count < kBucketMin) {
+      std::nth_element(src + lo, src + lo + m, src + hi,
+                       [axis](const Rec& x, const Rec& y) { return rec_less(x, y, axis); });
+      return b;
+    }
+    Rec* dst = buf[b ^ 1];
+    int nb = 16;
+    while (nb < count / 4 && nb < 4096) nb *= 2;
+    const double sd = std::sqrt(mo.var[axis]);
+    const double base = mo.mean[axis] - sd;
+    // a spread too small to scale (or none) puts every record in one bin
+    const double scale = sd > 0.0 && nb / (2.0 * sd) < 1e300 ? nb / (2.0 * sd) : 0.0;
+    const double top = nb - 1;
+    // monotone in v: a lower bin never holds a larger coordinate
+    auto bin = [=](float v) {
+      const double x = (static_cast<double>(v) - base) * scale;
+      return static_cast<int>(std::min(std::max(x, 0.0), top));
+    };
+    const int64_t C = std::max<int64_t>(1, chunks_for(count));
+    auto chunk_lo = [=](int64_t k) { return lo + count * k / C; };
+    // per-thread scratch: split never runs twice at once on one thread
+    thread_local std::vector<int32_t> hist;
+    thread_local std::vector<int64_t> at;
+    hist.assign(static_cast<size_t>(C * nb), 0);
+    at.resize(static_cast<size_t>(3 * C));
+    int32_t* const hp = hist.data();
+    int64_t* const ap = at.data();
+    // Both passes first compute the bins of a block of records, then update
+    // the counters: when many records share a bin (the clamped ends), a
+    // counter update per record would wait for the previous one.
+    constexpr int kBlock = 64;
+    auto histogram = [=](int k) {
+      int32_t* h = hp + static_cast<int64_t>(k) * nb;
+      const int64_t b1 = chunk_lo(k + 1);
+      int32_t bins[kBlock];
+      for (int64_t i = chunk_lo(k); i < b1; i += kBlock) {
+        const int len = static_cast<int>(std::min<int64_t>(kBlock, b1 - i));
+        for (int t = 0; t < len; ++t) bins[t] = bin(src[i + t].c[axis]);
+        for (int t = 0; t < len; ++t) ++h[bins[t]];
+      }
+    };
+    if (C > 1) parallel_for(static_cast<int>(C), histogram); else histogram(0);
+    // the bin j holding rank m and the records below it
+    int64_t n_lt = 0, n_eq = 0;
+    int j = 0;
+    for (;; ++j) {
+      n_eq = 0;
+      for (int64_t k = 0; k < C; ++k) n_eq += hp[k * nb + j];
+      if (n_lt + n_eq > m || j == nb - 1) break;
+      n_lt += n_eq;
+    }
+    // write offsets per chunk of the three groups, chunks in order
+    int64_t o[3] = {lo, lo + n_lt, lo + n_lt + n_eq};
+    for (int64_t k = 0; k < C; ++k) {
+      const int32_t* h = hp + k * nb;
+      int64_t lt = 0;
+      for (int i = 0; i < j; ++i) lt += h[i];
+      const int64_t eq = h[j];
+      ap[3 * k] = o[0];
+      ap[3 * k + 1] = o[1];
+      ap[3 * k + 2] = o[2];
+      o[0] += lt;
+      o[1] += eq;
+      o[2] += chunk_lo(k + 1) - chunk_lo(k) - lt - eq;
+    }
+    auto scatter = [=](int k) {
+      int64_t w[3] = {ap[3 * k], ap[3 * k + 1], ap[3 * k + 2]};
+      const int64_t b1 = chunk_lo(k + 1);
+      int32_t grp[kBlock];
+      for (int64_t i = chunk_lo(k); i < b1; i += kBlock) {
+        const int len = static_cast<int>(std::min<int64_t>(kBlock, b1 - i));
+        for (int t = 0; t < len; ++t) {
+          const int g = bin(src[i + t].c[axis]);
+          grp[t] = (g >= j) + (g > j);
+        }
+        for (int t = 0; t < len; ++t) dst[w[grp[t]]++] = src[i + t];
+      }
+    };
+    if (C > 1) parallel_for(static_cast<int>(C), scatter); else scatter(0);
+    Rec* band = dst + lo + n_lt;
+    std::nth_element(band, band + (m - n_lt), band + n_eq,
+                     [axis](const Rec& x, const Rec& y) { return rec_less(x, y, axis); });
+    return b ^ 1;
+  }
+
+  // Sums about c of the records [lo, lo + m) and [lo + m, hi) of buf[b].
+  void child_sums(int b, int64_t lo, int64_t hi, int64_t m, const double c[3], Sums* left, Sums* right) const {
+    const int64_t count = hi - lo;
+    const Rec* r = buf[b];
+    const int64_t C = std::max<int64_t>(1, chunks_for(count));
+    Sums part_small[2];
+    std::vector<Sums> part_big(C > 1 ? static_cast<size_t>(2 * C) : 0);
+    Sums* part = C > 1 ? part_big.data() : part_small;
+    auto body = [=](int k) {
+      const int64_t b0 = lo + count * k / C, b1 = lo + count * (k + 1) / C, mid = lo + m;
+      Sums sl, sr;
+      for (int64_t i = b0; i < std::min(b1, mid); ++i) sl.add(r[i], c);
+      for (int64_t i = std::max(b0, mid); i < b1; ++i) sr.add(r[i], c);
+      part[2 * k] = sl;
+      part[2 * k + 1] = sr;
+    };
+    if (C > 1) parallel_for(static_cast<int>(C), body); else body(0);
+    for (int64_t k = 0; k < C; ++k) {
+      left->add(part[2 * k]);
+      right->add(part[2 * k + 1]);
+    }
+  }
+
+  // Builds the subtree of `node` over [lo, hi) of buf[b]; mo are the node's
+  // moments.  Leaves copy their records into buf[0] if they sit in buf[1].
+  void build(uint64_t node, int b, int64_t lo, int64_t hi, int depth, const Moments& mo) {
     n_nodes.fetch_add(1, std::memory_order_relaxed);
     const int64_t count = hi - lo;
-    if (count <= leaf_size || depth >= max_depth) {
+    if (is_leaf(count, depth)) {
+      if (b == 1) std::memcpy(buf[0] + lo, buf[1] + lo, static_cast<size_t>(count) * sizeof(Rec));
       heap[node].a = static_cast<uint32_t>(lo);
       heap[node].meta = kLeafTag | (static_cast<uint32_t>(count) << 2);
       return;
     }
-    const int axis = round_robin ? depth % 3 : split_axis(lo, hi);
+    const int axis = round_robin ? depth % 3 : widest_axis(mo);
     const int64_t m = count / 2;
-    std::nth_element(recs + lo, recs + lo + m, recs + hi, [axis](const Rec& a, const Rec& b) {
-      return a.c[axis] < b.c[axis] || (a.c[axis] == b.c[axis] && a.idx < b.idx);
-    });
-    const float split = recs[lo + m].c[axis];
+    const int nb = split(b, lo, hi, m, axis, mo);
+    const float split_value = buf[nb][lo + m].c[axis];
     uint32_t bits;
-    std::memcpy(&bits, &split, sizeof(bits));
+    std::memcpy(&bits, &split_value, sizeof(bits));
     heap[node].a = bits;
     heap[node].meta = static_cast<uint32_t>(axis);
-    if (depth < parallel_depth && count >= (1 << 13)) {
-      std::future<void> left;
-      try {
-        left = std::async(std::launch::async, [=] { build(2 * node, lo, lo + m, depth + 1); });
-      } catch (const std::exception&) {
-        build(2 * node, lo, lo + m, depth + 1);
-        build(2 * node + 1, lo + m, hi, depth + 1);
-        return;
-      }
-      build(2 * node + 1, lo + m, hi, depth + 1);
-      left.get();
-    } else {
-      build(2 * node, lo, lo + m, depth + 1);
-      build(2 * node + 1, lo + m, hi, depth + 1);
+    // the children's moments, unless both are leaves (which need none)
+    Moments ml{}, mr{};
+    if (!is_leaf(count - m, depth + 1)) {
+      Sums sl, sr;
+      child_sums(nb, lo, hi, m, mo.mean, &sl, &sr);
+      ml = Moments::from(sl, mo.mean);
+      mr = Moments::from(sr, mo.mean);
+      if (!ml.accurate) ml = moments_about(nb, lo, lo + m, ml.mean);
+      if (!mr.accurate) mr = moments_about(nb, lo + m, hi, mr.mean);
     }
+    if (depth < parallel_depth && count >= (1 << 13)) {
+      parallel_for(2, [&](int side) {
+        if (side == 0) build(2 * node, nb, lo, lo + m, depth + 1, ml);
+        else build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
+      });
+    } else {
+      build(2 * node, nb, lo, lo + m, depth + 1, ml);
+      build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
+    }
+  }
+
+  // Moments of the records [lo, hi) of buf[b] from sums about c.
+  Moments moments_about(int b, int64_t lo, int64_t hi, const double c[3]) const {
+    const int64_t count = hi - lo;
+    const int64_t C = std::max<int64_t>(1, chunks_for(count));
+    Sums part_small[1];
+    std::vector<Sums> part_big(C > 1 ? static_cast<size_t>(C) : 0);
+    Sums* part = C > 1 ? part_big.data() : part_small;
+    const Rec* r = buf[b];
+    auto body = [=](int k) {
+      Sums u;
+      const int64_t e = lo + count * (k + 1) / C;
+      for (int64_t i = lo + count * k / C; i < e; ++i) u.add(r[i], c);
+      part[k] = u;
+    };
+    if (C > 1) parallel_for(static_cast<int>(C), body); else body(0);
+    Sums tot;
+    for (int64_t k = 0; k < C; ++k) tot.add(part[k]);
+    return Moments::from(tot, c);
+  }
+
+  // Moments of the whole cloud: sums about the origin give the mean, then
+  // sums about the mean.
+  Moments root_moments(int64_t n) const {
+    const double zero[3] = {0.0, 0.0, 0.0};
+    const Moments first = moments_about(0, 0, n, zero);
+    return moments_about(0, 0, n, first.mean);
   }
 };
 
@@ -119,15 +330,50 @@ int32_t tree_depth(int64_t n, int32_t leaf_size, int32_t max_depth) {
 
 int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t) {
-  for (int64_t i = 0; i < 3 * n; ++i)
-    if (!std::isfinite(xyz[i]))
-      return fail(ICPNN_ERR_NONFINITE, "kdtree_build: non-finite coordinate at point " +
-                                           std::to_string(i / 3));
-  const int32_t depth = tree_depth(n, leaf_size, max_depth);
-  const int64_t largest_leaf = (n + (int64_t{1} << depth) - 1) >> depth;
-  if (largest_leaf >= (int64_t{1} << 30))
-    return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: a leaf would hold 2^30 points or more");
+  // one pass, chunked over the pool: finiteness check, records and bounding box
+  const int64_t C = std::max<int64_t>(1, std::min<int64_t>(kMaxChunks, n / (4 * kChunk)));
   try {
+    std::vector<int64_t> first_bad(static_cast<size_t>(C), -1);
+    std::vector<float> box(static_cast<size_t>(6 * C));
+    const int32_t depth = tree_depth(n, leaf_size, max_depth);
+    const int64_t largest_leaf = (n + (int64_t{1} << depth) - 1) >> depth;
+    if (largest_leaf >= (int64_t{1} << 30))
+      return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: a leaf would hold 2^30 points or more");
+    t->records.resize(static_cast<size_t>(4 * n));
+    Rec* recs = reinterpret_cast<Rec*>(t->records.data());
+    parallel_for(static_cast<int>(C), [&](int c) {
+      float lo[3] = {INFINITY, INFINITY, INFINITY};
+      float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+      for (int64_t i = n * c / C; i < n * (c + 1) / C; ++i) {
+        for (int d = 0; d < 3; ++d) {
+          const float v = xyz[3 * i + d];
+          if (!std::isfinite(v)) {
+            first_bad[static_cast<size_t>(c)] = i;
+            return;
+          }
+          recs[i].c[d] = v;
+          lo[d] = std::min(lo[d], v);
+          hi[d] = std::max(hi[d], v);
+        }
+        recs[i].idx = static_cast<int32_t>(i);
+      }
+      for (int d = 0; d < 3; ++d) {
+        box[static_cast<size_t>(6 * c + d)] = lo[d];
+        box[static_cast<size_t>(6 * c + 3 + d)] = hi[d];
+      }
+    });
+    for (int64_t c = 0; c < C; ++c)
+      if (first_bad[static_cast<size_t>(c)] >= 0)
+        return fail(ICPNN_ERR_NONFINITE, "kdtree_build: non-finite coordinate at point " +
+                                             std::to_string(first_bad[static_cast<size_t>(c)]));
+    for (int d = 0; d < 3; ++d) {
+      t->bbox_lo[d] = INFINITY;
+      t->bbox_hi[d] = -INFINITY;
+      for (int64_t c = 0; c < C; ++c) {
+        t->bbox_lo[d] = std::min(t->bbox_lo[d], box[static_cast<size_t>(6 * c + d)]);
+        t->bbox_hi[d] = std::max(t->bbox_hi[d], box[static_cast<size_t>(6 * c + 3 + d)]);
+      }
+    }
     t->n = n;
     t->leaf_size = leaf_size;
     t->max_depth = max_depth;
@@ -135,35 +381,20 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     t->depth = depth;
     t->heap_slots = int64_t{1} << (depth + 1);
     t->nodes.assign(static_cast<size_t>(t->heap_slots), Node{0u, 0u});
-    t->records.resize(static_cast<size_t>(4 * n));
-    Rec* recs = reinterpret_cast<Rec*>(t->records.data());
-    float lo[3] = {INFINITY, INFINITY, INFINITY};
-    float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
-    for (int64_t i = 0; i < n; ++i) {
-      for (int d = 0; d < 3; ++d) {
-        const float v = xyz[3 * i + d];
-        recs[i].c[d] = v;
-        lo[d] = std::min(lo[d], v);
-        hi[d] = std::max(hi[d], v);
-      }
-      recs[i].idx = static_cast<int32_t>(i);
-    }
-    for (int d = 0; d < 3; ++d) {
-      t->bbox_lo[d] = lo[d];
-      t->bbox_hi[d] = hi[d];
-    }
 
+    std::vector<Rec> temp(static_cast<size_t>(n));
     Builder b;
     b.leaf_size = leaf_size;
     b.max_depth = max_depth;
-    b.recs = recs;
+    b.buf[0] = recs;
+    b.buf[1] = temp.data();
     b.heap = t->nodes.data();
     b.round_robin = round_robin;
     const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
     int pd = 0;
     while ((1u << pd) < 4 * hw && pd < 8) ++pd;
     b.parallel_depth = pd;
-    b.build(1, 0, n, 0);
+    b.build(1, 0, 0, n, 0, b.root_moments(n));
     t->n_nodes = b.n_nodes.load();
   } catch (const std::bad_alloc&) {
     return fail(ICPNN_ERR_NO_MEMORY, "kdtree_build: host allocation failed");

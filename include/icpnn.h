@@ -162,7 +162,7 @@ int icpnn_nn_query(const icpnn_tree* tree, const float* xyz, int64_t n, int32_t*
 int icpnn_voxel_downsample(const float* xyz, int64_t n, float voxel_size, float* out_xyz, int64_t* out_n,
                            void* stream);
 
-/* ------------------------------------------------------------------ ICP --/* ------------------------------------------------------------------ ICP --
+/* ------------------------------------------------------------------ ICP --
  * Moments of one correspondence pass (page sections 2.1, 3.3, 4.4): the
  * original source points s_i whose transformed image R s_i + t has a nearest
  * target point q_i within the maximum distance are "accepted";

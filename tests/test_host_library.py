@@ -77,6 +77,40 @@ def test_round_robin_tree_matches_oracle_tree(lib, oracle_mod, name):
     assert _leaf_sets(ex) == _leaf_sets(oex)
 
 
+def _big_tree_clouds():
+    """Clouds large enough that the top nodes are split chunk-parallel and by
+    binned selection, with the distributions that stress it: surface samples,
+    tight clusters (most of a node in one bin), heavy coordinate ties, and a
+    zero-spread axis."""
+    rng = np.random.default_rng(77)
+    centres = rng.uniform(-30, 30, (5, 3))
+    clustered = W.gaussian_mixture(90_000, rng, centres, np.array([0.001, 0.01, 0.5, 2.0, 0.0001]))
+    coarse = np.round(rng.normal(size=(70_000, 3)) * 4).astype(np.float32) * 0.25
+    flat = np.c_[rng.uniform(-5, 5, (60_000, 2)), np.zeros(60_000)].astype(np.float32)
+    return {
+        "scene100k": (W.scene_case().target, 12),
+        "lidar": (W.lidar_case().target, 8),
+        "clustered": (clustered, 10),
+        "coarse_ties": (coarse, 4),
+        "flat": (flat, 16),
+    }
+
+
+@pytest.mark.parametrize("round_robin", [False, True])
+@pytest.mark.parametrize("name", list(_big_tree_clouds()))
+def test_large_tree_matches_oracle_tree(lib, oracle_mod, name, round_robin):
+    pts, leaf = _big_tree_clouds()[name]
+    t = lib.kdtree_build(pts, leaf, round_robin=round_robin)
+    o = oracle_mod.KDTree(pts, leaf, round_robin=round_robin)
+    ex, oex = lib.kdtree_export(t), o.export()
+    for k in ("split_val", "split_dim", "left", "right", "start", "end"):
+        np.testing.assert_array_equal(ex[k], oex[k], err_msg=k)
+    assert _leaf_sets(ex) == _leaf_sets(oex)
+    # repeated builds give the same leaf order, whatever the thread timing
+    np.testing.assert_array_equal(lib.kdtree_export(lib.kdtree_build(pts, leaf, round_robin=round_robin))
+                                  ["leaf_index"], ex["leaf_index"])
+
+
 def test_tree_depth_cap(lib, oracle_mod):
     pts = W.uniform_cloud(3000, 4)
     t = lib.kdtree_build(pts, 1, max_depth=5)
