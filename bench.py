@@ -51,7 +51,7 @@ ICP_BYTES_PER_QUERY = 1922.64
 # from ncu captures of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum): 3.59 MB on the first pass, 3.90 MB on a converged
 # pass.  None whenever the kernel has changed since the last capture.
-ICP_PASS_DRAM_BYTES = 3.75e6
+ICP_PASS_DRAM_BYTES = None
 
 SLOWDOWN_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 

@@ -427,11 +427,16 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   }
   Node* nodes = nullptr;
   float* pts = nullptr;
+  // nodes and boxes share one allocation; heap_slots >= 2 is a power of two,
+  // so the boxes start 16-byte aligned
   const size_t nb = static_cast<size_t>(t->heap_slots) * sizeof(Node);
+  const size_t bb = static_cast<size_t>(t->heap_slots) * 8 * sizeof(float);
   const size_t pb = static_cast<size_t>(t->n) * 4 * sizeof(float);
-  cudaError_t e = cudaMalloc(&nodes, nb);
+  cudaError_t e = cudaMalloc(&nodes, nb + bb);
+  float* boxes = nodes ? reinterpret_cast<float*>(reinterpret_cast<char*>(nodes) + nb) : nullptr;
   if (e == cudaSuccess) e = cudaMalloc(&pts, pb);
   if (e == cudaSuccess) e = cudaMemcpyAsync(nodes, t->nodes.data(), nb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(boxes, t->boxes.data(), bb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pts, t->records.data(), pb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
@@ -443,6 +448,7 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   }
   t->dev.device = cur;
   t->dev.nodes = nodes;
+  t->dev.boxes = boxes;
   t->dev.points = pts;
   return ICPNN_OK;
 }

@@ -27,6 +27,11 @@ namespace icpnn {
 //   leaf : a = first point record,            meta = 3 | (count << 2)
 // Slot 0 is unused (zeroed).
 //
+// Beside the nodes, every node has the tight bounding box of its points (two
+// float4, lo and hi).  The search keeps the page's splitting-plane test and
+// adds the box test where it prunes most: before it takes up a pending sibling
+// subtree and before it scans a leaf it descended to.
+//
 // Points are stored in leaf order as float4 records {x, y, z, index bits}:
 // one 16-byte load returns both the coordinates and the original target index
 // (the page's leaf_index indirection, section 3.2, disappears).
@@ -43,7 +48,8 @@ inline bool node_is_leaf(const Node& n) { return (n.meta & 3u) == kLeafTag; }
 
 struct DeviceTree {
   int device = -1;
-  Node* nodes = nullptr;      // heap_slots entries
+  Node* nodes = nullptr;      // heap_slots entries; the boxes follow in the same allocation
+  float* boxes = nullptr;     // heap_slots x 8 floats
   float* points = nullptr;    // n float4 records (x, y, z, index bits)
 };
 
@@ -61,6 +67,9 @@ struct icpnn_tree {
   float bbox_hi[3] = {0, 0, 0};
   std::vector<icpnn::Node> nodes;   // heap layout, heap_slots entries
   std::vector<float> records;       // 4 floats per point, leaf order
+  // Tight bounding box of each node's points, 8 floats per heap slot:
+  // lo.x, lo.y, lo.z, 0, hi.x, hi.y, hi.z, 0 (unused slots zero).
+  std::vector<float> boxes;
   icpnn::DeviceTree dev;
 };
 

@@ -24,6 +24,10 @@
 // a two-pass sum by parts in 1e15, far inside the relative 1e-9 within which
 // axes count as tied (the lowest tied axis wins).
 //
+// Each node also gets the tight bounding box of its points (leaves from their
+// records, inner nodes as the union of their children's) for the search's
+// box test.
+//
 // Parallelism.  The subtrees of nodes near the root are tasks of the library's
 // host pool, and a node of two or more kChunk-record chunks runs its passes
 // chunk-parallel, summing per chunk and adding the chunk sums in chunk order.
@@ -116,6 +120,7 @@ struct Builder {
   int32_t max_depth = 0;
   Rec* buf[2] = {nullptr, nullptr};  // records ([0], the output) and scratch
   Node* heap = nullptr;
+  float* box = nullptr;  // 8 floats per heap slot
   int parallel_depth = 0;
   bool round_robin = false;  // axis = depth mod 3 instead of largest variance
   std::atomic<int64_t> n_nodes{0};
@@ -253,6 +258,16 @@ struct Builder {
       if (b == 1) std::memcpy(buf[0] + lo, buf[1] + lo, static_cast<size_t>(count) * sizeof(Rec));
       heap[node].a = static_cast<uint32_t>(lo);
       heap[node].meta = kLeafTag | (static_cast<uint32_t>(count) << 2);
+      float* bx = box + 8 * node;
+      for (int d = 0; d < 3; ++d) {
+        bx[d] = INFINITY;
+        bx[4 + d] = -INFINITY;
+      }
+      for (int64_t i = lo; i < hi; ++i)
+        for (int d = 0; d < 3; ++d) {
+          bx[d] = std::min(bx[d], buf[0][i].c[d]);
+          bx[4 + d] = std::max(bx[4 + d], buf[0][i].c[d]);
+        }
       return;
     }
     const int axis = round_robin ? depth % 3 : widest_axis(mo);
@@ -281,6 +296,13 @@ struct Builder {
     } else {
       build(2 * node, nb, lo, lo + m, depth + 1, ml);
       build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
+    }
+    float* bx = box + 8 * node;
+    const float* l = box + 16 * node;
+    const float* r = l + 8;
+    for (int d = 0; d < 3; ++d) {
+      bx[d] = std::min(l[d], r[d]);
+      bx[4 + d] = std::max(l[4 + d], r[4 + d]);
     }
   }
 
@@ -381,6 +403,7 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     t->depth = depth;
     t->heap_slots = int64_t{1} << (depth + 1);
     t->nodes.assign(static_cast<size_t>(t->heap_slots), Node{0u, 0u});
+    t->boxes.assign(static_cast<size_t>(8 * t->heap_slots), 0.f);
 
     std::vector<Rec> temp(static_cast<size_t>(n));
     Builder b;
@@ -389,6 +412,7 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     b.buf[0] = recs;
     b.buf[1] = temp.data();
     b.heap = t->nodes.data();
+    b.box = t->boxes.data();
     b.round_robin = round_robin;
     const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
     int pd = 0;

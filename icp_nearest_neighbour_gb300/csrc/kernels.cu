@@ -466,6 +466,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const float* __restric
 
 struct TreeView {
   const uint2* __restrict__ nodes;   // heap, 1-based
+  const float4* __restrict__ boxes;  // per heap slot: lo, hi (tight box of the node's points)
   const float4* __restrict__ pts;    // leaf-ordered records
   const uint2* smem;                 // copy of heap slots [0, smem_slots)
   uint32_t smem_slots;
@@ -549,9 +550,64 @@ __device__ __forceinline__ float sibling_bound(uint2 parent, uint32_t node, floa
   return same_side ? 0.f : __fmul_rn(delta, delta);
 }
 
+// Lower bound for every point of a node: the squared distance from the query
+// to the node's box, with the rounding of dist2 (per-axis offset rounded,
+// squared, summed as (x + y) + z).  Rounding is monotone, so no point in the
+// box has a smaller dist2, and a node whose bound exceeds the best distance
+// cannot hold an equal or better point.
+__device__ __forceinline__ float box_dist2(const float4& lo, const float4& hi, float qx, float qy, float qz) {
+  const float ox = fmaxf(fmaxf(__fsub_rn(lo.x, qx), __fsub_rn(qx, hi.x)), 0.f);
+  const float oy = fmaxf(fmaxf(__fsub_rn(lo.y, qy), __fsub_rn(qy, hi.y)), 0.f);
+  const float oz = fmaxf(fmaxf(__fsub_rn(lo.z, qz), __fsub_rn(qz, hi.z)), 0.f);
+  return __fadd_rn(__fadd_rn(__fmul_rn(ox, ox), __fmul_rn(oy, oy)), __fmul_rn(oz, oz));
+}
+__device__ __forceinline__ float box_bound(const TreeView& tv, uint32_t node, float qx, float qy, float qz) {
+  return box_dist2(__ldg(&tv.boxes[2 * node]), __ldg(&tv.boxes[2 * node + 1]), qx, qy, qz);
+}
+
+// Scan a leaf reached by descent if its box is within reach.  The box and the
+// leaf's first records are fetched together, so the test adds no round trip
+// when it passes.
+__device__ __forceinline__ void scan_leaf_boxed(const TreeView& tv, uint32_t node, uint2 nd, float qx, float qy,
+                                                float qz, Best& b) {
+  const uint32_t start = nd.x;
+  const uint32_t count = nd.y >> 2;  // >= 1
+  const float4 lo = __ldg(&tv.boxes[2 * node]);
+  const float4 hi = __ldg(&tv.boxes[2 * node + 1]);
+  const float4 r0 = __ldg(&tv.pts[start]);
+  const float4 r1 = count > 1 ? __ldg(&tv.pts[start + 1]) : r0;
+  const float4 r2 = count > 2 ? __ldg(&tv.pts[start + 2]) : r0;
+  const float4 r3 = count > 3 ? __ldg(&tv.pts[start + 3]) : r0;
+  if (box_dist2(lo, hi, qx, qy, qz) > b.d2()) return;
+  consider(r0, start, qx, qy, qz, b);
+  if (count > 1) consider(r1, start + 1, qx, qy, qz, b);
+  if (count > 2) consider(r2, start + 2, qx, qy, qz, b);
+  if (count > 3) consider(r3, start + 3, qx, qy, qz, b);
+  uint32_t k = 4;
+  for (; k + 4 <= count; k += 4) {
+    const float4 s0 = __ldg(&tv.pts[start + k]);
+    const float4 s1 = __ldg(&tv.pts[start + k + 1]);
+    const float4 s2 = __ldg(&tv.pts[start + k + 2]);
+    const float4 s3 = __ldg(&tv.pts[start + k + 3]);
+    consider(s0, start + k, qx, qy, qz, b);
+    consider(s1, start + k + 1, qx, qy, qz, b);
+    consider(s2, start + k + 2, qx, qy, qz, b);
+    consider(s3, start + k + 3, qx, qy, qz, b);
+  }
+  for (; k < count; ++k) consider(__ldg(&tv.pts[start + k]), start + k, qx, qy, qz, b);
+}
+
 // Exact nearest neighbour, optionally warm-started at a leaf (start > 1: the
 // leaf where this query's best point was found in the previous pass).
 // Returns the leaf holding the best point found by this search (0 if none).
+// The descent takes the near side of each splitting plane (8-byte node loads);
+// the far child is recorded as pending only if its plane and its box are both
+// within reach, a pending sibling is taken up if its plane still is, and a
+// leaf reached by descent is scanned only if its box is.  For points off a
+// sampled surface -- every query of an early ICP pass, or a scan against
+// another scan -- the boxes are far tighter than the planes (a cell of a flat
+// region is unbounded across it): several-fold fewer leaves and pending
+// siblings.
 __device__ __forceinline__ uint32_t search_from(const TreeView& tv, float qx, float qy, float qz, Best& b,
                                                 uint32_t start) {
   uint32_t node = 1, depth = 0, trail = 0, best_leaf = 0;
@@ -559,9 +615,9 @@ __device__ __forceinline__ uint32_t search_from(const TreeView& tv, float qx, fl
   bool scanned = false;
   if (start > 1) {
     // Warm start: scan the leaf, then bound every sibling along its root path
-    // at once (independent loads), keeping the ones still within reach as
-    // pending; with the leaf they cover the whole tree, so the result is the
-    // same exact neighbour from any starting leaf.
+    // by its box at once (independent loads), keeping the ones still within
+    // reach as pending; with the leaf they cover the whole tree, so the result
+    // is the same exact neighbour from any starting leaf.
     node = start;
     depth = 31u - __clz(start);
     const unsigned long long before = b.key;
@@ -571,11 +627,12 @@ __device__ __forceinline__ uint32_t search_from(const TreeView& tv, float qx, fl
     for (uint32_t lvl = 1; lvl <= ICPNN_MAX_DEPTH; ++lvl) {
       if (lvl <= depth) {
         const uint32_t sib = (node >> (depth - lvl)) ^ 1u;
-        if (sibling_bound(load_node(tv, sib >> 1), sib, qx, qy, qz) <= b.d2()) trail |= 1u << lvl;
+        if (box_bound(tv, sib, qx, qy, qz) <= b.d2()) trail |= 1u << lvl;
       }
     }
     scanned = true;
   } else {
+    if (box_bound(tv, 1u, qx, qy, qz) > b.d2()) return 0u;  // nothing within the initial radius
     nd = load_node(tv, node);
   }
   for (;;) {
@@ -584,13 +641,18 @@ __device__ __forceinline__ uint32_t search_from(const TreeView& tv, float qx, fl
         const float qd = nd.y == 0 ? qx : (nd.y == 1 ? qy : qz);
         const float split = __uint_as_float(nd.x);
         const float delta = __fsub_rn(qd, split);
-        node = 2 * node + (qd < split ? 0u : 1u);
+        const uint32_t near = 2 * node + (qd < split ? 0u : 1u);
+        const uint2 next = load_node(tv, near);
         ++depth;
-        if (__fmul_rn(delta, delta) <= b.d2()) trail |= 1u << depth;
-        nd = load_node(tv, node);
+        // the far child becomes pending only if both its plane and its box
+        // are within reach (the box loads overlap the near child's load)
+        if (__fmul_rn(delta, delta) <= b.d2() && box_bound(tv, near ^ 1u, qx, qy, qz) <= b.d2())
+          trail |= 1u << depth;
+        node = near;
+        nd = next;
       }
       const unsigned long long before = b.key;
-      scan_leaf(tv, nd, qx, qy, qz, b);
+      scan_leaf_boxed(tv, node, nd, qx, qy, qz, b);
       if (b.key != before) best_leaf = node;
     }
     scanned = false;
@@ -603,6 +665,8 @@ __device__ __forceinline__ uint32_t search_from(const TreeView& tv, float qx, fl
       depth = d;
       const uint2 parent = load_node(tv, node >> 1);
       nd = load_node(tv, node);
+      // the box passed when the sibling was recorded; the best may have
+      // shrunk since, so the cheap plane test is repeated
       if (sibling_bound(parent, node, qx, qy, qz) <= b.d2()) break;
     }
   }
@@ -636,13 +700,14 @@ __device__ __forceinline__ void stage_top(const uint2* __restrict__ nodes, uint2
 // ------------------------------------------------------------ NN query --
 
 __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ nodes,
+                                                      const float4* __restrict__ boxes,
                                                       const float4* __restrict__ pts, int smem_slots,
                                                       const float4* __restrict__ q, int64_t n,
                                                       int32_t* __restrict__ out_idx,
                                                       float* __restrict__ out_d2) {
   extern __shared__ uint2 s_nodes[];
   stage_top(nodes, s_nodes, smem_slots);
-  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+  const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
   const int lane = threadIdx.x & 31;
   for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
     const int64_t i = c * 32 + lane;
@@ -760,13 +825,13 @@ __device__ __forceinline__ void transform_point(const IcpPassParams& p, float sx
 
 template <bool kPerPoint, bool kSlot>
 __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
-    const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
-    const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
+    const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
+    int smem_slots, const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
     unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
     float* __restrict__ out_d2, int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of) {
   extern __shared__ uint2 s_nodes[];
   stage_top(nodes, s_nodes, smem_slots);
-  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+  const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
 
   float acc[16];
 #pragma unroll
@@ -928,6 +993,7 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nn_kernel, kThreads, smem);
   const int grid = blocks_for(n, kThreads, std::max(1, per_sm) * num_sms());
   nn_kernel<<<grid, kThreads, smem, s>>>(reinterpret_cast<const uint2*>(t.dev.nodes),
+                                          reinterpret_cast<const float4*>(t.dev.boxes),
                                           reinterpret_cast<const float4*>(t.dev.points), slots,
                                           queries, n, idx, dist2);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
@@ -948,19 +1014,20 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
   const int slots = smem_slots_for(t);
   const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
+  const float4* boxes = reinterpret_cast<const float4*>(t.dev.boxes);
   const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
   const bool per_point = idx != nullptr || dist2 != nullptr;
   if (per_point && slot_of != nullptr)
-    icp_pass_kernel<true, true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+    icp_pass_kernel<true, true><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
                                                               counter, out, idx, dist2, slot_of, leaf_of);
   else if (per_point)
-    icp_pass_kernel<true, false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+    icp_pass_kernel<true, false><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
                                                                counter, out, idx, dist2, nullptr, leaf_of);
   else if (slot_of != nullptr)
-    icp_pass_kernel<false, true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+    icp_pass_kernel<false, true><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
                                                                counter, out, nullptr, nullptr, slot_of, leaf_of);
   else
-    icp_pass_kernel<false, false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, src, n, p, partials,
+    icp_pass_kernel<false, false><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
                                                                 counter, out, nullptr, nullptr, nullptr, leaf_of);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
@@ -1077,15 +1144,15 @@ namespace {
 
 template <bool kPerPoint>
 __global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
-    const uint2* __restrict__ nodes, const float4* __restrict__ pts, int smem_slots,
-    const float* __restrict__ xyz, int64_t n, IcpPassParams p, double* __restrict__ scratch,
+    const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
+    int smem_slots, const float* __restrict__ xyz, int64_t n, IcpPassParams p, double* __restrict__ scratch,
     int32_t* __restrict__ out_idx, float* __restrict__ out_d2) {
   extern __shared__ uint2 s_nodes[];
   double* partials = scratch;
   double* result = scratch + kNoAllocResult;
   unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kNoAllocCounter);
   stage_top(nodes, s_nodes, smem_slots);
-  const TreeView tv{nodes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+  const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
 
   float acc[16];
 #pragma unroll
@@ -1151,12 +1218,13 @@ cudaError_t launch_icp_pass_inplace(const icpnn_tree& t, const float* xyz, int64
   const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
   const int grid = static_cast<int>((n + kThreads - 1) / kThreads);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
+  const float4* boxes = reinterpret_cast<const float4*>(t.dev.boxes);
   const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
   if (idx != nullptr)
-    icp_pass_inplace_kernel<true><<<grid, kThreads, smem, s>>>(nodes, pts, slots, xyz, n, p, scratch,
+    icp_pass_inplace_kernel<true><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, xyz, n, p, scratch,
                                                                idx, dist2);
   else
-    icp_pass_inplace_kernel<false><<<grid, kThreads, smem, s>>>(nodes, pts, slots, xyz, n, p, scratch,
+    icp_pass_inplace_kernel<false><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, xyz, n, p, scratch,
                                                                 nullptr, nullptr);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
