@@ -782,13 +782,17 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     double s = 0.0;
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) s += s_fin[g][threadIdx.x];
-    out[threadIdx.x] = s;
-    if (kPublish) __threadfence_system();
+    s_fin[0][threadIdx.x] = s;  // row 0 was read above by this thread only
   }
-  if (threadIdx.x == 0) *counter = 0u;
-  if (kPublish) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
+  __syncthreads();
+  // One thread stores the result and, after one system-scope fence that
+  // orders its own stores, the sequence word: the host never sees the new
+  // sequence before the values.
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
+    *counter = 0u;
+    if (kPublish) {
       __threadfence_system();
       *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq;
     }
