@@ -231,10 +231,25 @@ class KDTree:
                                          "start", "end", "leaf_index")])
         return out
 
-    def query(self, queries, counts: bool = False):
+    def query(self, queries, counts: bool = False, workers: int = 1):
+        """Exact 1-NN of every query.  workers > 1 splits the queries into
+        contiguous chunks searched by that many host threads (each query's
+        search is the same; only the timing changes)."""
         q = _f32(queries)
         idx = np.empty(len(q), np.int32)
         d2 = np.empty(len(q), np.float32)
+        if workers > 1 and not counts and len(q) >= 2 * workers:
+            from concurrent.futures import ThreadPoolExecutor
+            bounds = np.linspace(0, len(q), workers + 1).astype(np.int64)
+
+            def run(k):
+                a, b = int(bounds[k]), int(bounds[k + 1])
+                # ctypes releases the GIL for the duration of the C call
+                _lib.orc_tree_nn(self._h, _ptr(q[a:b]), b - a, _ptr(idx[a:b]), _ptr(d2[a:b]), None, None)
+
+            with ThreadPoolExecutor(workers) as ex:
+                list(ex.map(run, range(workers)))
+            return idx, d2
         if counts:
             nodes = np.empty(len(q), np.int64)
             pts = np.empty(len(q), np.int64)
@@ -282,7 +297,7 @@ def accept_mask(idx, d2, max_corr_dist):
 
 # ----------------------------------------------------------------- ICP ----
 
-def icp_step(tree: KDTree, source, T, max_corr_dist):
+def icp_step(tree: KDTree, source, T, max_corr_dist, workers: int = 1):
     """One correspondence + reduction pass under transform T (double 4x4).
 
     Returns a dict: idx, d2 (per source point), accepted mask, n_accepted,
@@ -292,7 +307,7 @@ def icp_step(tree: KDTree, source, T, max_corr_dist):
         raise NonFiniteError("non-finite source point")
     R32, t32 = as_kernel_rt(T)
     p = transform(R32, t32, src)
-    idx, d2 = tree.query(p)
+    idx, d2 = tree.query(p, workers=workers)
     acc = accept_mask(idx, d2, max_corr_dist)
     n_acc = int(acc.sum())
     out = {"idx": idx, "d2": d2, "accepted": acc, "n_accepted": n_acc,
@@ -344,7 +359,7 @@ def residual_reject(step, source, tree: KDTree, T1, n_sigma: float):
 
 
 def icp_align(tree: KDTree, source, max_iter: int, eps: float, max_corr_dist,
-              init_T=None, residual_sigma: float = 0.0):
+              init_T=None, residual_sigma: float = 0.0, workers: int = 1):
     """Section 3.3 loop with the section 4.6 stopping rule; residual_sigma > 0
     adds the section 4.4 residual rejection and re-solve to every iteration.
 
@@ -355,7 +370,7 @@ def icp_align(tree: KDTree, source, max_iter: int, eps: float, max_corr_dist,
     mses = []
     iters = 0
     for k in range(max_iter):
-        st = icp_step(tree, source, T, max_corr_dist)
+        st = icp_step(tree, source, T, max_corr_dist, workers)
         if st["n_accepted"] < 3:
             raise DegenerateError("fewer than 3 accepted correspondences")
         T_next = solve_from_step(st, source, tree)
@@ -372,7 +387,7 @@ def icp_align(tree: KDTree, source, max_iter: int, eps: float, max_corr_dist,
         if (k >= 2 and abs(mses[-2] - mses[-1]) < eps
                 and abs(mses[-3] - mses[-2]) < eps):
             break
-    fin = icp_step(tree, source, T, max_corr_dist)
+    fin = icp_step(tree, source, T, max_corr_dist, workers)
     return {"T": T, "iters": iters, "final_mse": fin["mse"], "final_n_accepted": fin["n_accepted"],
             "trace": trace}
 

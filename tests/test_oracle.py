@@ -498,3 +498,14 @@ def test_section6_regression_curve(oracle_mod):
         assert rot[k + 1] <= rot[k] * 1.05 + 1e-6
         assert tra[k + 1] <= tra[k] * 1.05 + 1e-6
     assert rot[-1] < 1e-4 and tra[-1] < 1e-3
+
+
+def test_threaded_query_equals_serial(oracle_mod):
+    """Splitting the queries over host threads changes nothing in the result."""
+    ref = W.uniform_cloud(20000, 91)
+    q = W.uniform_cloud(7001, 92, -1.1, 1.1)
+    tree = oracle_mod.KDTree(ref, 12)
+    i1, d1 = tree.query(q)
+    i4, d4 = tree.query(q, workers=4)
+    np.testing.assert_array_equal(i1, i4)
+    np.testing.assert_array_equal(d1.view(np.uint32), d4.view(np.uint32))
