@@ -83,6 +83,7 @@ def load(build_if_missing: bool = False):
                              ctypes.c_double)
     sig = {
         "icpnn_kdtree_build": ([P, i64, i32, i32, u32, ctypes.POINTER(P)], ctypes.c_int),
+        "icpnn_kdtree_build_device": ([P, i64, i32, i32, u32, ctypes.POINTER(P), P], ctypes.c_int),
         "icpnn_kdtree_upload": ([P, P], ctypes.c_int),
         "icpnn_kdtree_free": ([P], None),
         "icpnn_kdtree_info": ([P, P, P, P, P, P], ctypes.c_int),
@@ -194,6 +195,21 @@ def kdtree_build(points, leaf_size: int, max_depth: int = -1, round_robin: bool 
     h = ctypes.c_void_p()
     _check(lib.icpnn_kdtree_build(_ptr(pts, np.float32, 3, "points"), len(pts), int(leaf_size),
                                   int(max_depth), SPLIT_ROUND_ROBIN if round_robin else 0, ctypes.byref(h)))
+    return KDTree(h)
+
+
+def kdtree_build_device(points, leaf_size: int, max_depth: int = -1, round_robin: bool = False,
+                        stream=None) -> KDTree:
+    """Device build of the same tree (points: a CUDA tensor, or host array);
+    the tree is left on the device, already uploaded."""
+    if not _is_torch(points):
+        points = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
+    lib = load()
+    h = ctypes.c_void_p()
+    _check(lib.icpnn_kdtree_build_device(_ptr(points, np.float32, 3, "points"), int(points.shape[0]),
+                                         int(leaf_size), int(max_depth),
+                                         SPLIT_ROUND_ROBIN if round_robin else 0, ctypes.byref(h),
+                                         _stream(stream)))
     return KDTree(h)
 
 

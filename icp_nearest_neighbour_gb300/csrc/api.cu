@@ -367,6 +367,33 @@ void transform_to_f32(const double T[16], float R[9], float t[3]) {
   }
 }
 
+// Host copies of a device-built tree's nodes, boxes and records, made on first
+// need.
+int ensure_host_copy(icpnn_tree* t) {
+  if (!t->host_stale) return ICPNN_OK;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  cudaError_t e = cudaSetDevice(t->dev.device);
+  try {
+    t->nodes.resize(static_cast<size_t>(t->heap_slots));
+    t->boxes.resize(static_cast<size_t>(8 * t->heap_slots));
+    t->records.resize(static_cast<size_t>(4 * t->n));
+  } catch (const std::bad_alloc&) {
+    cudaSetDevice(cur);
+    return fail(ICPNN_ERR_NO_MEMORY, "tree: host allocation failed");
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpy(t->nodes.data(), t->dev.nodes, t->nodes.size() * sizeof(Node), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(t->boxes.data(), t->dev.boxes, t->boxes.size() * sizeof(float), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(t->records.data(), t->dev.points, t->records.size() * sizeof(float), cudaMemcpyDeviceToHost);
+  cudaSetDevice(cur);
+  if (e != cudaSuccess) return fail(ICPNN_ERR_CUDA, std::string("tree: copy to the host: ") + cudaGetErrorString(e));
+  t->host_stale = false;
+  return ICPNN_OK;
+}
+
 }  // namespace
 }  // namespace icpnn
 
@@ -398,6 +425,45 @@ int icpnn_kdtree_build(const float* xyz_host, int64_t n, int32_t leaf_size, int3
   return ICPNN_OK;
 }
 
+int icpnn_kdtree_build_device(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth,
+                              uint32_t flags, icpnn_tree** out, void* stream) {
+  clear_error();
+  if (out == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build_device: out is NULL");
+  *out = nullptr;
+  if (xyz == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build_device: xyz is NULL");
+  if (n < 1 || n > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build_device: n must be in [1, 2^31-1]");
+  if (leaf_size < 1 || leaf_size > ICPNN_MAX_LEAF_SIZE)
+    return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build_device: leaf_size must be in [1, 64]");
+  if (max_depth == -1) max_depth = ICPNN_MAX_DEPTH;
+  if (max_depth < 0 || max_depth > ICPNN_MAX_DEPTH)
+    return fail(ICPNN_ERR_TREE_DEPTH, "kdtree_build_device: max_depth must be in [0, 20] or -1");
+  if (flags & ~ICPNN_SPLIT_ROUND_ROBIN) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build_device: unknown flag");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  icpnn_tree* t = new (std::nothrow) icpnn_tree();
+  if (t == nullptr) return fail(ICPNN_ERR_NO_MEMORY, "kdtree_build_device: host allocation failed");
+  int rc = ICPNN_OK;
+  {
+    Scratch sc(s);
+    const float* d_xyz = xyz;
+    if (!is_device_pointer(xyz)) {
+      float* tmp = nullptr;
+      cudaError_t e = sc.alloc(&tmp, 3 * n);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(tmp, xyz, static_cast<size_t>(n) * 3 * sizeof(float), cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) rc = fail(ICPNN_ERR_CUDA, std::string("kdtree_build_device: ") + cudaGetErrorString(e));
+      d_xyz = tmp;
+    }
+    if (rc == ICPNN_OK)
+      rc = build_tree_device(d_xyz, n, leaf_size, max_depth, (flags & ICPNN_SPLIT_ROUND_ROBIN) != 0, t, s);
+  }
+  if (rc != ICPNN_OK) {
+    delete t;
+    return rc;
+  }
+  *out = t;
+  return ICPNN_OK;
+}
+
 void icpnn_kdtree_free(icpnn_tree* t) {
   if (t == nullptr) return;
   if (t->dev.nodes != nullptr) {
@@ -418,6 +484,7 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   int cur = -1;
   ICPNN_CUDA(cudaGetDevice(&cur));
   if (t->dev.nodes != nullptr && t->dev.device == cur) return ICPNN_OK;
+  if (int rc = ensure_host_copy(t)) return rc;
   if (t->dev.nodes != nullptr) {
     cudaSetDevice(t->dev.device);
     cudaFree(t->dev.nodes);
@@ -472,6 +539,7 @@ int icpnn_kdtree_export(const icpnn_tree* t, int64_t node_capacity, float* split
   if (t == nullptr || !split_val || !split_dim || !left || !right || !start || !end || !leaf_index)
     return fail(ICPNN_ERR_INVALID_ARG, "kdtree_export: NULL argument");
   if (node_capacity < t->n_nodes) return fail(ICPNN_ERR_INVALID_ARG, "kdtree_export: node_capacity too small");
+  if (int rc = ensure_host_copy(const_cast<icpnn_tree*>(t))) return rc;
   // Walk the heap depth-first, left first: that numbering is the page's
   // recursion order.  Returns [start, end) of the subtree's points.
   struct Frame {

@@ -1,6 +1,8 @@
 // Internal declarations shared by the host and device parts of libicpnn.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 #include <functional>
 #include <string>
@@ -71,6 +73,9 @@ struct icpnn_tree {
   // lo.x, lo.y, lo.z, 0, hi.x, hi.y, hi.z, 0 (unused slots zero).
   std::vector<float> boxes;
   icpnn::DeviceTree dev;
+  // Built on the device: nodes, boxes and records exist there only until a
+  // caller needs them on the host (export, upload to another device).
+  bool host_stale = false;
 };
 
 namespace icpnn {
@@ -82,6 +87,12 @@ void clear_error();
 // Host tree build (kdtree_build.cpp).
 int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t);
+int32_t tree_depth(int64_t n, int32_t leaf_size, int32_t max_depth);
+
+// Device tree build (kdtree_build_gpu.cu): the same tree from device points,
+// left in t->dev; the host arrays are filled on demand (host_stale).
+int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
+                      icpnn_tree* t, cudaStream_t s);
 
 // Process-wide host worker pool (host_pool.cpp).  pool_submit queues a job
 // (ensuring at least min_threads workers); parallel_for runs fn(0..tasks-1)

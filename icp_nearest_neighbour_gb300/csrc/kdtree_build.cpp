@@ -335,6 +335,8 @@ struct Builder {
   }
 };
 
+}  // namespace
+
 // Deepest level that holds a node.  With median splits the nodes at depth k
 // hold floor or ceil of n / 2^k points, so the tree stops at the first k whose
 // largest node fits in a leaf, or at the cap.
@@ -347,8 +349,6 @@ int32_t tree_depth(int64_t n, int32_t leaf_size, int32_t max_depth) {
   }
   return d;
 }
-
-}  // namespace
 
 int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t) {

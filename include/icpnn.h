@@ -101,6 +101,24 @@ typedef struct icpnn_tree icpnn_tree; /* opaque; owned by the library */
 int icpnn_kdtree_build(const float* xyz_host, int64_t n, int32_t leaf_size, int32_t max_depth,
                        uint32_t flags, icpnn_tree** out);
 
+/* icpnn_kdtree_build_device -- the same tree as icpnn_kdtree_build, node for
+ * node (split axes, split values, leaf ranges and the set of points in each
+ * leaf; only the order of points inside a leaf may differ), built on the
+ * current CUDA device and left there, already uploaded.  The pages build the
+ * tree on the host (section 5.1); this is for pipelines in which the host
+ * build would be the longest step.
+ *   xyz        n x 3 float32 target points, device or host memory (a host
+ *              array is copied to the device first); the caller keeps
+ *              ownership.
+ *   n, leaf_size, max_depth, flags, out: as for icpnn_kdtree_build.
+ *   stream     cudaStream_t (NULL = legacy default stream); synchronised
+ *              before return.
+ * The host copies of the nodes and records are made on first need
+ * (icpnn_kdtree_export, icpnn_kdtree_upload to another device).
+ * Errors: as icpnn_kdtree_build, plus CUDA. */
+int icpnn_kdtree_build_device(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth,
+                              uint32_t flags, icpnn_tree** out, void* stream);
+
 /* icpnn_kdtree_upload -- copy the tree (node array and leaf-ordered point
  * records) to the current device, enqueued on `stream`, which is then
  * synchronised.  Done once per target (page sections 2.3, 5.5).  A second call
