@@ -163,63 +163,39 @@ __device__ __forceinline__ bool block_chunk(const LevelArgs& a, uint32_t* k, int
 }
 
 // ------------------------------------------------ levels of large nodes --
+//
+// Each pass over a level runs one block per (node, chunk); the last block of
+// a node to finish (a per-node counter, reset by that block) combines the
+// node's chunk partials in chunk order.
 
-// Pass 1 over each chunk of list 0: coordinate sums and box.  part[block] =
-// {sx, sy, sz, -minx, -miny, -minz, maxx, maxy, maxz}.
-__global__ void __launch_bounds__(kBT) level_sums_kernel(LevelArgs a, const float4* __restrict__ L0,
-                                                         double* __restrict__ part) {
-  __shared__ double shd[kBWarps];
-  __shared__ float shf[kBWarps];
-  uint32_t k;
-  int64_t lo, cnt, b0, b1;
-  int j;
-  if (!block_chunk(a, &k, &lo, &cnt, &b0, &b1, &j)) return;
-  double s[3] = {0.0, 0.0, 0.0};
-  float mn[3] = {INFINITY, INFINITY, INFINITY}, mx[3] = {-INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 4
-  for (int64_t i = b0 + threadIdx.x; i < b1; i += kBT) {
-    const float4 p = L0[i];
-    const float c[3] = {p.x, p.y, p.z};
-#pragma unroll
-    for (int e = 0; e < 3; ++e) {
-      s[e] += static_cast<double>(c[e]);
-      mn[e] = fminf(mn[e], c[e]);
-      mx[e] = fmaxf(mx[e], c[e]);
-    }
-  }
-  double r[9];
-#pragma unroll
-  for (int e = 0; e < 3; ++e) {
-    r[e] = block_sum(s[e], shd);
-    r[3 + e] = static_cast<double>(-block_min(mn[e], shf));
-    r[6 + e] = static_cast<double>(-block_min(-mx[e], shf));
-  }
+// True in every thread of the block that finishes the node's pass last.
+__device__ __forceinline__ bool last_of_node(unsigned int* counter, int chunks, bool* s_last) {
+  __threadfence();
+  __syncthreads();
   if (threadIdx.x == 0) {
-#pragma unroll
-    for (int e = 0; e < 9; ++e) part[static_cast<int64_t>(blockIdx.x) * 9 + e] = r[e];
+    *s_last = atomicAdd(counter, 1u) == static_cast<unsigned int>(chunks - 1);
+    if (*s_last) *counter = 0u;
   }
+  __syncthreads();
+  if (*s_last) __threadfence();
+  return *s_last;
 }
 
 // Per node, one warp: the chunk partials added in a fixed order (lanes over
-// chunks, then a butterfly); the mean and the box.
-__global__ void __launch_bounds__(256) level_mean_kernel(LevelArgs a, const double* __restrict__ part,
-                                                         double* __restrict__ mean, Node* __restrict__ nodes,
-                                                         float4* __restrict__ boxes) {
-  const int64_t slot = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+// chunks, then a butterfly); the mean and the box, and for a leaf its node
+// record.
+__device__ __forceinline__ void node_mean(const LevelArgs& a, uint32_t k, int64_t slot, int64_t lo, int64_t cnt,
+                                          int chunks, const double* __restrict__ part, double* __restrict__ mean,
+                                          Node* __restrict__ nodes, float4* __restrict__ boxes) {
   const int lane = threadIdx.x & 31;
-  if (slot >= (int64_t{1} << a.d)) return;
-  const uint32_t k = (1u << a.d) + static_cast<uint32_t>(slot);
-  int64_t lo, cnt;
-  if (!node_range(k, a.d, a.n, a.leaf, a.max_depth, &lo, &cnt)) return;
-  const int chunks = static_cast<int>((cnt + kChunk - 1) / kChunk);
   double s[3] = {0.0, 0.0, 0.0}, nmn[3] = {-INFINITY, -INFINITY, -INFINITY}, mx[3] = {-INFINITY, -INFINITY, -INFINITY};
   for (int j = lane; j < chunks; j += 32) {
     const double* p = part + (slot * a.blocks_per_node + j) * 9;
 #pragma unroll
     for (int e = 0; e < 3; ++e) {
-      s[e] += p[e];
-      nmn[e] = fmax(nmn[e], p[3 + e]);
-      mx[e] = fmax(mx[e], p[6 + e]);
+      s[e] += __ldcg(&p[e]);
+      nmn[e] = fmax(nmn[e], __ldcg(&p[3 + e]));
+      mx[e] = fmax(mx[e], __ldcg(&p[6 + e]));
     }
   }
 #pragma unroll
@@ -244,15 +220,93 @@ __global__ void __launch_bounds__(256) level_mean_kernel(LevelArgs a, const doub
   }
 }
 
-// Pass 2: sums of squared deviations about the node's mean (inner nodes).
-__global__ void __launch_bounds__(kBT) level_sq_kernel(LevelArgs a, const float4* __restrict__ L0,
-                                                       const double* __restrict__ mean,
-                                                       double* __restrict__ part) {
+
+// Pass 1 over each chunk of list 0: coordinate sums and box.  part[block] =
+// {sx, sy, sz, -minx, -miny, -minz, maxx, maxy, maxz}.
+__global__ void __launch_bounds__(kBT) level_sums_kernel(LevelArgs a, const float4* __restrict__ L0,
+                                                         double* __restrict__ part, unsigned int* __restrict__ counter,
+                                                         double* __restrict__ mean, Node* __restrict__ nodes,
+                                                         float4* __restrict__ boxes) {
   __shared__ double shd[kBWarps];
+  __shared__ float shf[kBWarps];
+  __shared__ bool s_last;
   uint32_t k;
   int64_t lo, cnt, b0, b1;
   int j;
-  if (!block_chunk(a, &k, &lo, &cnt, &b0, &b1, &j) || is_leaf_node(cnt, a.d, a)) return;
+  if (!block_chunk(a, &k, &lo, &cnt, &b0, &b1, &j) || b0 >= b1) return;
+  double s[3] = {0.0, 0.0, 0.0};
+  float mn[3] = {INFINITY, INFINITY, INFINITY}, mx[3] = {-INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 4
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += kBT) {
+    const float4 p = L0[i];
+    const float c[3] = {p.x, p.y, p.z};
+#pragma unroll
+    for (int e = 0; e < 3; ++e) {
+      s[e] += static_cast<double>(c[e]);
+      mn[e] = fminf(mn[e], c[e]);
+      mx[e] = fmaxf(mx[e], c[e]);
+    }
+  }
+  double r[9];
+#pragma unroll
+  for (int e = 0; e < 3; ++e) {
+    r[e] = block_sum(s[e], shd);
+    r[3 + e] = static_cast<double>(-block_min(mn[e], shf));
+    r[6 + e] = static_cast<double>(-block_min(-mx[e], shf));
+  }
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int e = 0; e < 9; ++e) part[static_cast<int64_t>(blockIdx.x) * 9 + e] = r[e];
+  }
+  const int64_t slot = k - (1u << a.d);
+  const int chunks = static_cast<int>((cnt + kChunk - 1) / kChunk);
+  if (!last_of_node(&counter[slot], chunks, &s_last) || threadIdx.x >= 32) return;
+  node_mean(a, k, slot, lo, cnt, chunks, part, mean, nodes, boxes);
+}
+
+// Axis by the largest variance, ties within a relative 1e-9 to the lowest.
+__device__ __forceinline__ int widest(double v0, double v1, double v2) {
+  const double vmax = fmax(v0, fmax(v1, v2));
+  const double lim = vmax * (1.0 - 1e-9);
+  return v0 >= lim ? 0 : (v1 >= lim ? 1 : 2);
+}
+
+// Per inner node, one warp: the variance, the split axis, the median (the
+// record at position lo + count/2 of the axis's list) and the node record.
+__device__ __forceinline__ void node_split(const LevelArgs& a, uint32_t k, int64_t slot, int64_t lo, int64_t cnt,
+                                           int chunks, const double* __restrict__ part,
+                                           const float4* __restrict__ L0, const float4* __restrict__ L1,
+                                           const float4* __restrict__ L2, Node* __restrict__ nodes) {
+  const int lane = threadIdx.x & 31;
+  double q[3] = {0.0, 0.0, 0.0};
+  for (int j = lane; j < chunks; j += 32) {
+    const double* p = part + (slot * a.blocks_per_node + j) * 9;
+#pragma unroll
+    for (int e = 0; e < 3; ++e) q[e] += __ldcg(&p[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 3; ++e) q[e] = warp_sum(q[e]);
+  if (lane != 0) return;
+  const double c = static_cast<double>(cnt);
+  const int axis = a.round_robin ? a.d % 3 : widest(q[0] / c, q[1] / c, q[2] / c);
+  const float4* L = axis == 0 ? L0 : (axis == 1 ? L1 : L2);
+  nodes[k].a = __float_as_uint(coord(L[lo + cnt / 2], axis));
+  nodes[k].meta = static_cast<uint32_t>(axis);
+}
+
+// Pass 2: sums of squared deviations about the node's mean (inner nodes).
+__global__ void __launch_bounds__(kBT) level_sq_kernel(LevelArgs a, const float4* __restrict__ L0,
+                                                       const float4* __restrict__ L1,
+                                                       const float4* __restrict__ L2,
+                                                       const double* __restrict__ mean,
+                                                       double* __restrict__ part, unsigned int* __restrict__ counter,
+                                                       Node* __restrict__ nodes) {
+  __shared__ double shd[kBWarps];
+  __shared__ bool s_last;
+  uint32_t k;
+  int64_t lo, cnt, b0, b1;
+  int j;
+  if (!block_chunk(a, &k, &lo, &cnt, &b0, &b1, &j) || b0 >= b1 || is_leaf_node(cnt, a.d, a)) return;
   const int64_t slot = k - (1u << a.d);
   const double m0 = mean[slot * 3], m1 = mean[slot * 3 + 1], m2 = mean[slot * 3 + 2];
   double q0 = 0.0, q1 = 0.0, q2 = 0.0;
@@ -274,44 +328,11 @@ __global__ void __launch_bounds__(kBT) level_sq_kernel(LevelArgs a, const float4
     part[static_cast<int64_t>(blockIdx.x) * 9 + 1] = r1;
     part[static_cast<int64_t>(blockIdx.x) * 9 + 2] = r2;
   }
-}
-
-// Axis by the largest variance, ties within a relative 1e-9 to the lowest.
-__device__ __forceinline__ int widest(double v0, double v1, double v2) {
-  const double vmax = fmax(v0, fmax(v1, v2));
-  const double lim = vmax * (1.0 - 1e-9);
-  return v0 >= lim ? 0 : (v1 >= lim ? 1 : 2);
-}
-
-// Per inner node, one warp: the variance, the split axis, the median (the
-// record at position lo + count/2 of the axis's list) and the node record.
-__global__ void __launch_bounds__(256) level_split_kernel(LevelArgs a, const double* __restrict__ part,
-                                                          const float4* __restrict__ L0,
-                                                          const float4* __restrict__ L1,
-                                                          const float4* __restrict__ L2,
-                                                          Node* __restrict__ nodes) {
-  const int64_t slot = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (slot >= (int64_t{1} << a.d)) return;
-  const uint32_t k = (1u << a.d) + static_cast<uint32_t>(slot);
-  int64_t lo, cnt;
-  if (!node_range(k, a.d, a.n, a.leaf, a.max_depth, &lo, &cnt) || is_leaf_node(cnt, a.d, a)) return;
   const int chunks = static_cast<int>((cnt + kChunk - 1) / kChunk);
-  double q[3] = {0.0, 0.0, 0.0};
-  for (int j = lane; j < chunks; j += 32) {
-    const double* p = part + (slot * a.blocks_per_node + j) * 9;
-#pragma unroll
-    for (int e = 0; e < 3; ++e) q[e] += p[e];
-  }
-#pragma unroll
-  for (int e = 0; e < 3; ++e) q[e] = warp_sum(q[e]);
-  if (lane != 0) return;
-  const double c = static_cast<double>(cnt);
-  const int axis = a.round_robin ? a.d % 3 : widest(q[0] / c, q[1] / c, q[2] / c);
-  const float4* L = axis == 0 ? L0 : (axis == 1 ? L1 : L2);
-  nodes[k].a = __float_as_uint(coord(L[lo + cnt / 2], axis));
-  nodes[k].meta = static_cast<uint32_t>(axis);
+  if (!last_of_node(&counter[slot], chunks, &s_last) || threadIdx.x >= 32) return;
+  node_split(a, k, slot, lo, cnt, chunks, part, L0, L1, L2, nodes);
 }
+
 
 // Inner nodes: each point's side from its position in the chosen axis's list
 // (1 = left).  Leaves: their records, in the order of list 0.
@@ -341,12 +362,14 @@ __global__ void __launch_bounds__(kBT) level_count_kernel(LevelArgs a, const flo
                                                           const float4* __restrict__ L1,
                                                           const float4* __restrict__ L2,
                                                           const uint8_t* __restrict__ left,
-                                                          uint32_t* __restrict__ cntl) {
+                                                          uint32_t* __restrict__ cntl,
+                                                          unsigned int* __restrict__ counter) {
   __shared__ uint32_t sh[3][kBWarps];
+  __shared__ bool s_last;
   uint32_t k;
   int64_t lo, cnt, b0, b1;
   int j;
-  if (!block_chunk(a, &k, &lo, &cnt, &b0, &b1, &j) || is_leaf_node(cnt, a.d, a)) return;
+  if (!block_chunk(a, &k, &lo, &cnt, &b0, &b1, &j) || b0 >= b1 || is_leaf_node(cnt, a.d, a)) return;
   uint32_t c0 = 0, c1 = 0, c2 = 0;
 #pragma unroll 4
   for (int64_t i = b0 + threadIdx.x; i < b1; i += kBT) {
@@ -368,24 +391,16 @@ __global__ void __launch_bounds__(kBT) level_count_kernel(LevelArgs a, const flo
     for (int w = 0; w < kBWarps; ++w) t += sh[threadIdx.x][w];
     cntl[static_cast<int64_t>(blockIdx.x) * 3 + threadIdx.x] = t;
   }
-}
-
-// Per inner node and list: exclusive prefix of the chunks' left counts, in
-// chunk order (in place); one thread per node and list.
-__global__ void __launch_bounds__(256) level_scan_kernel(LevelArgs a, uint32_t* __restrict__ cntl) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t slot = t / 3;
-  const int l = static_cast<int>(t % 3);
-  if (slot >= (int64_t{1} << a.d)) return;
-  const uint32_t k = (1u << a.d) + static_cast<uint32_t>(slot);
-  int64_t lo, cnt;
-  if (!node_range(k, a.d, a.n, a.leaf, a.max_depth, &lo, &cnt) || is_leaf_node(cnt, a.d, a)) return;
+  // the node's last block: exclusive prefix of the chunks' counts, in chunk
+  // order, per list (in place)
+  const int64_t slot = k - (1u << a.d);
   const int chunks = static_cast<int>((cnt + kChunk - 1) / kChunk);
+  if (!last_of_node(&counter[slot], chunks, &s_last) || threadIdx.x >= 3) return;
   uint32_t run = 0;
-  for (int j = 0; j < chunks; ++j) {
-    uint32_t* c = cntl + (slot * a.blocks_per_node + j) * 3 + l;
-    const uint32_t v = *c;
-    *c = run;
+  for (int c = 0; c < chunks; ++c) {
+    uint32_t* p = cntl + (slot * a.blocks_per_node + c) * 3 + threadIdx.x;
+    const uint32_t v = __ldcg(p);
+    *p = run;
     run += v;
   }
 }
@@ -533,24 +548,29 @@ __global__ void __launch_bounds__(256) level_warp_kernel(LevelArgs a, const floa
   }
   for (int64_t i = lo + lane; i < hi; i += 32) left[rec_id(L[i])] = i < mid ? 1 : 0;
   __syncwarp();
+  // the three lists in the same rounds: their loads are in flight together
   const float4* Ls[3] = {L0, L1, L2};
   float4* Ts[3] = {T0, T1, T2};
+  int64_t nl[3] = {0, 0, 0}, nr[3] = {0, 0, 0};
+  for (int64_t base = lo; base < hi; base += 32) {
+    const int64_t i = base + lane;
+    const bool valid = i < hi;
+    const int64_t round_n = min(static_cast<int64_t>(32), hi - base);
+    float4 r[3];
 #pragma unroll
-  for (int l = 0; l < 3; ++l) {
-    int64_t nl = 0, nr = 0;
-    for (int64_t base = lo; base < hi; base += 32) {
-      const int64_t i = base + lane;
-      const bool valid = i < hi;
-      const float4 r = valid ? Ls[l][i] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const uint32_t f = valid ? left[rec_id(r)] : 0u;
-      const uint32_t bal = __ballot_sync(kFull, f != 0u);
+    for (int l = 0; l < 3; ++l) r[l] = valid ? Ls[l][i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t f[3];
+#pragma unroll
+    for (int l = 0; l < 3; ++l) f[l] = valid ? left[rec_id(r[l])] : 0u;
+#pragma unroll
+    for (int l = 0; l < 3; ++l) {
+      const uint32_t bal = __ballot_sync(kFull, f[l] != 0u);
       if (valid) {
         const int64_t rl = __popc(bal & ((1u << lane) - 1u));
-        Ts[l][f ? lo + nl + rl : mid + nr + (i - base - rl)] = r;
+        Ts[l][f[l] ? lo + nl[l] + rl : mid + nr[l] + (i - base - rl)] = r[l];
       }
-      const int64_t round_n = min(static_cast<int64_t>(32), hi - base);
-      nl += __popc(bal);
-      nr += round_n - __popc(bal);
+      nl[l] += __popc(bal);
+      nr[l] += round_n - __popc(bal);
     }
   }
 }
@@ -625,9 +645,9 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
     if (e == cudaSuccess) e = m.alloc(&P, n);
     if (e == cudaSuccess) e = m.alloc(&keys, 3 * n);
     if (e == cudaSuccess) e = m.alloc(&ids, 3 * n);
-    if (e == cudaSuccess) e = m.alloc(&alt_k, n);
-    if (e == cudaSuccess) e = m.alloc(&alt_v, n);
-    if (e == cudaSuccess) e = m.alloc(&temp, radix_temp_words(n));
+    if (e == cudaSuccess) e = m.alloc(&alt_k, 3 * n);
+    if (e == cudaSuccess) e = m.alloc(&alt_v, 3 * n);
+    if (e == cudaSuccess) e = m.alloc(&temp, 3 * radix_temp_words(n));
     if (e == cudaSuccess) e = m.alloc(&lists[0][0], 3 * n);
     if (e == cudaSuccess) e = m.alloc(&lists[1][0], 3 * n);
     if (e == cudaSuccess) e = m.alloc(&left, n);
@@ -635,6 +655,9 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
     if (e == cudaSuccess) e = m.alloc(&mean, (int64_t{1} << depth) * 3);
     if (e == cudaSuccess) e = m.alloc(&cntl, max_blocks * 3);
     if (e == cudaSuccess) e = m.alloc(&first_bad, 1);
+    unsigned int* node_count = nullptr;  // per node of a level, zero between passes
+    if (e == cudaSuccess) e = m.alloc(&node_count, int64_t{1} << depth);
+    if (e == cudaSuccess) e = cudaMemsetAsync(node_count, 0, sizeof(unsigned int) << depth, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(nodes, 0, nb + bb, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(first_bad, 0xff, sizeof(unsigned long long), s);
     const int big_grid = static_cast<int>(std::min<int64_t>(grid_for(3 * n), 8 * 1024));
@@ -644,15 +667,10 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
     }
     // one stable sort per axis by (coordinate, index): equal keys keep the
     // index order they start in
-    for (int l = 0; l < 3 && e == cudaSuccess; ++l) {
-      uint32_t* sorted = nullptr;
-      e = radix_sort(keys + l * n, ids + l * n, alt_k, alt_v, temp, n, 0, 32, s, &sorted);
-      if (e == cudaSuccess && sorted != ids + l * n)
-        e = cudaMemcpyAsync(ids + l * n, sorted, static_cast<size_t>(n) * sizeof(uint32_t),
-                            cudaMemcpyDeviceToDevice, s);
-    }
+    uint32_t* sorted = ids;
+    if (e == cudaSuccess) e = radix_sort(keys, ids, alt_k, alt_v, temp, n, 0, 32, s, &sorted, 3);
     if (e == cudaSuccess) {
-      gather_lists_kernel<<<big_grid, 256, 0, s>>>(P, n, ids, lists[0][0]);
+      gather_lists_kernel<<<big_grid, 256, 0, s>>>(P, n, sorted, lists[0][0]);
       e = cudaGetLastError();
     }
     for (int b = 0; b < 2; ++b) {
@@ -670,7 +688,7 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
       const int64_t largest = (n + (int64_t{1} << d) - 1) >> d;
       a.blocks_per_node = static_cast<int>(std::max<int64_t>(1, (largest + kChunk - 1) / kChunk));
       const int blocks = static_cast<int>((int64_t{1} << d) * a.blocks_per_node);
-      const int warp_grid = grid_for((int64_t{1} << d) * 32);
+      const int warp_grid = grid_for((int64_t{1} << d) * 32);  // one warp per node
       float4** L = lists[cur];
       float4** T = lists[cur ^ 1];
       float4* records = reinterpret_cast<float4*>(pts);
@@ -680,19 +698,14 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
                                                     records);
         g_launch_count.fetch_add(1, std::memory_order_relaxed);
       } else {
-        level_sums_kernel<<<blocks, kBT, 0, s>>>(a, L[0], part);
-        level_mean_kernel<<<warp_grid, 256, 0, s>>>(a, part, mean, nodes, boxes);
-        if (inner_level) {
-          level_sq_kernel<<<blocks, kBT, 0, s>>>(a, L[0], mean, part);
-          level_split_kernel<<<warp_grid, 256, 0, s>>>(a, part, L[0], L[1], L[2], nodes);
-        }
+        level_sums_kernel<<<blocks, kBT, 0, s>>>(a, L[0], part, node_count, mean, nodes, boxes);
+        if (inner_level) level_sq_kernel<<<blocks, kBT, 0, s>>>(a, L[0], L[1], L[2], mean, part, node_count, nodes);
         level_flag_kernel<<<blocks, kBT, 0, s>>>(a, L[0], L[1], L[2], nodes, left, records);
         if (inner_level) {
-          level_count_kernel<<<blocks, kBT, 0, s>>>(a, L[0], L[1], L[2], left, cntl);
-          level_scan_kernel<<<grid_for((int64_t{1} << d) * 3), 256, 0, s>>>(a, cntl);
+          level_count_kernel<<<blocks, kBT, 0, s>>>(a, L[0], L[1], L[2], left, cntl, node_count);
           level_scatter_kernel<<<blocks, kBT, 0, s>>>(a, L[0], L[1], L[2], T[0], T[1], T[2], left, cntl);
         }
-        g_launch_count.fetch_add(inner_level ? 8 : 3, std::memory_order_relaxed);
+        g_launch_count.fetch_add(inner_level ? 5 : 2, std::memory_order_relaxed);
       }
       if (inner_level) cur ^= 1;
       e = cudaGetLastError();

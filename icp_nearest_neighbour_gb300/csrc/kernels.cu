@@ -169,10 +169,18 @@ constexpr int kRadix = 1 << kRadixBits;
 constexpr int kSortItems = 8;
 constexpr int kSortTile = kThreads * kSortItems;
 
+// Segments: blockIdx.y sorts its own array of n keys (offset blockIdx.y * n)
+// with its own histogram region (offset blockIdx.y * (tiles + 1) * kRadix).
+__device__ __forceinline__ int64_t seg_temp(int tiles) {
+  return static_cast<int64_t>(blockIdx.y) * (static_cast<int64_t>(tiles) + 1) * kRadix;
+}
+
 __global__ void __launch_bounds__(kThreads) radix_hist_kernel(const uint32_t* __restrict__ keys, int64_t n,
                                                               int shift, uint32_t* __restrict__ hist,
                                                               int tiles) {
   __shared__ uint32_t cnt[kRadix];
+  keys += static_cast<int64_t>(blockIdx.y) * n;
+  hist += seg_temp(tiles);
   for (int i = threadIdx.x; i < kRadix; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kSortTile;
@@ -217,6 +225,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 __global__ void __launch_bounds__(kThreads) digit_row_scan_kernel(uint32_t* __restrict__ hist, int tiles,
                                                                   uint32_t* __restrict__ digit_total) {
   __shared__ uint32_t warp_sums[kThreads / 32];
+  hist += seg_temp(tiles);
+  digit_total += seg_temp(tiles);
   uint32_t* row = hist + static_cast<int64_t>(blockIdx.x) * tiles;
   uint32_t carry = 0;
   for (int base = 0; base < tiles; base += kThreads) {
@@ -240,6 +250,15 @@ __global__ void __launch_bounds__(kThreads) radix_scatter_kernel(
   __shared__ uint32_t wcount[kWarps][kRadix];
   __shared__ uint32_t warp_sums[kWarps];
   const int t = threadIdx.x, warp = t >> 5;
+  {
+    const int64_t e = static_cast<int64_t>(blockIdx.y) * n;
+    keys_in += e;
+    vals_in += e;
+    keys_out += e;
+    vals_out += e;
+    row_prefix += seg_temp(tiles);
+    digit_total += seg_temp(tiles);
+  }
   const uint32_t digit_offset = block_exclusive_scan(digit_total[t], warp_sums, nullptr);
   base[t] = digit_offset + row_prefix[static_cast<int64_t>(t) * tiles + blockIdx.x];
   const int64_t tile0 = static_cast<int64_t>(blockIdx.x) * kSortTile;
@@ -961,7 +980,7 @@ int64_t radix_temp_words(int64_t n) {
 
 cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
                        uint32_t* temp, int64_t n, int lo_bit, int hi_bit, cudaStream_t s,
-                       uint32_t** sorted_vals) {
+                       uint32_t** sorted_vals, int segments) {
   *sorted_vals = vals;
   if (n <= 1) return cudaSuccess;
   const int tiles = static_cast<int>((n + kSortTile - 1) / kSortTile);
@@ -969,9 +988,10 @@ cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint3
   uint32_t* digit_total = temp + static_cast<int64_t>(tiles) * kRadix;
   uint32_t *ki = keys, *vi = vals, *ko = keys_alt, *vo = vals_alt;
   for (int shift = lo_bit; shift < hi_bit; shift += kRadixBits) {
-    radix_hist_kernel<<<tiles, kThreads, 0, s>>>(ki, n, shift, hist, tiles);
-    digit_row_scan_kernel<<<kRadix, kThreads, 0, s>>>(hist, tiles, digit_total);
-    radix_scatter_kernel<<<tiles, kThreads, 0, s>>>(ki, vi, ko, vo, n, shift, hist, digit_total, tiles);
+    radix_hist_kernel<<<dim3(tiles, segments), kThreads, 0, s>>>(ki, n, shift, hist, tiles);
+    digit_row_scan_kernel<<<dim3(kRadix, segments), kThreads, 0, s>>>(hist, tiles, digit_total);
+    radix_scatter_kernel<<<dim3(tiles, segments), kThreads, 0, s>>>(ki, vi, ko, vo, n, shift, hist, digit_total,
+                                                                     tiles);
     g_launch_count.fetch_add(3, std::memory_order_relaxed);
     std::swap(ki, ko);
     std::swap(vi, vo);

@@ -39,12 +39,14 @@ cudaError_t launch_morton(const float* xyz, int64_t n, const int32_t* bbox6, uin
 
 // Stable LSD radix sort of (key, value) pairs on key bits [lo_bit, hi_bit)
 // (8 bits per pass).  Buffers: keys/vals (input), keys_alt/vals_alt (same
-// size), temp of radix_temp_words(n) words.  *sorted_vals receives whichever
-// value buffer holds the result.
+// size), temp of segments * radix_temp_words(n) words.  *sorted_vals receives
+// whichever value buffer holds the result.  With segments > 1 the buffers
+// hold that many independent arrays of n pairs, back to back, sorted in the
+// same launches.
 int64_t radix_temp_words(int64_t n);
 cudaError_t radix_sort(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt,
                        uint32_t* temp, int64_t n, int lo_bit, int hi_bit, cudaStream_t s,
-                       uint32_t** sorted_vals);
+                       uint32_t** sorted_vals, int segments = 1);
 
 // records[i] = (xyz[perm[i]], perm[i]) as float4; perm == nullptr -> identity.
 cudaError_t launch_gather(const float* xyz, int64_t n, const uint32_t* perm, float4* records,
