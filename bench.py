@@ -410,24 +410,28 @@ def measured_hbm_peak():
 
 def l2_roofline(achieved, l2_bytes):
     """Secondary roofline: the working set is L2-resident, so set the achieved
-    algorithmic GB/s against a live L2 read probe (sum over a tensor of half
-    the L2 size, best of 10) -- a lower bound of the L2 read bandwidth."""
+    algorithmic GB/s against a live L2 read probe (the library's probe kernel:
+    32 L1-bypassing passes over a buffer of half the L2 size in one launch,
+    best of 5)."""
     import torch
+    import icp_nearest_neighbour_gb300 as nn
     x = torch.ones(l2_bytes // 2 // 4, dtype=torch.float32, device="cuda")
-    for _ in range(3):
-        x.sum()
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    reps = 32
+    for _ in range(2):
+        nn.probe_l2_read(x, reps, sink)
     best = float("inf")
-    for _ in range(10):
+    for _ in range(5):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        x.sum()
+        nn.probe_l2_read(x, reps, sink)
         b.record()
         torch.cuda.synchronize()
         best = min(best, a.elapsed_time(b) * 1e-3)
-    peak = x.numel() * 4 / best / 1e9
+    peak = x.numel() * 4 * reps / best / 1e9
     return {"achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "peak_source": "live probe: torch sum over an L2-resident tensor of half the L2 size, best of 10 "
-                           "(a lower bound of the L2 read bandwidth)"}
+            "peak_source": "live probe: icpnn_probe_l2_read, 32 L1-bypassing read passes over half the "
+                           "L2 in one launch, best of 5"}
 
 
 def host_cores():

@@ -98,6 +98,7 @@ def load(build_if_missing: bool = False):
         "icpnn_last_error": ([], ctypes.c_char_p),
         "icpnn_launch_count": ([], i64),
         "icpnn_version": ([], i32),
+        "icpnn_probe_l2_read": ([P, i64, i32, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -211,6 +212,13 @@ def kdtree_build_device(points, leaf_size: int, max_depth: int = -1, round_robin
                                          SPLIT_ROUND_ROBIN if round_robin else 0, ctypes.byref(h),
                                          _stream(stream)))
     return KDTree(h)
+
+
+def probe_l2_read(buf, repeats: int, sink, stream=None):
+    """Measurement helper: `repeats` L1-bypassing read passes over a device
+    buffer (a CUDA tensor whose byte size is a multiple of 16) in one launch."""
+    _check(load().icpnn_probe_l2_read(ctypes.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size(),
+                                      int(repeats), ctypes.c_void_p(sink.data_ptr()), _stream(stream)))
 
 
 def kdtree_upload(tree: KDTree, stream=None):

@@ -142,3 +142,14 @@ def test_device_tree_uploads_to_host_copy_on_demand(nn, oracle_mod):
     ex2 = nn.kdtree_export(t)
     for k in ex1:
         np.testing.assert_array_equal(ex1[k], ex2[k])
+
+
+def test_l2_probe_runs_and_checks_its_arguments(nn):
+    import torch
+    x = torch.ones(1 << 20, dtype=torch.float32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nn.probe_l2_read(x, 4, sink)
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 0
+    with pytest.raises(nn.IcpnnError):
+        nn.probe_l2_read(x[:3], 1, sink)      # 12 bytes: not a multiple of 16

@@ -20,9 +20,11 @@ def lib():
 
 
 def test_library_exports_every_declared_symbol(lib):
-    header = open(os.path.join(ROOT, "include", "icpnn.h")).read()
+    import glob
+    header = "".join(open(h).read() for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
     declared = set(re.findall(r"\b(icpnn_[a-z_0-9]+)\s*\(", header))
-    assert {"icpnn_kdtree_build", "icpnn_kdtree_upload", "icpnn_nn_query", "icpnn_icp_align"} <= declared
+    assert {"icpnn_kdtree_build", "icpnn_kdtree_build_device", "icpnn_kdtree_upload", "icpnn_nn_query",
+            "icpnn_icp_align", "icpnn_probe_l2_read"} <= declared
     handle = lib.load()
     for name in sorted(declared):
         assert hasattr(handle, name), name
