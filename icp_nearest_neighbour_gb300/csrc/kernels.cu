@@ -399,20 +399,27 @@ __global__ void __launch_bounds__(kThreads) gather_u32_kernel(const uint32_t* __
     dst[i] = src[perm[i]];
 }
 
-__device__ __forceinline__ bool voxel_head(const float* __restrict__ xyz, const uint32_t* __restrict__ order,
-                                           int64_t i, int64_t m, const VoxelGrid& g) {
+// Voxel key of every kept point in sorted order (computed once; the run
+// boundaries and centroids below compare these instead of recomputing).
+__global__ void __launch_bounds__(kThreads) voxel_sorted_keys_kernel(const float* __restrict__ xyz,
+                                                                     const uint32_t* __restrict__ order, int64_t m,
+                                                                     VoxelGrid g,
+                                                                     unsigned long long* __restrict__ skey) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < m; i += stride)
+    skey[i] = voxel_key(xyz, order[i], g);
+}
+
+__device__ __forceinline__ bool voxel_head(const unsigned long long* __restrict__ skey, int64_t i, int64_t m) {
   if (i >= m) return false;
-  if (i == 0) return true;
-  return voxel_key(xyz, order[i], g) != voxel_key(xyz, order[i - 1], g);
+  return i == 0 || skey[i] != skey[i - 1];
 }
 
 // per block of kThreads sorted positions: number of voxel heads
-__global__ void __launch_bounds__(kThreads) voxel_head_count_kernel(const float* __restrict__ xyz,
-                                                                    const uint32_t* __restrict__ order,
-                                                                    int64_t m, VoxelGrid g,
-                                                                    uint32_t* __restrict__ block_heads) {
+__global__ void __launch_bounds__(kThreads) voxel_head_count_kernel(const unsigned long long* __restrict__ skey,
+                                                                    int64_t m, uint32_t* __restrict__ block_heads) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  const uint32_t h = voxel_head(xyz, order, i, m, g) ? 1u : 0u;
+  const uint32_t h = voxel_head(skey, i, m) ? 1u : 0u;
   const uint32_t c = __reduce_add_sync(kFull, h);
   __shared__ uint32_t warp_c[kThreads / 32];
   if ((threadIdx.x & 31) == 0) warp_c[threadIdx.x >> 5] = c;
@@ -441,27 +448,50 @@ __global__ void __launch_bounds__(kThreads) scan_one_block_kernel(uint32_t* __re
 }
 
 // every voxel head: its ordinal (block offset + rank in block), then the
-// centroid of its run of equal keys, summed in sorted (= input) order
+// centroid of its run of equal keys, summed in sorted (= input) order; the
+// run's keys and indices are read four at a time.
 __global__ void __launch_bounds__(kThreads) voxel_emit_kernel(const float* __restrict__ xyz,
                                                               const uint32_t* __restrict__ order, int64_t m,
-                                                              VoxelGrid g,
+                                                              const unsigned long long* __restrict__ skey,
                                                               const uint32_t* __restrict__ block_offset,
                                                               float* __restrict__ out) {
   __shared__ uint32_t warp_sums[kThreads / 32];
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  const bool head = voxel_head(xyz, order, i, m, g);
+  const bool head = voxel_head(skey, i, m);
   const uint32_t rank = block_exclusive_scan(head ? 1u : 0u, warp_sums, nullptr);
   if (!head) return;
   const int64_t ord = static_cast<int64_t>(block_offset[blockIdx.x]) + rank;
-  const unsigned long long key = voxel_key(xyz, order[i], g);
+  const unsigned long long key = skey[i];
   double sx = 0.0, sy = 0.0, sz = 0.0;
   int64_t j = i;
-  for (; j < m; ++j) {
-    const uint32_t p = order[j];
-    if (j > i && voxel_key(xyz, p, g) != key) break;
-    sx += static_cast<double>(xyz[3 * static_cast<int64_t>(p)]);
-    sy += static_cast<double>(xyz[3 * static_cast<int64_t>(p) + 1]);
-    sz += static_cast<double>(xyz[3 * static_cast<int64_t>(p) + 2]);
+  for (bool more = true; more;) {
+    uint32_t p[4];
+    bool in[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t jj = j + u;
+      in[u] = jj < m && skey[jj] == key;
+      p[u] = in[u] ? order[jj] : 0u;
+    }
+    float c[4][3];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t q = static_cast<int64_t>(p[u]);
+      c[u][0] = in[u] ? xyz[3 * q] : 0.f;
+      c[u][1] = in[u] ? xyz[3 * q + 1] : 0.f;
+      c[u][2] = in[u] ? xyz[3 * q + 2] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!in[u]) {
+        more = false;
+        break;
+      }
+      sx += static_cast<double>(c[u][0]);
+      sy += static_cast<double>(c[u][1]);
+      sz += static_cast<double>(c[u][2]);
+      ++j;
+    }
   }
   const double cnt = static_cast<double>(j - i);
   out[3 * ord] = static_cast<float>(sx / cnt);
@@ -1066,11 +1096,14 @@ cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const i
   return cudaGetLastError();
 }
 
-int64_t voxel_scratch_words(int64_t n) {
-  // key_lo, key_hi, vals, alt keys, alt vals, gathered hi, radix temp, block heads
+// Scratch words: key_lo, key_hi, vals, alt keys, alt vals, gathered hi,
+// radix temp, block heads, then (8-byte aligned) the sorted 64-bit keys.
+int64_t voxel_key_offset(int64_t n) {
   const int64_t blocks = (n + kThreads - 1) / kThreads;
-  return 6 * std::max<int64_t>(n, 1) + radix_temp_words(n) + std::max<int64_t>(blocks, 1) + 64;
+  const int64_t w = 6 * std::max<int64_t>(n, 1) + radix_temp_words(n) + std::max<int64_t>(blocks, 1) + 64;
+  return (w + 1) & ~int64_t{1};
 }
+int64_t voxel_scratch_words(int64_t n) { return voxel_key_offset(n) + 2 * std::max<int64_t>(n, 1); }
 
 int voxel_downsample(const float* xyz, int64_t n, float v, float* out, int64_t* out_n, uint32_t* scratch,
                      long long* bounds, unsigned long long* total, long long* host_bounds, cudaStream_t s,
@@ -1111,6 +1144,7 @@ int voxel_downsample(const float* xyz, int64_t n, float v, float* out, int64_t* 
   uint32_t* gath = scratch + 5 * n;
   uint32_t* temp = scratch + 6 * n;
   uint32_t* block_heads = temp + radix_temp_words(n);
+  unsigned long long* skey = reinterpret_cast<unsigned long long*>(scratch + voxel_key_offset(n));
   voxel_keys_kernel<<<grid, kThreads, 0, s>>>(xyz, n, g, key_lo, bits > 32 ? key_hi : nullptr, vals);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   uint32_t* order = nullptr;
@@ -1126,10 +1160,11 @@ int voxel_downsample(const float* xyz, int64_t n, float v, float* out, int64_t* 
       return 0;
   }
   const int blocks = static_cast<int>((m + kThreads - 1) / kThreads);
-  voxel_head_count_kernel<<<blocks, kThreads, 0, s>>>(xyz, order, m, g, block_heads);
+  voxel_sorted_keys_kernel<<<grid, kThreads, 0, s>>>(xyz, order, m, g, skey);
+  voxel_head_count_kernel<<<blocks, kThreads, 0, s>>>(skey, m, block_heads);
   scan_one_block_kernel<<<1, kThreads, 0, s>>>(block_heads, blocks, total);
-  voxel_emit_kernel<<<blocks, kThreads, 0, s>>>(xyz, order, m, g, block_heads, out);
-  g_launch_count.fetch_add(3, std::memory_order_relaxed);
+  voxel_emit_kernel<<<blocks, kThreads, 0, s>>>(xyz, order, m, skey, block_heads, out);
+  g_launch_count.fetch_add(4, std::memory_order_relaxed);
   if ((*err = cudaGetLastError()) != cudaSuccess) return 0;
   unsigned long long h_total = 0;
   if ((*err = cudaMemcpyAsync(&h_total, total, sizeof(h_total), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return 0;
