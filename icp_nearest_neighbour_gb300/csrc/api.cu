@@ -254,13 +254,17 @@ struct Pass {
   uint32_t* leaf_of = nullptr; // per source record: leaf of the last best match (warm start)
   float shift_q[3] = {0, 0, 0};
   float max_d2 = INFINITY;
+  float* thr = nullptr;  // device: the 3-sigma threshold handed from one residual pass to the next
 };
 
 int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bool want_slots,
                bool warm_start, cudaStream_t s, Scratch& sc, Pass* ps) {
   ps->tree = t;
   ps->n = n;
-  if (want_slots) ICPNN_CUDA(sc.alloc(&ps->slot_of, n));
+  if (want_slots) {
+    ICPNN_CUDA(sc.alloc(&ps->slot_of, n));
+    ICPNN_CUDA(sc.alloc(&ps->thr, 1));
+  }
   if (warm_start) {
     ICPNN_CUDA(sc.alloc(&ps->leaf_of, n));
     ICPNN_CUDA(cudaMemsetAsync(ps->leaf_of, 0, static_cast<size_t>(n) * sizeof(uint32_t), s));
@@ -334,25 +338,41 @@ int timing_events(size_t count, cudaEvent_t** out) {
 // One residual pass (see launch_residual_pass) under float32 (R, t): returns
 // the number of matched pairs, the sum of their squared residuals, and the
 // moments of the pairs with e2 <= thr.
-int residual_run(const Pass& ps, const float R[9], const float tr[3], float thr, cudaStream_t s,
-                 double* pairs, double* sum_e2, icpnn_moments* kept) {
+// Residual rejection of one iteration (page section 4.4), two passes back to
+// back on the stream: the first sums e2 over all matched pairs and leaves the
+// 3-sigma threshold in device memory, the second keeps the pairs within it
+// and sums their moments; the host waits once.  The first pass publishes in
+// the upper half of the mapped buffer.
+constexpr int kSecondSlot = 32;
+
+int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream_t s, double* sigma2,
+                 icpnn_moments* kept) {
   IcpPassParams p;
   std::memcpy(p.R, R, sizeof(p.R));
   std::memcpy(p.t, tr, sizeof(p.t));
   std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
   std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
-  p.max_d2 = thr;
-  p.seq = ++ps.mb->seq;
+  p.max_d2 = INFINITY;
+  const unsigned long long seq_a = ++ps.mb->seq;
+  p.seq = seq_a;
   ICPNN_CUDA(launch_residual_pass(*ps.tree, ps.src.recs, ps.slot_of, ps.n, p, ps.partials, ps.counter,
-                                  ps.mb->dev, ps.grid, s));
-  const volatile unsigned long long* flag =
+                                  ps.mb->dev + kSecondSlot, ps.grid, s, nullptr, ps.thr));
+  const unsigned long long seq_b = ++ps.mb->seq;
+  p.seq = seq_b;
+  ICPNN_CUDA(launch_residual_pass(*ps.tree, ps.src.recs, ps.slot_of, ps.n, p, ps.partials, ps.counter,
+                                  ps.mb->dev, ps.grid, s, ps.thr, nullptr));
+  const volatile unsigned long long* flag_b =
       reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-  if (int rc = wait_published(flag, p.seq, s)) return rc;
+  const volatile unsigned long long* flag_a =
+      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kSecondSlot + kMomentSlots);
+  if (int rc = wait_published(flag_b, seq_b, s)) return rc;
+  if (int rc = wait_published(flag_a, seq_a, s)) return rc;
   std::atomic_thread_fence(std::memory_order_acquire);
   double raw[kMomentSlots];
+  std::memcpy(raw, const_cast<const double*>(ps.mb->host + kSecondSlot), sizeof(raw));
+  const double pairs = raw[1];
+  *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
   std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
-  *pairs = raw[1];
-  *sum_e2 = raw[17];
   decode_moments(raw, ps.src.shift, ps.shift_q, kept);
   kept->n_nonfinite = 0;
   kept->sum_d2 = 0.0;
@@ -749,12 +769,8 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       // page section 4.4: residuals under the first solve, 3-sigma rule, re-solve
       float R1[9], t1[3];
       transform_to_f32(Tn, R1, t1);
-      double pairs = 0.0, sum_e2 = 0.0;
       icpnn_moments kept;
-      if (int rc = residual_run(ps, R1, t1, INFINITY, s, &pairs, &sum_e2, &kept)) return rc;
-      sigma2 = pairs > 0.0 ? sum_e2 / pairs : 0.0;
-      if (int rc = residual_run(ps, R1, t1, float_threshold(9.0 * sigma2), s, &pairs, &sum_e2, &kept))
-        return rc;
+      if (int rc = residual_run(ps, R1, t1, s, &sigma2, &kept)) return rc;
       n_inliers = kept.n_accepted;
       if (n_inliers < 3 || kabsch_solve(kept, Tn) != ICPNN_OK)
         return fail(ICPNN_ERR_DEGENERATE, "icp_align: residual rejection left a degenerate pair set at "

@@ -24,6 +24,8 @@
 // visiting order.
 #include <cuda_runtime.h>
 
+#include <cfloat>
+
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -783,11 +785,24 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
 // the block partials in block order.  out[0] = c0, out[1] = c1 (counts),
 // out[2 + v] = acc[v].  With kPublish the last block then publishes `seq`
 // in the word after the result, once the result is visible system-wide.
+// The float threshold t with float(e2) <= t exactly when e2 <= limit in
+// double: the largest float not above limit (+inf stays +inf).
+__device__ __forceinline__ float float_threshold_dev(double limit) {
+  if (isinf(limit)) return __int_as_float(0x7f800000);
+  if (limit >= static_cast<double>(FLT_MAX)) return FLT_MAX;
+  float f = __double2float_rn(limit);
+  if (static_cast<double>(f) > limit) f = nextafterf(f, -__int_as_float(0x7f800000));
+  return f;
+}
+
+// With thr_out, the last block also stores the 3-sigma threshold of the
+// residual rejection from this reduction's c1 (pairs) and acc[15] (sum of e2):
+// float_threshold(9 * sum_e2 / pairs), 0 pairs giving sigma^2 = 0.
 template <bool kPublish>
 __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
                                                double* __restrict__ partials,
                                                unsigned int* __restrict__ counter, double* out,
-                                               unsigned long long seq) {
+                                               unsigned long long seq, float* thr_out = nullptr) {
   __shared__ double s_warp[kThreads / 32][kMomentSlots];
   __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
   __shared__ bool s_last;
@@ -841,6 +856,11 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
     *counter = 0u;
+    if (thr_out != nullptr) {
+      const double pairs = s_fin[0][1];
+      const double sigma2 = pairs > 0.0 ? s_fin[0][17] / pairs : 0.0;
+      *thr_out = float_threshold_dev(9.0 * sigma2);
+    }
     if (kPublish) {
       __threadfence_system();
       *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq;
@@ -941,7 +961,8 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
 __global__ void __launch_bounds__(kThreads) residual_pass_kernel(
     const float4* __restrict__ pts, const float4* __restrict__ src, const int32_t* __restrict__ slot_of,
     int64_t n, IcpPassParams p, double* __restrict__ partials, unsigned int* __restrict__ counter,
-    double* out) {
+    double* out, const float* thr_in, float* thr_out) {
+  if (thr_in != nullptr) p.max_d2 = *thr_in;  // written by the previous pass on this stream
   float acc[16];
 #pragma unroll
   for (int v = 0; v < 16; ++v) acc[v] = 0.f;
@@ -964,7 +985,7 @@ __global__ void __launch_bounds__(kThreads) residual_pass_kernel(
     }
     acc[15] = sum_e2;
   }
-  reduce_moments<true>(acc, n_keep, n_pair, partials, counter, out, p.seq);
+  reduce_moments<true>(acc, n_keep, n_pair, partials, counter, out, p.seq, thr_out);
 }
 
 inline int smem_slots_for(const icpnn_tree& t) {
@@ -1089,9 +1110,10 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
 
 cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,
                                  int64_t n, const IcpPassParams& p, double* partials,
-                                 uint32_t* counter, double* out, int grid, cudaStream_t s) {
+                                 uint32_t* counter, double* out, int grid, cudaStream_t s,
+                                 const float* thr_in, float* thr_out) {
   residual_pass_kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(t.dev.points), src,
-                                                 slot_of, n, p, partials, counter, out);
+                                                 slot_of, n, p, partials, counter, out, thr_in, thr_out);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

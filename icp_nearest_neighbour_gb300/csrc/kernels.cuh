@@ -74,11 +74,14 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
 
 // Residual pass of the residual rejection (same grid, partials, counter and
 // published result layout as the ICP pass): out[0] = pairs with
-// e2 <= p.max_d2, out[1] = pairs with a match, out[2..16] = moments of the
-// kept pairs, out[17] = sum of e2 over all matched pairs.
+// e2 <= threshold, out[1] = pairs with a match, out[2..16] = moments of the
+// kept pairs, out[17] = sum of e2 over all matched pairs.  The threshold is
+// p.max_d2, or *thr_in (device) when thr_in is given; with thr_out the pass
+// stores float_threshold(9 * out[17] / out[1]) there for the next pass.
 cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,
                                  int64_t n, const IcpPassParams& p, double* partials,
-                                 uint32_t* counter, double* out, int grid, cudaStream_t s);
+                                 uint32_t* counter, double* out, int grid, cudaStream_t s,
+                                 const float* thr_in = nullptr, float* thr_out = nullptr);
 
 // Voxel-grid downsampling of n points (device xyz) into out (device, capacity
 // n x 3); *out_n = occupied voxels.  scratch: voxel_scratch_words(n) words;
