@@ -238,7 +238,7 @@ def run_ours(args):
     _, frame_srcs, _ = workloads.scene_frames(8)
     frame_dev = [torch.from_numpy(f).cuda() for f in frame_srcs]
     multi = {}
-    for mc in (1, 4):
+    for mc in (1, 4, 8):
         nn.icp_align_batch(tree, frame_dev, case.max_iter, case.eps, dmax, max_concurrent=mc, stream=stream)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
