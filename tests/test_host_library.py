@@ -138,6 +138,16 @@ def test_tree_build_rejects_bad_input(lib):
         lib.kdtree_build(bad, 8)
 
 
+def test_device_build_checks_arguments_before_touching_a_device(lib):
+    """icpnn_kdtree_build_device validates like the host build, before any CUDA call."""
+    pts = W.uniform_cloud(100, 2)
+    for args, status in [((pts, 0), "INVALID_ARG"), ((pts, 65), "INVALID_ARG"),
+                         ((pts, 8, 21), "TREE_DEPTH"), ((np.zeros((0, 3), np.float32), 8), "INVALID_ARG")]:
+        with pytest.raises(lib.IcpnnError) as e:
+            lib.kdtree_build_device(*args)
+        assert e.value.status == status
+
+
 def _moments_from_pairs(S, Q):
     S = np.asarray(S, np.float64)
     Q = np.asarray(Q, np.float64)
