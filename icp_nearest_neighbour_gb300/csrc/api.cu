@@ -18,6 +18,27 @@
 
 namespace icpnn {
 
+// Scratch memory comes from the device's default stream-ordered pool.  By
+// default the pool hands freed memory back to the driver at every
+// synchronisation, so the next call maps it again; keep up to 1 GiB of it
+// per device instead (a setting of this process's pool only).
+void keep_pool_memory() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<bool> done[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return;
+  if (done[dev].load(std::memory_order_acquire)) return;
+  cudaMemPool_t pool = nullptr;
+  if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+    uint64_t keep = uint64_t{1} << 30;
+    uint64_t cur = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &cur) == cudaSuccess && cur < keep)
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  }
+  cudaGetLastError();
+  done[dev].store(true, std::memory_order_release);
+}
+
 extern std::atomic<int64_t> g_launch_count;
 
 namespace {
@@ -56,7 +77,7 @@ bool is_device_pointer(const void* p) {
 // Device allocations from the stream-ordered pool, returned on the same stream.
 class Scratch {
  public:
-  explicit Scratch(cudaStream_t s) : s_(s) {}
+  explicit Scratch(cudaStream_t s) : s_(s) { keep_pool_memory(); }
   ~Scratch() {
     for (void* p : ptrs_) cudaFreeAsync(p, s_);
   }
@@ -387,6 +408,23 @@ void transform_to_f32(const double T[16], float R[9], float t[3]) {
   }
 }
 
+// Device arrays of a tree come from the device's stream-ordered pool.  The
+// release waits for all work on the device first, as cudaFree would, then
+// hands the arrays back to the pool (kept for the next tree).
+void release_device_tree(DeviceTree* d) {
+  if (d->nodes == nullptr) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  cudaSetDevice(d->device);
+  cudaDeviceSynchronize();
+  cudaFreeAsync(d->nodes, nullptr);
+  if (d->points) cudaFreeAsync(d->points, nullptr);
+  cudaStreamSynchronize(nullptr);
+  cudaGetLastError();
+  cudaSetDevice(cur);
+  *d = DeviceTree{};
+}
+
 // Host copies of a device-built tree's nodes, boxes and records, made on first
 // need.
 int ensure_host_copy(icpnn_tree* t) {
@@ -486,14 +524,7 @@ int icpnn_kdtree_build_device(const float* xyz, int64_t n, int32_t leaf_size, in
 
 void icpnn_kdtree_free(icpnn_tree* t) {
   if (t == nullptr) return;
-  if (t->dev.nodes != nullptr) {
-    int cur = -1;
-    cudaGetDevice(&cur);
-    cudaSetDevice(t->dev.device);
-    cudaFree(t->dev.nodes);
-    cudaFree(t->dev.points);
-    cudaSetDevice(cur);
-  }
+  release_device_tree(&t->dev);
   delete t;
 }
 
@@ -505,13 +536,7 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   ICPNN_CUDA(cudaGetDevice(&cur));
   if (t->dev.nodes != nullptr && t->dev.device == cur) return ICPNN_OK;
   if (int rc = ensure_host_copy(t)) return rc;
-  if (t->dev.nodes != nullptr) {
-    cudaSetDevice(t->dev.device);
-    cudaFree(t->dev.nodes);
-    cudaFree(t->dev.points);
-    cudaSetDevice(cur);
-    t->dev = DeviceTree{};
-  }
+  release_device_tree(&t->dev);
   Node* nodes = nullptr;
   float* pts = nullptr;
   // nodes and boxes share one allocation; heap_slots >= 2 is a power of two,
@@ -519,17 +544,20 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   const size_t nb = static_cast<size_t>(t->heap_slots) * sizeof(Node);
   const size_t bb = static_cast<size_t>(t->heap_slots) * 8 * sizeof(float);
   const size_t pb = static_cast<size_t>(t->n) * 4 * sizeof(float);
-  cudaError_t e = cudaMalloc(&nodes, nb + bb);
+  keep_pool_memory();
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nodes), nb + bb, s);
   float* boxes = nodes ? reinterpret_cast<float*>(reinterpret_cast<char*>(nodes) + nb) : nullptr;
-  if (e == cudaSuccess) e = cudaMalloc(&pts, pb);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&pts), pb, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(nodes, t->nodes.data(), nb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(boxes, t->boxes.data(), bb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pts, t->records.data(), pb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    if (nodes) cudaFree(nodes);
-    if (pts) cudaFree(pts);
+    if (nodes) cudaFreeAsync(nodes, s);
+    if (pts) cudaFreeAsync(pts, s);
+    cudaStreamSynchronize(s);
+    cudaGetLastError();
     return fail(e == cudaErrorMemoryAllocation ? ICPNN_ERR_NO_MEMORY : ICPNN_ERR_CUDA,
                 std::string("kdtree_upload: ") + cudaGetErrorString(e));
   }

@@ -84,6 +84,9 @@ namespace icpnn {
 int fail(int code, const std::string& msg);
 void clear_error();
 
+// Keep freed scratch in the device's default memory pool (api.cu).
+void keep_pool_memory();
+
 // Host tree build (kdtree_build.cpp).
 int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t);

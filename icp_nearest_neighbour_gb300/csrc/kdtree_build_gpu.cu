@@ -580,7 +580,7 @@ inline int grid_for(int64_t items) { return static_cast<int>(std::max<int64_t>(1
 struct DeviceMem {
   std::vector<void*> ptrs;
   cudaStream_t s;
-  explicit DeviceMem(cudaStream_t st) : s(st) {}
+  explicit DeviceMem(cudaStream_t st) : s(st) { keep_pool_memory(); }
   ~DeviceMem() {
     for (void* p : ptrs) cudaFreeAsync(p, s);
   }
@@ -613,11 +613,14 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
   float* pts = nullptr;
   const size_t nb = static_cast<size_t>(slots) * sizeof(Node);
   const size_t bb = static_cast<size_t>(slots) * 8 * sizeof(float);
-  e = cudaMalloc(&nodes, nb + bb);
-  if (e == cudaSuccess) e = cudaMalloc(&pts, static_cast<size_t>(n) * 4 * sizeof(float));
+  keep_pool_memory();
+  e = cudaMallocAsync(reinterpret_cast<void**>(&nodes), nb + bb, s);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&pts), static_cast<size_t>(n) * 4 * sizeof(float), s);
   auto release = [&]() {
-    if (nodes) cudaFree(nodes);
-    if (pts) cudaFree(pts);
+    if (nodes) cudaFreeAsync(nodes, s);
+    if (pts) cudaFreeAsync(pts, s);
+    cudaStreamSynchronize(s);
+    cudaGetLastError();
   };
   if (e != cudaSuccess) {
     cudaGetLastError();
