@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(256) gather_lists_kernel(const float4* __restr
     L[i] = __ldg(&P[ids[i]]);
 }
 
-// Fixed-order reductions: butterfly in the warp (every lane gets the result),
-// then the warps of the block in order.
+// Fixed-order reductions: butterfly in the warp (every lane gets the result);
+// blocks then add the warps' results in warp order.
 __device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
@@ -130,27 +130,6 @@ __device__ __forceinline__ float warp_min(float v) {
   for (int off = 16; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, off));
   return v;
 }
-__device__ __forceinline__ double block_sum(double v, double* sh) {
-  v = warp_sum(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
-  __syncthreads();
-  double s = 0.0;
-#pragma unroll
-  for (int w = 0; w < kBWarps; ++w) s += sh[w];
-  return s;
-}
-__device__ __forceinline__ float block_min(float v, float* sh) {
-  v = warp_min(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float s = sh[0];
-#pragma unroll
-  for (int w = 1; w < kBWarps; ++w) s = fminf(s, sh[w]);
-  return s;
-}
-
 // The block's node and chunk; false (block-uniform) when there is none.
 __device__ __forceinline__ bool block_chunk(const LevelArgs& a, uint32_t* k, int64_t* lo, int64_t* cnt,
                                             int64_t* b0, int64_t* b1, int* j) {
@@ -227,8 +206,6 @@ __global__ void __launch_bounds__(kBT) level_sums_kernel(LevelArgs a, const floa
                                                          double* __restrict__ part, unsigned int* __restrict__ counter,
                                                          double* __restrict__ mean, Node* __restrict__ nodes,
                                                          float4* __restrict__ boxes) {
-  __shared__ double shd[kBWarps];
-  __shared__ float shf[kBWarps];
   __shared__ bool s_last;
   uint32_t k;
   int64_t lo, cnt, b0, b1;
@@ -247,16 +224,28 @@ __global__ void __launch_bounds__(kBT) level_sums_kernel(LevelArgs a, const floa
       mx[e] = fmaxf(mx[e], c[e]);
     }
   }
+  // all nine values in one round: butterfly in each warp, then the warps in
+  // order (a fixed association)
   double r[9];
 #pragma unroll
   for (int e = 0; e < 3; ++e) {
-    r[e] = block_sum(s[e], shd);
-    r[3 + e] = static_cast<double>(-block_min(mn[e], shf));
-    r[6 + e] = static_cast<double>(-block_min(-mx[e], shf));
+    r[e] = warp_sum(s[e]);
+    r[3 + e] = static_cast<double>(-warp_min(mn[e]));
+    r[6 + e] = static_cast<double>(-warp_min(-mx[e]));
   }
+  __shared__ double sh9[kBWarps][9];
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int e = 0; e < 9; ++e) sh9[threadIdx.x >> 5][e] = r[e];
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int e = 0; e < 9; ++e) part[static_cast<int64_t>(blockIdx.x) * 9 + e] = r[e];
+    for (int e = 0; e < 9; ++e) {
+      double v = sh9[0][e];
+      for (int w = 1; w < kBWarps; ++w) v = e < 3 ? v + sh9[w][e] : fmax(v, sh9[w][e]);
+      part[static_cast<int64_t>(blockIdx.x) * 9 + e] = v;
+    }
   }
   const int64_t slot = k - (1u << a.d);
   const int chunks = static_cast<int>((cnt + kChunk - 1) / kChunk);
@@ -301,7 +290,6 @@ __global__ void __launch_bounds__(kBT) level_sq_kernel(LevelArgs a, const float4
                                                        const double* __restrict__ mean,
                                                        double* __restrict__ part, unsigned int* __restrict__ counter,
                                                        Node* __restrict__ nodes) {
-  __shared__ double shd[kBWarps];
   __shared__ bool s_last;
   uint32_t k;
   int64_t lo, cnt, b0, b1;
@@ -320,13 +308,23 @@ __global__ void __launch_bounds__(kBT) level_sq_kernel(LevelArgs a, const float4
     q1 += e1 * e1;
     q2 += e2 * e2;
   }
-  const double r0 = block_sum(q0, shd);
-  const double r1 = block_sum(q1, shd);
-  const double r2 = block_sum(q2, shd);
+  q0 = warp_sum(q0);
+  q1 = warp_sum(q1);
+  q2 = warp_sum(q2);
+  __shared__ double sh3[kBWarps][3];
+  if ((threadIdx.x & 31) == 0) {
+    sh3[threadIdx.x >> 5][0] = q0;
+    sh3[threadIdx.x >> 5][1] = q1;
+    sh3[threadIdx.x >> 5][2] = q2;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    part[static_cast<int64_t>(blockIdx.x) * 9] = r0;
-    part[static_cast<int64_t>(blockIdx.x) * 9 + 1] = r1;
-    part[static_cast<int64_t>(blockIdx.x) * 9 + 2] = r2;
+#pragma unroll
+    for (int e = 0; e < 3; ++e) {
+      double v = 0.0;
+      for (int w = 0; w < kBWarps; ++w) v += sh3[w][e];
+      part[static_cast<int64_t>(blockIdx.x) * 9 + e] = v;
+    }
   }
   const int chunks = static_cast<int>((cnt + kChunk - 1) / kChunk);
   if (!last_of_node(&counter[slot], chunks, &s_last) || threadIdx.x >= 32) return;

@@ -153,3 +153,24 @@ def test_l2_probe_runs_and_checks_its_arguments(nn):
     assert int(sink.item()) == 0
     with pytest.raises(nn.IcpnnError):
         nn.probe_l2_read(x[:3], 1, sink)      # 12 bytes: not a multiple of 16
+
+
+def test_device_tree_matches_host_tree_at_4M_points(nn):
+    """The large workload's 4M-point target (leaf 16, depth 18): device build
+    against the host build, node for node (two independent implementations;
+    the host build is pinned to the oracle on the smaller clouds)."""
+    c = W.large_case()
+    th = nn.kdtree_build(c.target, c.leaf_size)
+    td = nn.kdtree_build_device(c.target, c.leaf_size)
+    eh, ed = nn.kdtree_export(th), nn.kdtree_export(td)
+    for k in ("split_val", "split_dim", "left", "right", "start", "end"):
+        np.testing.assert_array_equal(ed[k], eh[k], err_msg=k)
+    # same point sets per leaf: indices sorted within each leaf's range
+    leaves = np.flatnonzero(eh["left"] < 0)
+    order = np.argsort(eh["start"][leaves])
+    sizes = (eh["end"] - eh["start"])[leaves][order]
+    leaf_of_pos = np.repeat(np.arange(len(leaves)), sizes)
+    assert len(leaf_of_pos) == len(c.target)
+    def per_leaf_sorted(li):
+        return li[np.lexsort((li, leaf_of_pos))]
+    np.testing.assert_array_equal(per_leaf_sorted(ed["leaf_index"]), per_leaf_sorted(eh["leaf_index"]))
