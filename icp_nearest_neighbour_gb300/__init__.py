@@ -23,13 +23,15 @@ __all__ = [
     "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
     "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
     "kabsch", "icp_align", "icp_align_batch", "voxel_downsample",
-    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "MAX_DEPTH", "NOALLOC_MAX_POINTS",
+    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "NO_PRELAUNCH", "MAX_DEPTH",
+    "NOALLOC_MAX_POINTS",
 ]
 
 MORTON_SORT = 1
 TRACE_TIMING = 2
 RESIDUAL_REJECT = 4
 SPLIT_ROUND_ROBIN = 8
+NO_PRELAUNCH = 16
 MAX_DEPTH = 20
 NOALLOC_MAX_POINTS = 1 << 20
 
@@ -99,6 +101,7 @@ def load(build_if_missing: bool = False):
         "icpnn_launch_count": ([], i64),
         "icpnn_version": ([], i32),
         "icpnn_probe_l2_read": ([P, i64, i32, P, P], ctypes.c_int),
+        "icpnn_probe_command_wait": ([P, P, i64, ctypes.c_uint64, i32, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -221,6 +224,16 @@ def probe_l2_read(buf, repeats: int, sink, stream=None):
                                       int(repeats), ctypes.c_void_p(sink.data_ptr()), _stream(stream)))
 
 
+def probe_command_wait(tree: KDTree, src, wait_ns: int, mode: int, stream=None) -> int:
+    """Test helper: one pre-launched pass whose blocks wait at most wait_ns for
+    their command; mode 0 sends none, 1 the stop command, 2 the identity.
+    Returns what the pass published: 0 nothing, 1 the abort marker, 2 its result."""
+    out = ctypes.c_int32(-1)
+    _check(load().icpnn_probe_command_wait(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
+                                           int(wait_ns), int(mode), ctypes.byref(out), _stream(stream)))
+    return out.value
+
+
 def kdtree_upload(tree: KDTree, stream=None):
     _check(load().icpnn_kdtree_upload(tree.handle, _stream(stream)))
 
@@ -310,9 +323,10 @@ def kabsch(moments: dict) -> np.ndarray:
 
 def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
               init_T=None, trace: bool = False, timing: bool = False, residual_reject: bool = False,
-              stream=None) -> dict:
+              prelaunch: bool = True, stream=None) -> dict:
     """Register src onto the tree's points; returns dict(T, final_mse, iters, trace).
-    residual_reject adds the 3-sigma residual rejection and re-solve to every iteration."""
+    residual_reject adds the 3-sigma residual rejection and re-solve to every iteration;
+    prelaunch=False launches each pass only after its transform is solved."""
     T = np.zeros(16)
     fmse = ctypes.c_double()
     iters = ctypes.c_int32()
@@ -322,7 +336,8 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
         init = ctypes.c_void_p(init_arr.ctypes.data)
     cap = int(max_iter) if (trace or timing) else 0
     recs = (IterRecord * max(cap, 1))()
-    flags = (TRACE_TIMING if timing else 0) | (RESIDUAL_REJECT if residual_reject else 0)
+    flags = ((TRACE_TIMING if timing else 0) | (RESIDUAL_REJECT if residual_reject else 0)
+             | (0 if prelaunch else NO_PRELAUNCH))
     _check(load().icpnn_icp_align(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
                                   int(max_iter), float(eps), float(max_corr_dist), init,
                                   ctypes.c_void_p(T.ctypes.data), ctypes.byref(fmse), ctypes.byref(iters),
@@ -339,7 +354,7 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
 
 def icp_align_batch(tree: KDTree, srcs, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
                     init_T=None, residual_reject: bool = False, max_concurrent: int = 4,
-                    stream=None) -> dict:
+                    prelaunch: bool = True, stream=None) -> dict:
     """Register several sources against one tree, several frames in flight.
 
     Returns dict(T (n, 4, 4), final_mse (n,), iters (n,), status (n,))."""
@@ -359,7 +374,8 @@ def icp_align_batch(tree: KDTree, srcs, max_iter: int, eps: float, max_corr_dist
                                       float(max_corr_dist), init, ctypes.c_void_p(T.ctypes.data),
                                       ctypes.c_void_p(fmse.ctypes.data), ctypes.c_void_p(iters.ctypes.data),
                                       ctypes.c_void_p(status.ctypes.data),
-                                      RESIDUAL_REJECT if residual_reject else 0, int(max_concurrent),
+                                      (RESIDUAL_REJECT if residual_reject else 0)
+                                      | (0 if prelaunch else NO_PRELAUNCH), int(max_concurrent),
                                       _stream(stream))
     out = {"T": T.reshape(n, 4, 4), "final_mse": fmse, "iters": iters, "status": status}
     if rc != 0:

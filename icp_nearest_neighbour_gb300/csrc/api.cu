@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "icpnn_internal.h"
+#include "icpnn_probe.h"
 #include "kernels.cuh"
 
 namespace icpnn {
@@ -106,6 +107,12 @@ struct MappedBuffer {
 };
 thread_local MappedBuffer tl_mapped;
 constexpr int kMappedDoubles = 64;
+// Doubles [0, kMomentSlots] hold a pass's result and its sequence word; the
+// host-written PassCommand of pre-launched passes starts at byte 256, on a
+// cache line of its own.
+constexpr int kCommandOffset = 32;
+static_assert(kCommandOffset * sizeof(double) + sizeof(PassCommand) <= kMappedDoubles * sizeof(double),
+              "command block must fit the mapped buffer");
 
 int mapped_buffer(MappedBuffer** out) {
   if (tl_mapped.host == nullptr) {
@@ -270,6 +277,7 @@ struct Pass {
   int grid = 0;
   double* partials = nullptr;
   uint32_t* counter = nullptr;
+  CommandMirror* mirror = nullptr;  // device, zeroed: pre-launched passes' command copy
   MappedBuffer* mb = nullptr;
   int32_t* slot_of = nullptr;  // per Morton-ordered source record: matched slot or -1
   uint32_t* leaf_of = nullptr; // per source record: leaf of the last best match (warm start)
@@ -293,40 +301,105 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
   if (int rc = prepare_source(src, n, true, true, s, sc, &ps->src)) return rc;
   ps->grid = icp_pass_grid(*t, n);
   ICPNN_CUDA(sc.alloc(&ps->partials, static_cast<int64_t>(ps->grid) * kMomentSlots));
-  ICPNN_CUDA(sc.alloc(&ps->counter, 1));
-  ICPNN_CUDA(cudaMemsetAsync(ps->counter, 0, sizeof(uint32_t), s));
+  ICPNN_CUDA(sc.alloc(&ps->counter, 2));
+  ICPNN_CUDA(cudaMemsetAsync(ps->counter, 0, 2 * sizeof(uint32_t), s));
+  ICPNN_CUDA(sc.alloc(&ps->mirror, 1));
+  ICPNN_CUDA(cudaMemsetAsync(ps->mirror, 0, sizeof(CommandMirror), s));
   if (int rc = mapped_buffer(&ps->mb)) return rc;
   for (int d = 0; d < 3; ++d) ps->shift_q[d] = 0.5f * (t->bbox_lo[d] + t->bbox_hi[d]);
   ps->max_d2 = rejection_threshold(dmax);
   return ICPNN_OK;
 }
 
-// Wait until the pass with sequence number `seq` has published its result in
-// mapped memory.  Bounded: the stream is queried every few thousand polls, so
-// a failed or finished kernel ends the wait.
-int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s) {
+// Wait until the pass with sequence number `seq` has published its result (or
+// its abort marker, reported through *aborted) in mapped memory.  Bounded: the
+// stream is queried every few thousand polls, so a failed or finished kernel
+// ends the wait.
+int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s,
+                   bool* aborted = nullptr) {
   for (uint64_t spins = 1;; ++spins) {
-    if (*flag == seq) return ICPNN_OK;
-    if ((spins & 4095u) == 0) {
+    unsigned long long w = *flag;
+    if ((w & ~kPassAborted) != seq && (spins & 4095u) == 0) {
       const cudaError_t e = cudaStreamQuery(s);
-      if (e == cudaSuccess) {
-        if (*flag == seq) return ICPNN_OK;
-        return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
+      w = *flag;
+      if ((w & ~kPassAborted) != seq) {
+        if (e == cudaSuccess) return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
+        if (e != cudaErrorNotReady)
+          return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
       }
-      if (e != cudaErrorNotReady) return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
+    }
+    if ((w & ~kPassAborted) == seq) {
+      if (w & kPassAborted) {
+        if (aborted == nullptr) return fail(ICPNN_ERR_CUDA, "ICP pass aborted");
+        *aborted = true;
+      }
+      return ICPNN_OK;
     }
   }
 }
 
-int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, float* d2,
-             cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m) {
-  IcpPassParams p;
-  std::memcpy(p.R, R, sizeof(p.R));
-  std::memcpy(p.t, tr, sizeof(p.t));
+void read_moments(const Pass& ps, icpnn_moments* m) {
+  std::atomic_thread_fence(std::memory_order_acquire);
+  double raw[kMomentSlots];
+  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
+  decode_moments(raw, ps.src.shift, ps.shift_q, m);
+}
+
+IcpPassParams pass_params(const Pass& ps) {
+  IcpPassParams p{};
   std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
   std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
   p.max_d2 = ps.max_d2;
   p.seq = ++ps.mb->seq;
+  return p;
+}
+
+PassCommand* command_block(const MappedBuffer* mb, bool device) {
+  return reinterpret_cast<PassCommand*>((device ? mb->dev : mb->host) + kCommandOffset);
+}
+
+// Queue a pass whose transform the host supplies later (pass_command); its
+// sequence number goes to *seq.
+int pass_prelaunch(const Pass& ps, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned long long* seq) {
+  IcpPassParams p = pass_params(ps);
+  p.cmd = command_block(ps.mb, true);
+  p.mirror = ps.mirror;
+  p.wait_ns = kCommandWaitNs;
+  if (ev0) ICPNN_CUDA(cudaEventRecord(ev0, s));
+  ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev, nullptr,
+                             nullptr, ps.slot_of, ps.leaf_of, ps.grid, s));
+  if (ev1) ICPNN_CUDA(cudaEventRecord(ev1, s));
+  *seq = p.seq;
+  return ICPNN_OK;
+}
+
+// Hand pre-launched pass `seq` its transform, or (R == nullptr) tell it to
+// return without work.  The values are stored before the word that names
+// the pass, with release order.
+void pass_command(const Pass& ps, unsigned long long seq, const float* R, const float* tr) {
+  PassCommand* c = command_block(ps.mb, false);
+  if (R != nullptr) {
+    std::memcpy(c->rt, R, 9 * sizeof(float));
+    std::memcpy(c->rt + 9, tr, 3 * sizeof(float));
+  }
+  __atomic_store_n(&c->word, (seq << 1) | (R == nullptr ? 1ull : 0ull), __ATOMIC_RELEASE);
+}
+
+// A pre-launched pass that has no transform yet; stopped when the owner
+// leaves early, so that its blocks return at once.
+struct PendingPass {
+  const Pass* ps = nullptr;
+  unsigned long long seq = 0;
+  ~PendingPass() {
+    if (seq != 0) pass_command(*ps, seq, nullptr, nullptr);
+  }
+};
+
+int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, float* d2,
+             cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m) {
+  IcpPassParams p = pass_params(ps);
+  std::memcpy(p.R, R, sizeof(p.R));
+  std::memcpy(p.t, tr, sizeof(p.t));
   if (ev0) ICPNN_CUDA(cudaEventRecord(ev0, s));
   ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev,
                              idx, d2, ps.slot_of, idx == nullptr ? ps.leaf_of : nullptr, ps.grid, s));
@@ -334,10 +407,7 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
   const volatile unsigned long long* flag =
       reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
   if (int rc = wait_published(flag, p.seq, s)) return rc;
-  std::atomic_thread_fence(std::memory_order_acquire);
-  double raw[kMomentSlots];
-  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
-  decode_moments(raw, ps.src.shift, ps.shift_q, m);
+  read_moments(ps, m);
   return ICPNN_OK;
 }
 
@@ -368,7 +438,7 @@ constexpr int kSecondSlot = 32;
 
 int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream_t s, double* sigma2,
                  icpnn_moments* kept) {
-  IcpPassParams p;
+  IcpPassParams p{};
   std::memcpy(p.R, R, sizeof(p.R));
   std::memcpy(p.t, tr, sizeof(p.t));
   std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
@@ -712,7 +782,7 @@ int icpnn_icp_step_noalloc(const icpnn_tree* t, const float* src, int64_t n, con
   ICPNN_CUDA(cudaStreamSynchronize(s));
   float lo[3], hi[3];
   decode_bbox(h6, lo, hi);
-  IcpPassParams p;
+  IcpPassParams p{};
   std::memcpy(p.R, R, sizeof(p.R));
   std::memcpy(p.t, tr, sizeof(p.t));
   for (int d = 0; d < 3; ++d) {
@@ -752,9 +822,12 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: max_corr_dist is NaN");
   if (trace_cap < 0 || (trace_cap > 0 && trace == nullptr))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_align: bad trace buffer");
-  if (flags & ~(ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT))
+  if (flags & ~(ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_align: unknown flag");
   const bool residual = (flags & ICPNN_RESIDUAL_REJECT) != 0;
+  // the residual passes run between a pass and the next one's transform, so
+  // the next pass cannot be queued ahead of them
+  const bool prelaunch = !residual && (flags & ICPNN_NO_PRELAUNCH) == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   double T[16];
@@ -771,16 +844,60 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   Pass ps;
   if (int rc = pass_setup(t, src, n_src, max_corr_dist, residual, true, s, sc, &ps)) return rc;
 
+  // Pre-launched passes: `cur` evaluates T; `next` is queued behind it
+  // before its result is read and gets the solved transform as its command.
+  unsigned long long cur = 0;
+  PendingPass next{&ps, 0};
+  if (prelaunch) {
+    if (int rc = pass_prelaunch(ps, s, timed > 0 ? ev[0] : nullptr, timed > 0 ? ev[1] : nullptr, &cur))
+      return rc;
+    float R32[9], t32[3];
+    transform_to_f32(T, R32, t32);
+    pass_command(ps, cur, R32, t32);
+  }
+  // Result of pass `cur` (already commanded with transform T); a pass whose
+  // blocks gave up waiting is evaluated again by `next` under the same
+  // transform.  Queues a successor when `more` is set.
+  auto collect = [&](bool more, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m) -> int {
+    const volatile unsigned long long* flag =
+        reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
+    for (int attempt = 0;; ++attempt) {
+      if (more)
+        if (int rc = pass_prelaunch(ps, s, ev0, ev1, &next.seq)) return rc;
+      bool aborted = false;
+      if (int rc = wait_published(flag, cur, s, &aborted)) return rc;
+      if (!aborted) {
+        read_moments(ps, m);
+        return ICPNN_OK;
+      }
+      if (attempt == 3) return fail(ICPNN_ERR_CUDA, "icp_align: pass timed out waiting for its transform");
+      if (!more)
+        if (int rc = pass_prelaunch(ps, s, nullptr, nullptr, &next.seq)) return rc;
+      float R32[9], t32[3];
+      transform_to_f32(T, R32, t32);
+      pass_command(ps, next.seq, R32, t32);
+      cur = next.seq;
+      next.seq = 0;
+      ev0 = ev1 = nullptr;
+    }
+  };
+
   double mse_hist[3] = {0, 0, 0};
   int32_t done = 0;
   for (int32_t k = 0; k < max_iter; ++k) {
     float R32[9], t32[3];
     transform_to_f32(T, R32, t32);
     icpnn_moments m;
-    const bool time_it = k < timed;
-    if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, time_it ? ev[2 * k] : nullptr,
-                          time_it ? ev[2 * k + 1] : nullptr, &m))
-      return rc;
+    if (prelaunch) {
+      const bool time_next = k + 1 < timed;
+      if (int rc = collect(true, time_next ? ev[2 * k + 2] : nullptr, time_next ? ev[2 * k + 3] : nullptr, &m))
+        return rc;
+    } else {
+      const bool time_it = k < timed;
+      if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, time_it ? ev[2 * k] : nullptr,
+                            time_it ? ev[2 * k + 1] : nullptr, &m))
+        return rc;
+    }
     if (m.n_nonfinite > 0)
       return fail(ICPNN_ERR_NONFINITE, "icp_align: " + std::to_string(m.n_nonfinite) +
                                            " source points have non-finite coordinates");
@@ -821,6 +938,13 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     mse_hist[1] = mse_hist[2];
     mse_hist[2] = m.mse;
     done = k + 1;
+    if (prelaunch) {
+      // the queued pass evaluates T_{k+1}: the next iteration's pass or the final one
+      transform_to_f32(T, R32, t32);
+      pass_command(ps, next.seq, R32, t32);
+      cur = next.seq;
+      next.seq = 0;
+    }
     if (k >= 2 && std::fabs(mse_hist[1] - mse_hist[2]) < eps && std::fabs(mse_hist[0] - mse_hist[1]) < eps)
       break;
   }
@@ -832,7 +956,11 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   float R32[9], t32[3];
   transform_to_f32(T, R32, t32);
   icpnn_moments fin;
-  if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, &fin)) return rc;
+  if (prelaunch) {
+    if (int rc = collect(false, nullptr, nullptr, &fin)) return rc;
+  } else {
+    if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, &fin)) return rc;
+  }
   std::memcpy(out_T, T, sizeof(T));
   *final_mse = fin.mse;
   *iters = done;
@@ -883,6 +1011,37 @@ int icpnn_voxel_downsample(const float* xyz, int64_t n, float voxel_size, float*
     }
   }
   *out_n = count;
+  return ICPNN_OK;
+}
+
+int icpnn_probe_command_wait(const icpnn_tree* t, const float* src, int64_t n, uint64_t wait_ns, int32_t mode,
+                             int32_t* outcome, void* stream) {
+  clear_error();
+  if (int rc = check_tree_on_device(t)) return rc;
+  if (!src || !outcome) return fail(ICPNN_ERR_INVALID_ARG, "probe_command_wait: NULL pointer");
+  *outcome = -1;
+  if (n < 1 || n > INT32_MAX) return fail(ICPNN_ERR_INVALID_ARG, "probe_command_wait: n out of range");
+  if (wait_ns < 1 || wait_ns > 1000000000ull)
+    return fail(ICPNN_ERR_INVALID_ARG, "probe_command_wait: wait_ns must be in [1, 1e9]");
+  if (mode < 0 || mode > 2) return fail(ICPNN_ERR_INVALID_ARG, "probe_command_wait: mode must be 0, 1 or 2");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Scratch sc(s);
+  Pass ps;
+  if (int rc = pass_setup(t, src, n, INFINITY, false, false, s, sc, &ps)) return rc;
+  IcpPassParams p = pass_params(ps);
+  p.cmd = command_block(ps.mb, true);
+  p.mirror = ps.mirror;
+  p.wait_ns = wait_ns;
+  ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev, nullptr,
+                             nullptr, nullptr, nullptr, ps.grid, s));
+  if (mode == 1) pass_command(ps, p.seq, nullptr, nullptr);
+  if (mode == 2) {
+    const float R[9] = {1, 0, 0, 0, 1, 0, 0, 0, 1}, tr[3] = {0, 0, 0};
+    pass_command(ps, p.seq, R, tr);
+  }
+  ICPNN_CUDA(cudaStreamSynchronize(s));
+  const unsigned long long w = *reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
+  *outcome = w == p.seq ? 2 : w == (p.seq | kPassAborted) ? 1 : 0;
   return ICPNN_OK;
 }
 

@@ -62,9 +62,13 @@ extern "C" int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames,
   for (int32_t f = 0; f < n_frames; ++f)
     if (srcs[f] == nullptr || n_src[f] < 1 || n_src[f] > INT32_MAX)
       return fail(ICPNN_ERR_INVALID_ARG, "icp_align_batch: bad source " + std::to_string(f));
-  if (flags & ~ICPNN_RESIDUAL_REJECT) return fail(ICPNN_ERR_INVALID_ARG, "icp_align_batch: unknown flag");
+  if (flags & ~(ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_align_batch: unknown flag");
   if (max_concurrent <= 0) max_concurrent = 4;
   const int workers = std::min<int32_t>(max_concurrent, n_frames);
+  // With several frames in flight a pass queued ahead of its transform would
+  // hold SM slots that other frames' passes can use: launch after the solve.
+  const uint32_t frame_flags = flags | (workers > 1 ? ICPNN_NO_PRELAUNCH : 0u);
   const int dev = target->dev.device;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != dev)
@@ -105,7 +109,7 @@ extern "C" int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames,
           r = icpnn_icp_align(target, srcs[f], n_src[f], max_iter, eps, max_corr_dist,
                               init_T ? init_T + 16 * static_cast<int64_t>(f) : nullptr,
                               out_T + 16 * static_cast<int64_t>(f), final_mse + f, iters + f, nullptr, 0,
-                              flags, ws);
+                              frame_flags, ws);
         status[f] = r;
         if (r != ICPNN_OK) sh.msg[static_cast<size_t>(f)] = rc != ICPNN_OK ? setup_msg : icpnn_last_error();
       }

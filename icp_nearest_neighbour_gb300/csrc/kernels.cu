@@ -798,11 +798,19 @@ __device__ __forceinline__ float float_threshold_dev(double limit) {
 // With thr_out, the last block also stores the 3-sigma threshold of the
 // residual rejection from this reduction's c1 (pairs) and acc[15] (sum of e2):
 // float_threshold(9 * sum_e2 / pairs), 0 pairs giving sigma^2 = 0.
+//
+// `skipped` (block-uniform) is this block's outcome when the pass waited for a
+// command: 0 ran, kSkipStopped found the stop bit or a later seq, kSkipTimedOut
+// found no command in time.  counter[1] collects them; the last block
+// publishes the result only if every block ran.
+constexpr unsigned int kSkipStopped = 1u, kSkipTimedOut = 1u << 16;
+
 template <bool kPublish>
 __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
                                                double* __restrict__ partials,
                                                unsigned int* __restrict__ counter, double* out,
-                                               unsigned long long seq, float* thr_out = nullptr) {
+                                               unsigned long long seq, float* thr_out = nullptr,
+                                               unsigned int skipped = 0u) {
   __shared__ double s_warp[kThreads / 32][kMomentSlots];
   __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
   __shared__ bool s_last;
@@ -821,12 +829,16 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = static_cast<double>(acc[v]);
   }
   __syncthreads();
+  // every thread of the block is past its search: a kernel launched as a
+  // programmatic dependent of this one may start once all blocks are here
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x < kMomentSlots) {
     double s = 0.0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
     partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
   }
+  if (threadIdx.x == 0 && skipped != 0u) atomicAdd(counter + 1, skipped);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
@@ -853,9 +865,17 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // orders its own stores, the sequence word: the host never sees the new
   // sequence before the values.
   if (threadIdx.x == 0) {
+    *counter = 0u;
+    const unsigned int skips = atomicExch(counter + 1, 0u);
+    if (skips != 0u) {
+      if (kPublish && skips >= kSkipTimedOut) {
+        __threadfence_system();
+        *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq | kPassAborted;
+      }
+      return;
+    }
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
-    *counter = 0u;
     if (thr_out != nullptr) {
       const double pairs = s_fin[0][1];
       const double sigma2 = pairs > 0.0 ? s_fin[0][17] / pairs : 0.0;
@@ -885,7 +905,17 @@ __device__ __forceinline__ void add_pair(float (&acc)[16], float sx, float sy, f
   acc[15] = __fadd_rn(acc[15], d2);
 }
 
-// p = R s + t, each row ((R_a0 s_x + R_a1 s_y) + R_a2 s_z) + t_a
+// p = R s + t, each row ((R_a0 s_x + R_a1 s_y) + R_a2 s_z) + t_a; rt holds R
+// (row-major) then t.
+__device__ __forceinline__ void transform_point(const float* rt, float sx, float sy, float sz,
+                                                float (&q)[3]) {
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    float v = __fadd_rn(__fmul_rn(rt[3 * a], sx), __fmul_rn(rt[3 * a + 1], sy));
+    v = __fadd_rn(v, __fmul_rn(rt[3 * a + 2], sz));
+    q[a] = __fadd_rn(v, rt[9 + a]);
+  }
+}
 __device__ __forceinline__ void transform_point(const IcpPassParams& p, float sx, float sy, float sz,
                                                 float (&q)[3]) {
 #pragma unroll
@@ -896,22 +926,142 @@ __device__ __forceinline__ void transform_point(const IcpPassParams& p, float sx
   }
 }
 
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Polls use relaxed loads (an acquire load would invalidate the SM's L1 on
+// every poll, under the feet of co-resident blocks); the poll that sees the
+// awaited word is followed by one acquire fence.
+__device__ __forceinline__ unsigned long long load_relaxed_sys(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long load_relaxed_gpu(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void store_release_gpu(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(a), "l"(v) : "memory");
+}
+
+// The 12 floats of a command (16-byte aligned) in three vector loads issued
+// together: one round trip instead of twelve.
+template <bool kSystem>
+__device__ __forceinline__ void load_rt(const float* a, float* rt) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    if (kSystem)
+      asm volatile("ld.relaxed.sys.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(rt[4 * k]), "=f"(rt[4 * k + 1]), "=f"(rt[4 * k + 2]), "=f"(rt[4 * k + 3])
+                   : "l"(a + 4 * k) : "memory");
+    else
+      asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(rt[4 * k]), "=f"(rt[4 * k + 1]), "=f"(rt[4 * k + 2]), "=f"(rt[4 * k + 3])
+                   : "l"(a + 4 * k) : "memory");
+  }
+}
+
+// One thread per block: wait until the host's command names pass `seq` (or
+// gives up on it) and copy its R and t to rt.  Returns 0 (run), kSkipStopped
+// or kSkipTimedOut.  The first block to arrive polls host memory, for at most
+// wait_ns of global time, and forwards the outcome through the device mirror;
+// the others wait on the mirror, for at most 2 * wait_ns.
+__device__ __forceinline__ unsigned int await_command(const IcpPassParams& p, float* rt) {
+  constexpr unsigned long long kRun = 0, kStop = 1, kTimeout = 2;
+  const unsigned long long seq = p.seq, t0 = global_ns();
+  CommandMirror* m = p.mirror;
+  unsigned long long outcome = kTimeout;
+  if (atomicMax(&m->elect, seq) < seq) {
+    for (;;) {
+      const unsigned long long w = load_relaxed_sys(&p.cmd->word);
+      if ((w >> 1) == seq) {
+        outcome = (w & 1ull) ? kStop : kRun;
+        if (outcome == kRun) {
+          asm volatile("fence.acq_rel.sys;" ::: "memory");
+          float v[12];
+          load_rt<true>(p.cmd->rt, v);
+#pragma unroll
+          for (int k = 0; k < 12; ++k) {
+            rt[k] = v[k];
+            m->rt[k] = v[k];
+          }
+        }
+        break;
+      }
+      if ((w >> 1) > seq) {
+        outcome = kStop;
+        break;
+      }
+      if (global_ns() - t0 > p.wait_ns) break;
+      __nanosleep(200);
+    }
+    store_release_gpu(&m->word, (seq << 2) | outcome);
+  } else {
+    for (;;) {
+      const unsigned long long w = load_relaxed_gpu(&m->word);
+      if ((w >> 2) >= seq) {
+        outcome = (w >> 2) == seq ? (w & 3ull) : kStop;
+        if (outcome == kRun) {
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          float v[12];
+          load_rt<false>(m->rt, v);
+#pragma unroll
+          for (int k = 0; k < 12; ++k) rt[k] = v[k];
+        }
+        break;
+      }
+      if (global_ns() - t0 > 2 * p.wait_ns) break;
+      __nanosleep(100);
+    }
+  }
+  return outcome == kRun ? 0u : outcome == kStop ? kSkipStopped : kSkipTimedOut;
+}
+
+// Three resident blocks per SM: without the bound the command wait makes
+// the register allocator settle on 64 registers and spill.
 template <bool kPerPoint, bool kSlot>
-__global__ void __launch_bounds__(kThreads) icp_pass_kernel(
+__global__ void __launch_bounds__(kThreads, 3) icp_pass_kernel(
     const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
     int smem_slots, const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
     unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
     float* __restrict__ out_d2, int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of) {
   extern __shared__ uint2 s_nodes[];
-  stage_top(nodes, s_nodes, smem_slots);
+  __shared__ float s_rt[12];
+  __shared__ unsigned int s_skip;
+  if (p.cmd == nullptr) {
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int k = 0; k < 9; ++k) s_rt[k] = p.R[k];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) s_rt[9 + k] = p.t[k];
+      s_skip = 0u;
+    }
+  } else if (threadIdx.x == 0) {
+    s_skip = await_command(p, s_rt);
+  }
+  stage_top(nodes, s_nodes, smem_slots);  // ends with a block barrier
   const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+  const unsigned int skipped = s_skip;
+  const int64_t n_run = skipped == 0u ? n : 0;
+  // A pass launched as a programmatic dependent of the previous one may start
+  // during that pass's tail: everything above only reads the tree and the
+  // command; the warm-start hints, partials and counters below wait for the
+  // previous grid to complete (a no-op for an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   float acc[16];
 #pragma unroll
   for (int v = 0; v < 16; ++v) acc[v] = 0.f;
   uint32_t n_acc = 0, n_bad = 0;
 
-  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
+  for (int64_t c = first_chunk(); c * 32 < n_run; c += chunk_stride()) {
     const int64_t i = c * 32 + (threadIdx.x & 31);
     if (i >= n) continue;
     const float4 s = src[i];
@@ -922,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
       ++n_bad;
     } else {
       float q[3];
-      transform_point(p, s.x, s.y, s.z, q);
+      transform_point(s_rt, s.x, s.y, s.z, q);
       if (finite3(q[0], q[1], q[2])) {
         // Without per-point outputs only accepted pairs matter, so the search
         // starts with the rejection radius as its best distance (the page's
@@ -950,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads) icp_pass_kernel(
     }
     if (kSlot) slot_of[i] = matched;
   }
-  reduce_moments<true>(acc, n_acc, n_bad, partials, counter, out, p.seq);
+  reduce_moments<true>(acc, n_acc, n_bad, partials, counter, out, p.seq, nullptr, skipped);
 }
 
 // Residual pass of the section 4.4 rejection: for every source record with a
@@ -1087,25 +1237,29 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             double* out, int32_t* idx, float* dist2, int32_t* slot_of,
                             uint32_t* leaf_of, int grid, cudaStream_t s) {
   const int slots = smem_slots_for(t);
-  const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
   const float4* boxes = reinterpret_cast<const float4*>(t.dev.boxes);
   const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
   const bool per_point = idx != nullptr || dist2 != nullptr;
-  if (per_point && slot_of != nullptr)
-    icp_pass_kernel<true, true><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
-                                                              counter, out, idx, dist2, slot_of, leaf_of);
-  else if (per_point)
-    icp_pass_kernel<true, false><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
-                                                               counter, out, idx, dist2, nullptr, leaf_of);
-  else if (slot_of != nullptr)
-    icp_pass_kernel<false, true><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
-                                                               counter, out, nullptr, nullptr, slot_of, leaf_of);
-  else
-    icp_pass_kernel<false, false><<<grid, kThreads, smem, s>>>(nodes, boxes, pts, slots, src, n, p, partials,
-                                                                counter, out, nullptr, nullptr, nullptr, leaf_of);
+  auto kernel = per_point ? (slot_of != nullptr ? icp_pass_kernel<true, true> : icp_pass_kernel<true, false>)
+                          : (slot_of != nullptr ? icp_pass_kernel<false, true> : icp_pass_kernel<false, false>);
+  // A pass that waits for its command is launched as a programmatic
+  // dependent: its blocks may become resident once every block of the
+  // previous kernel on the stream has finished its search.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(slots) * sizeof(uint2);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.cmd != nullptr ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, nodes, boxes, pts, slots, src, n, p, partials, counter,
+                                           out, idx, dist2, slot_of, leaf_of);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,

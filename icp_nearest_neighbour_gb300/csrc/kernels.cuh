@@ -19,6 +19,24 @@ constexpr int kSmemSlots = 4096;
 //   [8..16] sum (s - c_s)_a (q - c_q)_b at 8 + 3a + b, [17] sum d2.
 constexpr int kMomentSlots = 18;
 
+// Command block of a pass launched before its transform is known (host-mapped,
+// written by the host): rt = R (row-major) then t; word = (seq << 1) | stop,
+// stored last with release semantics.
+struct alignas(16) PassCommand {
+  float rt[12];
+  unsigned long long word;
+};
+
+// Device copy of a command (zeroed before a registration's first pass): the
+// first block of a pass to arrive (elect) alone polls the host's command and
+// forwards it here as word = (seq << 2) | outcome, with rt; the other blocks
+// poll this word in L2 instead of host memory.
+struct alignas(16) CommandMirror {
+  unsigned long long elect;
+  unsigned long long word;
+  float rt[12];  // at byte 16: read with 16-byte vector loads
+};
+
 struct IcpPassParams {
   float R[9];
   float t[3];
@@ -26,7 +44,18 @@ struct IcpPassParams {
   float shift_q[3];   // c_q
   float max_d2;       // accept iff d2 <= max_d2 (float threshold equivalent to the double test)
   unsigned long long seq;  // published after the result, see launch_icp_pass
+  // Non-null: R and t above are ignored; every block first waits, for at
+  // most wait_ns of global time, until cmd->word names this pass's seq and
+  // takes R and t from cmd->rt.  A block that finds the stop bit, a later
+  // seq, or no command in time does no work; the pass then publishes nothing
+  // (stop, later seq) or, if any block ran out of time, seq | kPassAborted.
+  const PassCommand* cmd;
+  CommandMirror* mirror;
+  unsigned long long wait_ns;
 };
+
+constexpr unsigned long long kPassAborted = 1ull << 63;
+constexpr unsigned long long kCommandWaitNs = 50ull * 1000 * 1000;
 
 // Bounding box of n points as order-preserving int encodings
 // (lo x, lo y, lo z, hi x, hi y, hi z); non-finite points are skipped.
@@ -57,7 +86,7 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
                       float* dist2, cudaStream_t s);
 
 // One fused ICP pass: transform, search, reject, reduce.  `partials` holds
-// grid * kMomentSlots doubles, `counter` one zeroed word (left zeroed), `out`
+// grid * kMomentSlots doubles, `counter` two zeroed words (left zeroed), `out`
 // kMomentSlots doubles followed by one 64-bit word (may be host-mapped): once
 // the result is complete and visible system-wide the kernel stores p.seq in
 // that word, so the host can poll it instead of synchronising the stream.

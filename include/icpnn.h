@@ -74,6 +74,8 @@ typedef enum icpnn_status {
 #define ICPNN_TRACE_TIMING 2u     /* fill icpnn_iter_record.kernel_ms (CUDA events) */
 #define ICPNN_RESIDUAL_REJECT 4u  /* page section 4.4: after each solve drop pairs whose
                                      residual exceeds 3 sigma and solve again */
+#define ICPNN_NO_PRELAUNCH 16u    /* launch each pass only once its transform is solved
+                                     (see icpnn_icp_align) */
 
 typedef struct icpnn_tree icpnn_tree; /* opaque; owned by the library */
 
@@ -250,6 +252,11 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   kept pairs (DEGENERATE if fewer than 3 remain).  The stopping rule still
  *   uses mse_k of the correspondence pass.
  *   Then one more pass (no solve) under the returned transform.
+ *   Pass launches: without ICPNN_RESIDUAL_REJECT or ICPNN_NO_PRELAUNCH each
+ *   pass is queued on `stream` while the previous one runs; its blocks wait
+ *   on the GPU (at most 50 ms, then the pass is re-issued) for the transform
+ *   the host writes to pinned memory after the solve, so the launch latency
+ *   overlaps the previous pass.  Results are bit-identical either way.
  *   src          n_src x 3 float32 (device, or host: copied in once).
  *   max_iter     >= 1.  eps >= 0 (0: run max_iter iterations).
  *   out_T        host double[16]: the last solved transform (target ~ T src).
@@ -257,7 +264,8 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   iters        host: number of solves performed.
  *   trace        optional host array of trace_cap records (one per
  *                iteration, up to trace_cap).
- *   flags        ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT, or 0.
+ *   flags        ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT |
+ *                ICPNN_NO_PRELAUNCH, or 0.
  * Synchronises `stream` once per iteration; scratch comes from the
  * stream-ordered allocator and is returned before the call ends.
  * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY, NONFINITE, DEGENERATE. */
@@ -279,7 +287,9 @@ int icpnn_icp_align(const icpnn_tree* target, const float* src, int64_t n_src, i
  *   out_T, final_mse, iters, status   per-frame outputs (host arrays of
  *                 16*n_frames, n_frames, n_frames, n_frames); status[f] is
  *                 frame f's icpnn_status.
- *   flags         ICPNN_RESIDUAL_REJECT or 0.
+ *   flags         ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH, or 0; with more
+ *                 than one frame in flight passes are never pre-launched
+ *                 (a waiting pass would hold SM slots other frames can use).
  *   stream        the frames start after work already enqueued on it; all
  *                 their work is complete when the call returns.
  * Returns ICPNN_OK if every frame succeeded, else the first failing frame's

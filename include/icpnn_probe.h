@@ -1,4 +1,4 @@
-/* icpnn_probe.h -- measurement helper of libicpnn; not part of the
+/* icpnn_probe.h -- measurement and test helpers of libicpnn; not part of the
  * registration path and not described by the pages.
  *
  * icpnn_probe_l2_read -- read a device buffer `repeats` times in one launch
@@ -12,6 +12,17 @@
  *   stream   cudaStream_t (NULL = legacy default stream); not synchronised.
  * Time it with events on `stream`; bytes read = bytes * repeats.
  * Errors: INVALID_ARG, CUDA. */
+/* icpnn_probe_command_wait -- exercise the bounded wait of a pass launched
+ * before its transform is known (the pre-launched passes of icpnn_icp_align):
+ * launch one fused pass over src (n x 3 float32, device or host) against the
+ * uploaded tree whose blocks wait at most wait_ns (1 .. 1e9) for their
+ * command, then, by mode:
+ *   0  write no command: every block gives up after wait_ns;
+ *   1  write the stop command: the blocks return without work;
+ *   2  write the identity transform: the pass runs normally;
+ * synchronise `stream`, and report what the pass published in *outcome:
+ * 0 nothing, 1 the abort marker, 2 its result.  Expected: 1, 0, 2.
+ * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY. */
 #ifndef ICPNN_PROBE_H
 #define ICPNN_PROBE_H
 
@@ -22,6 +33,10 @@ extern "C" {
 #endif
 
 int icpnn_probe_l2_read(const void* buf, int64_t bytes, int32_t repeats, uint32_t* sink, void* stream);
+
+struct icpnn_tree;
+int icpnn_probe_command_wait(const struct icpnn_tree* tree, const float* src, int64_t n, uint64_t wait_ns,
+                             int32_t mode, int32_t* outcome, void* stream);
 
 #ifdef __cplusplus
 }

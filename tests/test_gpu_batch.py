@@ -31,10 +31,11 @@ def setup():
 def test_batch_equals_single_frames(setup, residual):
     nn, c, tree, srcs, dsrcs = setup
     dmax = c.max_corr_dist[0]
-    single = [nn.icp_align(tree, s, c.max_iter, c.eps, dmax, residual_reject=residual) for s in dsrcs]
-    for mc in (1, 3, 8):
+    single = [nn.icp_align(tree, s, c.max_iter, c.eps, dmax, residual_reject=residual, prelaunch=False)
+              for s in dsrcs]
+    for mc, pre in ((1, True), (3, True), (8, True), (3, False)):
         b = nn.icp_align_batch(tree, dsrcs, c.max_iter, c.eps, dmax, residual_reject=residual,
-                               max_concurrent=mc)
+                               max_concurrent=mc, prelaunch=pre)
         for f, ref in enumerate(single):
             assert b["status"][f] == 0
             np.testing.assert_array_equal(b["T"][f], ref["T"])

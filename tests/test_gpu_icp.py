@@ -232,6 +232,58 @@ def test_align_is_deterministic(nn):
     assert [r["mse"] for r in a["trace"]] == [r["mse"] for r in b["trace"]]
 
 
+@pytest.mark.parametrize("name", ["tiny", "scene", "lidar"])
+def test_prelaunched_passes_match_plain_launches(nn, name):
+    """Queuing each pass before its transform is solved (the default) changes
+    when the kernels start, not what they compute: bit-identical transforms,
+    per-iteration records and final mse; also with timing and an initial
+    transform, and over several registrations on one stream."""
+    import torch
+    c = W.CASES[name]()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    src = dev(c.source)
+    dmax = c.max_corr_dist[0]
+    init = np.eye(4)
+    init[:3, 3] = [0.01, -0.02, 0.005]
+    for kw in ({}, {"timing": True}, {"init_T": init}):
+        a = nn.icp_align(t, src, c.max_iter, c.eps, dmax, trace=True, prelaunch=False, **kw)
+        b = nn.icp_align(t, src, c.max_iter, c.eps, dmax, trace=True, **kw)
+        np.testing.assert_array_equal(a["T"], b["T"])
+        assert a["iters"] == b["iters"] and a["final_mse"] == b["final_mse"]
+        for ra, rb in zip(a["trace"], b["trace"]):
+            assert (ra["mse"], ra["n_accepted"]) == (rb["mse"], rb["n_accepted"])
+            np.testing.assert_array_equal(ra["T"], rb["T"])
+        if kw.get("timing"):
+            assert all(r["kernel_ms"] > 0 for r in b["trace"])
+    s = torch.cuda.Stream()
+    outs = [nn.icp_align(t, src, 8, 0.0, dmax, stream=s) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o["T"], outs[0]["T"])
+
+
+def test_pass_command_wait_is_bounded(nn):
+    """A pre-launched pass whose command never comes gives up after its wait
+    limit and publishes the abort marker; the stop command makes it return
+    without a result; the identity command makes it run.  The context stays
+    usable throughout."""
+    c = W.scene_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    src = dev(c.source)
+    assert nn.probe_command_wait(t, src, 2_000_000, 0) == 1
+    assert nn.probe_command_wait(t, src, 2_000_000, 1) == 0
+    assert nn.probe_command_wait(t, src, 2_000_000, 2) == 2
+    assert nn.probe_command_wait(t, c.source[:1000], 2_000_000, 0) == 1   # host source, one block
+    for bad in ((0, 0), (2_000_000_000, 0), (1000, 3)):
+        with pytest.raises(nn.IcpnnError):
+            nn.probe_command_wait(t, src, *bad)
+    a = nn.icp_align(t, src, 10, 0.0, c.max_corr_dist[0], prelaunch=False)
+    b = nn.icp_align(t, src, 10, 0.0, c.max_corr_dist[0])
+    np.testing.assert_array_equal(a["T"], b["T"])
+
+
 def test_large_coarse_to_fine(nn, oracle_mod):
     """4M target / 2M source, two stages (2.0 m then 0.3 m).  The first pass of
     each stage is compared on a 20k-point source sample (the oracle's search is
@@ -276,9 +328,17 @@ def test_errors(nn):
     with pytest.raises(nn.IcpnnError) as e:
         nn.icp_align(t, dev(c.source), 5, -1.0, math.inf)
     assert e.value.status == "INVALID_ARG"
-    # a failed call leaves the library usable
+    # a failed call leaves the library usable, on its stream and on another
+    # (a pass queued ahead of the failure is stopped, not left waiting)
     res = nn.icp_align(t, dev(c.source), 5, 0.0, math.inf)
     assert res["iters"] == 5
+    import torch
+    s = torch.cuda.Stream()
+    with pytest.raises(nn.IcpnnError):
+        nn.icp_align(t, far, 5, 1e-6, 0.1, stream=s)
+    res2 = nn.icp_align(t, dev(c.source), 5, 0.0, math.inf)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(res2["T"], res["T"])
 
 
 def test_round_robin_tree_gives_the_same_registration(nn, oracle_mod):
