@@ -154,6 +154,9 @@ def run_ours(args):
     import workloads
 
     ws, rank, local = dist_env()
+    # --no-prelaunch: every pass an ordinary launch (bit-identical results),
+    # for profilers that serialise kernel launches
+    pre = not args.no_prelaunch
     if ws > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -192,8 +195,8 @@ def run_ours(args):
     def step(timing):
         # timing: per-pass CUDA events, which need ordinary launches (a
         # pre-launched pass starts before its events could bracket it)
-        return nn.icp_align(tree, src, case.max_iter, case.eps, dmax, timing=timing, prelaunch=not timing,
-                            stream=stream)
+        return nn.icp_align(tree, src, case.max_iter, case.eps, dmax, timing=timing,
+                            prelaunch=pre and not timing, stream=stream)
 
     for _ in range(args.warmup):
         step(False)
@@ -254,11 +257,12 @@ def run_ours(args):
     frame_dev = [torch.from_numpy(f).cuda() for f in frame_srcs]
     multi = {}
     for mc in (1, 4, 8):
-        nn.icp_align_batch(tree, frame_dev, case.max_iter, case.eps, dmax, max_concurrent=mc, stream=stream)
+        nn.icp_align_batch(tree, frame_dev, case.max_iter, case.eps, dmax, max_concurrent=mc, prelaunch=pre,
+                           stream=stream)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         b = nn.icp_align_batch(tree, frame_dev, case.max_iter, case.eps, dmax, max_concurrent=mc,
-                               stream=stream)
+                               prelaunch=pre, stream=stream)
         torch.cuda.synchronize()
         secs = time.perf_counter() - t0
         multi[f"frames_in_flight_{mc}"] = {"value": float(b["iters"].sum()) / secs, "unit": UNIT,
@@ -275,7 +279,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         ut = nn.kdtree_build_device(u_tgt, u.leaf_size, stream=stream)
-        nn.icp_align(ut, u_src, u.max_iter, u.eps, math.inf, stream=stream)
+        nn.icp_align(ut, u_src, u.max_iter, u.eps, math.inf, prelaunch=pre, stream=stream)
         torch.cuda.synchronize()
         if rep:
             u_ms.append((time.perf_counter() - t0) * 1e3)
@@ -288,7 +292,7 @@ def run_ours(args):
         for rule in (False, True):
             ct = nn.kdtree_build(cc.target, cc.leaf_size, round_robin=rule)
             nn.kdtree_upload(ct, stream=stream)
-            nn.icp_align(ct, csrc, cc.max_iter, cc.eps, cc.max_corr_dist[0], stream=stream)
+            nn.icp_align(ct, csrc, cc.max_iter, cc.eps, cc.max_corr_dist[0], prelaunch=pre, stream=stream)
             r = nn.icp_align(ct, csrc, cc.max_iter, cc.eps, cc.max_corr_dist[0], timing=True,
                              prelaunch=False, stream=stream)
             row["round_robin_pass_us" if rule else "max_variance_pass_us"] = \
@@ -324,7 +328,7 @@ def run_ours(args):
     e0 = time.perf_counter()
     for _ in range(args.steps):
         t_e = nn.kdtree_build_device(pinned_tgt, case.leaf_size, stream=stream)
-        r = nn.icp_align(t_e, pinned_src, case.max_iter, case.eps, dmax, stream=stream)
+        r = nn.icp_align(t_e, pinned_src, case.max_iter, case.eps, dmax, prelaunch=pre, stream=stream)
         e2e_iters += r["iters"]
         h2d += n_t * 12 + n * 12
         d2h += 24 + (r["iters"] + 1) * 18 * 8
@@ -338,7 +342,7 @@ def run_ours(args):
     for _ in range(args.steps):
         t_h = nn.kdtree_build(case.target, case.leaf_size)
         nn.kdtree_upload(t_h, stream=stream)
-        r = nn.icp_align(t_h, pinned_src, case.max_iter, case.eps, dmax, stream=stream)
+        r = nn.icp_align(t_h, pinned_src, case.max_iter, case.eps, dmax, prelaunch=pre, stream=stream)
         host_e2e_iters += r["iters"]
         t_h.free()
     torch.cuda.synchronize()
@@ -371,6 +375,8 @@ def run_ours(args):
             "iters_per_step": iters // args.steps, "passes_per_step": passes // args.steps,
             "l2": "flushed between steps (write of 2x L2 size); the tree stays L2-resident within a step",
             "parallelism": f"replicas x{ws}",
+            "pass_launch": "pre-launched (programmatic dependent, waits for its transform)" if pre
+                           else "ordinary (after the solve)",
         },
         "nn_queries_per_s": passes_all * n / t_max,
         "roofline": {
@@ -529,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--cpu-iters", type=int, default=50, help="oracle iterations in cpu_baseline")
     ap.add_argument("--ref-iters", type=int, default=8, help="oracle iterations per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prelaunch", action="store_true",
+                    help="launch every ICP pass after its solve (for profilers that serialise launches)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

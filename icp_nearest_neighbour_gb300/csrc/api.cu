@@ -827,7 +827,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   const bool residual = (flags & ICPNN_RESIDUAL_REJECT) != 0;
   // the residual passes run between a pass and the next one's transform, so
   // the next pass cannot be queued ahead of them
-  const bool prelaunch = !residual && (flags & ICPNN_NO_PRELAUNCH) == 0;
+  bool prelaunch = !residual && (flags & ICPNN_NO_PRELAUNCH) == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   double T[16];
@@ -855,31 +855,30 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     transform_to_f32(T, R32, t32);
     pass_command(ps, cur, R32, t32);
   }
-  // Result of pass `cur` (already commanded with transform T); a pass whose
-  // blocks gave up waiting is evaluated again by `next` under the same
-  // transform.  Queues a successor when `more` is set.
+  // Result of pass `cur` (already commanded with transform T); queues a
+  // successor first when `more` is set.  A pass whose blocks gave up waiting
+  // for their transform (a profiler or debugger that serialises launches, a
+  // host thread descheduled for the whole wait) is evaluated again by an
+  // ordinary launch, and the registration continues with ordinary launches.
   auto collect = [&](bool more, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m) -> int {
+    if (more)
+      if (int rc = pass_prelaunch(ps, s, ev0, ev1, &next.seq)) return rc;
     const volatile unsigned long long* flag =
         reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-    for (int attempt = 0;; ++attempt) {
-      if (more)
-        if (int rc = pass_prelaunch(ps, s, ev0, ev1, &next.seq)) return rc;
-      bool aborted = false;
-      if (int rc = wait_published(flag, cur, s, &aborted)) return rc;
-      if (!aborted) {
-        read_moments(ps, m);
-        return ICPNN_OK;
-      }
-      if (attempt == 3) return fail(ICPNN_ERR_CUDA, "icp_align: pass timed out waiting for its transform");
-      if (!more)
-        if (int rc = pass_prelaunch(ps, s, nullptr, nullptr, &next.seq)) return rc;
-      float R32[9], t32[3];
-      transform_to_f32(T, R32, t32);
-      pass_command(ps, next.seq, R32, t32);
-      cur = next.seq;
-      next.seq = 0;
-      ev0 = ev1 = nullptr;
+    bool aborted = false;
+    if (int rc = wait_published(flag, cur, s, &aborted)) return rc;
+    if (!aborted) {
+      read_moments(ps, m);
+      return ICPNN_OK;
     }
+    if (next.seq != 0) {
+      pass_command(ps, next.seq, nullptr, nullptr);
+      next.seq = 0;
+    }
+    prelaunch = false;
+    float R32[9], t32[3];
+    transform_to_f32(T, R32, t32);
+    return pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, m);
   };
 
   double mse_hist[3] = {0, 0, 0};

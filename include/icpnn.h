@@ -254,9 +254,12 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   Then one more pass (no solve) under the returned transform.
  *   Pass launches: without ICPNN_RESIDUAL_REJECT or ICPNN_NO_PRELAUNCH each
  *   pass is queued on `stream` while the previous one runs; its blocks wait
- *   on the GPU (at most 50 ms, then the pass is re-issued) for the transform
- *   the host writes to pinned memory after the solve, so the launch latency
- *   overlaps the previous pass.  Results are bit-identical either way.
+ *   on the GPU for the transform the host writes to pinned memory after the
+ *   solve, so the launch latency overlaps the previous pass.  The wait is
+ *   bounded (50 ms): a pass that runs out (a profiler that serialises
+ *   launches, a host thread descheduled that long) is run again as an
+ *   ordinary launch and so is the rest of the registration.  Results are
+ *   bit-identical either way.
  *   src          n_src x 3 float32 (device, or host: copied in once).
  *   max_iter     >= 1.  eps >= 0 (0: run max_iter iterations).
  *   out_T        host double[16]: the last solved transform (target ~ T src).
