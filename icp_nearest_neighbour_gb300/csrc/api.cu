@@ -301,8 +301,9 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
   if (int rc = prepare_source(src, n, true, true, s, sc, &ps->src)) return rc;
   ps->grid = icp_pass_grid(*t, n);
   ICPNN_CUDA(sc.alloc(&ps->partials, static_cast<int64_t>(ps->grid) * kMomentSlots));
-  ICPNN_CUDA(sc.alloc(&ps->counter, 2));
-  ICPNN_CUDA(cudaMemsetAsync(ps->counter, 0, 2 * sizeof(uint32_t), s));
+  const int64_t counter_words = reduction_counter_words(ps->grid);
+  ICPNN_CUDA(sc.alloc(&ps->counter, counter_words));
+  ICPNN_CUDA(cudaMemsetAsync(ps->counter, 0, static_cast<size_t>(counter_words) * sizeof(uint32_t), s));
   ICPNN_CUDA(sc.alloc(&ps->mirror, 1));
   ICPNN_CUDA(cudaMemsetAsync(ps->mirror, 0, sizeof(CommandMirror), s));
   if (int rc = mapped_buffer(&ps->mb)) return rc;
@@ -772,9 +773,9 @@ int icpnn_icp_step_noalloc(const icpnn_tree* t, const float* src, int64_t n, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   double* scratch = nullptr;
   ICPNN_CUDA(noalloc_scratch(&scratch));
-  // the finished-block counter must start at zero; the other words are
+  // the reduction's counters must start at zero; the other words are
   // written before they are read within this call
-  ICPNN_CUDA(cudaMemsetAsync(scratch + noalloc_counter_offset(), 0, sizeof(double), s));
+  ICPNN_CUDA(cudaMemsetAsync(scratch + noalloc_counter_offset(), 0, kNoAllocCounterDoubles * sizeof(double), s));
   int32_t* bbox6 = reinterpret_cast<int32_t*>(scratch + noalloc_bbox_offset());
   ICPNN_CUDA(launch_bbox(src, n, bbox6, s));
   int32_t h6[6];

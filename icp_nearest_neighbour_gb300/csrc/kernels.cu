@@ -803,7 +803,18 @@ __device__ __forceinline__ float float_threshold_dev(double limit) {
 // command: 0 ran, kSkipStopped found the stop bit or a later seq, kSkipTimedOut
 // found no command in time.  counter[1] collects them; the last block
 // publishes the result only if every block ran.
+//
+// Grids of more than kSingleLevelBlocks blocks reduce in two fixed-order
+// levels: the last block to finish of each group of kGroupBlocks consecutive
+// blocks (counter[2 + group]) adds the group's partials in block order, one
+// load per thread, and stores the sum over the group's first partial; the
+// last group to finish (counter[0]) adds the group sums in a fixed order.
+// (One level over a 391-block grid, the last block adding every partial, put
+// ~28 L2 loads per thread on the critical path: 4.2 us.)  Smaller grids keep
+// one level: the last block (counter[0]) adds at most four rows per thread.
 constexpr unsigned int kSkipStopped = 1u, kSkipTimedOut = 1u << 16;
+constexpr unsigned int kSingleLevelBlocks = 4 * kGroupBlocks;
+static_assert(kGroupBlocks * kMomentSlots <= kThreads, "one thread per partial of a group");
 
 template <bool kPublish>
 __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
@@ -841,17 +852,52 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   if (threadIdx.x == 0 && skipped != 0u) atomicAdd(counter + 1, skipped);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
+  const int r = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
+  // rows of partials the final block adds: every block's (one level) or every
+  // group's sum, stored over the group's first partial (two levels)
+  unsigned int rows = gridDim.x, row_stride = 1;
+  if (gridDim.x > kSingleLevelBlocks) {
+    const unsigned int group = blockIdx.x / kGroupBlocks, g0 = group * kGroupBlocks;
+    const unsigned int in_group = min(static_cast<unsigned int>(kGroupBlocks), gridDim.x - g0);
+    if (threadIdx.x == 0) s_last = (atomicAdd(counter + 2 + group, 1u) == in_group - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x < kGroupBlocks * kMomentSlots)
+      s_fin[r][v] = static_cast<unsigned int>(r) < in_group
+                        ? __ldcg(&partials[static_cast<int64_t>(g0 + r) * kMomentSlots + v]) : 0.0;
+    __syncthreads();
+    if (threadIdx.x < kMomentSlots) {
+      double s = 0.0;
+      for (unsigned int k = 0; k < in_group; ++k) s += s_fin[k][threadIdx.x];
+      partials[static_cast<int64_t>(g0) * kMomentSlots + threadIdx.x] = s;
+    }
+    if (threadIdx.x == 0) counter[2 + group] = 0u;
+    __threadfence();
+    __syncthreads();
+    rows = (gridDim.x + kGroupBlocks - 1) / kGroupBlocks;
+    row_stride = kGroupBlocks;
+  }
+  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == rows - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   constexpr int kGroups = kThreads / kMomentSlots;
   if (threadIdx.x < kGroups * kMomentSlots) {
-    const int g = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
+    // rows r, r + 14, ... in order, up to four loads in flight
     double s = 0.0;
-    for (int b = g; b < static_cast<int>(gridDim.x); b += kGroups)
-      s += __ldcg(&partials[static_cast<int64_t>(b) * kMomentSlots + v]);
-    s_fin[g][v] = s;
+    for (unsigned int j = r; j < rows; j += 4 * kGroups) {
+      double x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const unsigned int row = j + u * kGroups;
+        x[u] = row < rows ? __ldcg(&partials[static_cast<int64_t>(row) * row_stride * kMomentSlots + v]) : 0.0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j + u * kGroups < rows) s += x[u];
+    }
+    s_fin[r][v] = s;
   }
   __syncthreads();
   if (threadIdx.x < kMomentSlots) {
@@ -1361,11 +1407,11 @@ int voxel_downsample(const float* xyz, int64_t n, float v, float* out, int64_t* 
 // Layout of g_noalloc_scratch, in doubles:
 //   [0, kNoAllocMaxBlocks * kMomentSlots)   partial moments of each block
 //   [kNoAllocResult, + kMomentSlots)         the reduced result
-//   [kNoAllocCounter]                        low 32 bits: finished-block counter
+//   [kNoAllocCounter, + kNoAllocCounterDoubles)  the reduction's counter words
 //   [kNoAllocBbox, + 3)                      six int32 bounding-box words
 constexpr int64_t kNoAllocResult = static_cast<int64_t>(kNoAllocMaxBlocks) * kMomentSlots;
 constexpr int64_t kNoAllocCounter = kNoAllocResult + kMomentSlots;
-constexpr int64_t kNoAllocBbox = kNoAllocCounter + 1;
+constexpr int64_t kNoAllocBbox = kNoAllocCounter + kNoAllocCounterDoubles;
 constexpr int64_t kNoAllocDoubles = kNoAllocBbox + 3;
 static_assert(static_cast<int64_t>(kNoAllocMaxBlocks) * 256 == ICPNN_NOALLOC_MAX_POINTS,
               "one thread per point, 256 threads per block");
@@ -1378,7 +1424,7 @@ static __device__ __align__(256) double g_noalloc_scratch[kNoAllocDoubles];
 namespace {
 
 template <bool kPerPoint>
-__global__ void __launch_bounds__(kThreads) icp_pass_inplace_kernel(
+__global__ void __launch_bounds__(kThreads, 3) icp_pass_inplace_kernel(
     const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
     int smem_slots, const float* __restrict__ xyz, int64_t n, IcpPassParams p, double* __restrict__ scratch,
     int32_t* __restrict__ out_idx, float* __restrict__ out_d2) {

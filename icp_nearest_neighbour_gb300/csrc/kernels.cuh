@@ -19,6 +19,13 @@ constexpr int kSmemSlots = 4096;
 //   [8..16] sum (s - c_s)_a (q - c_q)_b at 8 + 3a + b, [17] sum d2.
 constexpr int kMomentSlots = 18;
 
+// The moment reduction combines block partials in groups of kGroupBlocks
+// (one load per thread of a 256-thread block); its counter array holds
+// reduction_counter_words(grid) zeroed 32-bit words: [0] finished groups,
+// [1] skipped blocks, [2 + g] finished blocks of group g.
+constexpr int kGroupBlocks = 256 / kMomentSlots;
+constexpr int64_t reduction_counter_words(int64_t grid) { return 2 + (grid + kGroupBlocks - 1) / kGroupBlocks; }
+
 // Command block of a pass launched before its transform is known (host-mapped,
 // written by the host): rt = R (row-major) then t; word = (seq << 1) | stop,
 // stored last with release semantics.
@@ -86,7 +93,8 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
                       float* dist2, cudaStream_t s);
 
 // One fused ICP pass: transform, search, reject, reduce.  `partials` holds
-// grid * kMomentSlots doubles, `counter` two zeroed words (left zeroed), `out`
+// grid * kMomentSlots doubles, `counter` reduction_counter_words(grid) zeroed
+// words (left zeroed), `out`
 // kMomentSlots doubles followed by one 64-bit word (may be host-mapped): once
 // the result is complete and visible system-wide the kernel stores p.seq in
 // that word, so the host can poll it instead of synchronising the stream.
@@ -132,7 +140,8 @@ cudaError_t noalloc_scratch(double** out);
 // Scratch offsets (in doubles) of the result record and the bounding box.
 constexpr int64_t noalloc_result_offset() { return static_cast<int64_t>(kNoAllocMaxBlocks) * kMomentSlots; }
 constexpr int64_t noalloc_counter_offset() { return noalloc_result_offset() + kMomentSlots; }
-constexpr int64_t noalloc_bbox_offset() { return noalloc_counter_offset() + 1; }
+constexpr int64_t kNoAllocCounterDoubles = (reduction_counter_words(kNoAllocMaxBlocks) + 1) / 2;
+constexpr int64_t noalloc_bbox_offset() { return noalloc_counter_offset() + kNoAllocCounterDoubles; }
 cudaError_t launch_icp_pass_inplace(const icpnn_tree& t, const float* xyz, int64_t n,
                                     const IcpPassParams& p, double* scratch, int32_t* idx,
                                     float* dist2, cudaStream_t s);
