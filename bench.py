@@ -323,6 +323,10 @@ def run_ours(args):
     h2d = 0
     d2h = 0
     e2e_iters = 0
+    for _ in range(args.warmup):
+        t_e = nn.kdtree_build_device(pinned_tgt, case.leaf_size, stream=stream)
+        nn.icp_align(t_e, pinned_src, case.max_iter, case.eps, dmax, prelaunch=pre, stream=stream)
+        t_e.free()
     barrier()
     torch.cuda.synchronize()
     e0 = time.perf_counter()
@@ -337,6 +341,11 @@ def run_ours(args):
     e2e_s = time.perf_counter() - e0
     # the same with the page's host build and one upload of the tree
     host_e2e_iters = 0
+    for _ in range(args.warmup):
+        t_h = nn.kdtree_build(case.target, case.leaf_size)
+        nn.kdtree_upload(t_h, stream=stream)
+        nn.icp_align(t_h, pinned_src, case.max_iter, case.eps, dmax, prelaunch=pre, stream=stream)
+        t_h.free()
     torch.cuda.synchronize()
     e1 = time.perf_counter()
     for _ in range(args.steps):
