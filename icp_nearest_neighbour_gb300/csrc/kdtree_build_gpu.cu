@@ -48,6 +48,7 @@ constexpr int kBT = 256;          // threads per block of the level kernels
 constexpr int kChunk = 2048;      // list positions per block of a node
 constexpr int kBWarps = kBT / 32;
 constexpr int kWarpNode = 256;    // levels whose nodes hold at most this many points: one warp per node
+constexpr int kBlockNode = 4096;  // ... at most this many (and more than kWarpNode): one block per node
 
 // Range of heap node k at depth d under the median rule; false when the node
 // does not exist (an ancestor is a leaf).
@@ -573,6 +574,150 @@ __global__ void __launch_bounds__(256) level_warp_kernel(LevelArgs a, const floa
   }
 }
 
+// ----------------------------------------------- levels of medium nodes --
+
+// One block per node of a level whose nodes hold at most kBlockNode points:
+// the steps of the multi-block passes, with block barriers in place of
+// kernel boundaries and block reductions (warp butterflies, then the warps
+// in order) in place of the chunk partials.
+__global__ void __launch_bounds__(kBT) level_block_kernel(LevelArgs a, const float4* __restrict__ L0,
+                                                          const float4* __restrict__ L1,
+                                                          const float4* __restrict__ L2,
+                                                          float4* __restrict__ T0, float4* __restrict__ T1,
+                                                          float4* __restrict__ T2, uint8_t* __restrict__ left,
+                                                          Node* __restrict__ nodes, float4* __restrict__ boxes,
+                                                          float4* __restrict__ records) {
+  __shared__ double sh[kBWarps][9];
+  __shared__ double s_tot[9];
+  __shared__ uint32_t s_cnt[3][kBWarps];
+  const uint32_t k = (1u << a.d) + blockIdx.x;
+  int64_t lo, cnt;
+  if (!node_range(k, a.d, a.n, a.leaf, a.max_depth, &lo, &cnt)) return;
+  const int64_t hi = lo + cnt;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // sums and box; the minima are kept negated so that one max combines both
+  {
+    double v[9] = {0.0, 0.0, 0.0, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kBT) {
+      const float4 p = L0[i];
+      const float c3[3] = {p.x, p.y, p.z};
+#pragma unroll
+      for (int e = 0; e < 3; ++e) {
+        v[e] += static_cast<double>(c3[e]);
+        v[3 + e] = fmax(v[3 + e], -static_cast<double>(c3[e]));
+        v[6 + e] = fmax(v[6 + e], static_cast<double>(c3[e]));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 9; ++e) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const double o = __shfl_xor_sync(kFull, v[e], off);
+        v[e] = e < 3 ? v[e] + o : fmax(v[e], o);
+      }
+      if (lane == 0) sh[warp][e] = v[e];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 9) {
+    const int e = threadIdx.x;
+    double t = sh[0][e];
+    for (int w = 1; w < kBWarps; ++w) t = e < 3 ? t + sh[w][e] : fmax(t, sh[w][e]);
+    s_tot[e] = t;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    boxes[2 * k] = make_float4(static_cast<float>(-s_tot[3]), static_cast<float>(-s_tot[4]),
+                               static_cast<float>(-s_tot[5]), 0.f);
+    boxes[2 * k + 1] = make_float4(static_cast<float>(s_tot[6]), static_cast<float>(s_tot[7]),
+                                   static_cast<float>(s_tot[8]), 0.f);
+  }
+  if (is_leaf_node(cnt, a.d, a)) {
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kBT) records[i] = L0[i];
+    if (threadIdx.x == 0) {
+      nodes[k].a = static_cast<uint32_t>(lo);
+      nodes[k].meta = kLeafTag | (static_cast<uint32_t>(cnt) << 2);
+    }
+    return;
+  }
+  const double c = static_cast<double>(cnt);
+  int axis;
+  if (a.round_robin) {
+    axis = a.d % 3;
+  } else {
+    const double m0 = s_tot[0] / c, m1 = s_tot[1] / c, m2 = s_tot[2] / c;
+    double q[3] = {0.0, 0.0, 0.0};
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kBT) {
+      const float4 p = L0[i];
+      const double e0 = static_cast<double>(p.x) - m0;
+      const double e1 = static_cast<double>(p.y) - m1;
+      const double e2 = static_cast<double>(p.z) - m2;
+      q[0] += e0 * e0;
+      q[1] += e1 * e1;
+      q[2] += e2 * e2;
+    }
+    __syncthreads();  // s_tot and sh are reused below
+#pragma unroll
+    for (int e = 0; e < 3; ++e) {
+      q[e] = warp_sum(q[e]);
+      if (lane == 0) sh[warp][e] = q[e];
+    }
+    __syncthreads();
+    if (threadIdx.x < 3) {
+      double t = sh[0][threadIdx.x];
+      for (int w = 1; w < kBWarps; ++w) t += sh[w][threadIdx.x];
+      s_tot[threadIdx.x] = t / c;
+    }
+    __syncthreads();
+    axis = widest(s_tot[0], s_tot[1], s_tot[2]);
+  }
+  const float4* L = axis == 0 ? L0 : (axis == 1 ? L1 : L2);
+  const int64_t mid = lo + cnt / 2;
+  if (threadIdx.x == 0) {
+    nodes[k].a = __float_as_uint(coord(L[mid], axis));
+    nodes[k].meta = static_cast<uint32_t>(axis);
+  }
+  for (int64_t i = lo + threadIdx.x; i < hi; i += kBT) left[rec_id(L[i])] = i < mid ? 1 : 0;
+  __syncthreads();
+  // stable partition of the three lists, kBT positions per round
+  const float4* Ls[3] = {L0, L1, L2};
+  float4* Ts[3] = {T0, T1, T2};
+  int64_t nl[3] = {0, 0, 0}, nr[3] = {0, 0, 0};
+  for (int64_t base = lo; base < hi; base += kBT) {
+    const int64_t i = base + threadIdx.x;
+    const bool valid = i < hi;
+    const int64_t round_n = min(static_cast<int64_t>(kBT), hi - base);
+    float4 r[3];
+    uint32_t f[3], bal[3];
+#pragma unroll
+    for (int l = 0; l < 3; ++l) r[l] = valid ? Ls[l][i] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int l = 0; l < 3; ++l) {
+      f[l] = valid ? left[rec_id(r[l])] : 0u;
+      bal[l] = __ballot_sync(kFull, f[l] != 0u);
+      if (lane == 0) s_cnt[l][warp] = __popc(bal[l]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int l = 0; l < 3; ++l) {
+      uint32_t before = 0, round_left = 0;
+#pragma unroll
+      for (int w = 0; w < kBWarps; ++w) {
+        if (w < warp) before += s_cnt[l][w];
+        round_left += s_cnt[l][w];
+      }
+      if (valid) {
+        const int64_t rl = before + __popc(bal[l] & ((1u << lane) - 1u));
+        const int64_t rr = (i - base) - rl;
+        Ts[l][f[l] ? lo + nl[l] + rl : mid + nr[l] + rr] = r[l];
+      }
+      nl[l] += round_left;
+      nr[l] += round_n - round_left;
+    }
+    __syncthreads();  // s_cnt is rewritten by the next round
+  }
+}
+
 inline int grid_for(int64_t items) { return static_cast<int>(std::max<int64_t>(1, (items + 255) / 256)); }
 
 struct DeviceMem {
@@ -697,6 +842,10 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
       if (largest <= kWarpNode) {
         level_warp_kernel<<<warp_grid, 256, 0, s>>>(a, L[0], L[1], L[2], T[0], T[1], T[2], left, nodes, boxes,
                                                     records);
+        g_launch_count.fetch_add(1, std::memory_order_relaxed);
+      } else if (largest <= kBlockNode) {
+        level_block_kernel<<<static_cast<int>(int64_t{1} << d), kBT, 0, s>>>(a, L[0], L[1], L[2], T[0], T[1], T[2],
+                                                                            left, nodes, boxes, records);
         g_launch_count.fetch_add(1, std::memory_order_relaxed);
       } else {
         level_sums_kernel<<<blocks, kBT, 0, s>>>(a, L[0], part, node_count, mean, nodes, boxes);
