@@ -9,6 +9,7 @@
 #include <cfloat>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -23,21 +24,34 @@ namespace icpnn {
 // default the pool hands freed memory back to the driver at every
 // synchronisation, so the next call maps it again; keep up to 1 GiB of it
 // per device instead (a setting of this process's pool only).
-void keep_pool_memory() {
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s) {
   constexpr int kMaxDev = 64;
-  static std::atomic<bool> done[kMaxDev];
+  static std::once_flag once[kMaxDev];
+  static cudaMemPool_t pools[kMaxDev];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return;
-  if (done[dev].load(std::memory_order_acquire)) return;
-  cudaMemPool_t pool = nullptr;
-  if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaMallocAsync(p, bytes, s);
+  std::call_once(once[dev], [dev] {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
     uint64_t keep = uint64_t{1} << 30;
-    uint64_t cur = 0;
-    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &cur) == cudaSuccess && cur < keep)
-      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-  }
-  cudaGetLastError();
-  done[dev].store(true, std::memory_order_release);
+    int off = 0;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowOpportunistic, &off);
+    cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowInternalDependencies, &off);
+    cudaGetLastError();
+    pools[dev] = pool;
+  });
+  if (pools[dev] == nullptr) return cudaMallocAsync(p, bytes, s);  // no pool of our own: the device's default
+  return cudaMallocFromPoolAsync(p, bytes, pools[dev], s);
 }
 
 extern std::atomic<int64_t> g_launch_count;
@@ -78,7 +92,7 @@ bool is_device_pointer(const void* p) {
 // Device allocations from the stream-ordered pool, returned on the same stream.
 class Scratch {
  public:
-  explicit Scratch(cudaStream_t s) : s_(s) { keep_pool_memory(); }
+  explicit Scratch(cudaStream_t s) : s_(s) {}
   ~Scratch() {
     for (void* p : ptrs_) cudaFreeAsync(p, s_);
   }
@@ -86,7 +100,7 @@ class Scratch {
   cudaError_t alloc(T** out, int64_t count) {
     void* p = nullptr;
     const size_t bytes = static_cast<size_t>(std::max<int64_t>(count, 1)) * sizeof(T);
-    cudaError_t e = cudaMallocAsync(&p, bytes, s_);
+    cudaError_t e = pool_alloc(&p, bytes, s_);
     if (e != cudaSuccess) return e;
     ptrs_.push_back(p);
     *out = static_cast<T*>(p);
@@ -615,10 +629,9 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   const size_t nb = static_cast<size_t>(t->heap_slots) * sizeof(Node);
   const size_t bb = static_cast<size_t>(t->heap_slots) * 8 * sizeof(float);
   const size_t pb = static_cast<size_t>(t->n) * 4 * sizeof(float);
-  keep_pool_memory();
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&nodes), nb + bb, s);
+  cudaError_t e = pool_alloc(reinterpret_cast<void**>(&nodes), nb + bb, s);
   float* boxes = nodes ? reinterpret_cast<float*>(reinterpret_cast<char*>(nodes) + nb) : nullptr;
-  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&pts), pb, s);
+  if (e == cudaSuccess) e = pool_alloc(reinterpret_cast<void**>(&pts), pb, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(nodes, t->nodes.data(), nb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(boxes, t->boxes.data(), bb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pts, t->records.data(), pb, cudaMemcpyHostToDevice, s);

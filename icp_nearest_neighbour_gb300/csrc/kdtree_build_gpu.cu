@@ -723,14 +723,14 @@ inline int grid_for(int64_t items) { return static_cast<int>(std::max<int64_t>(1
 struct DeviceMem {
   std::vector<void*> ptrs;
   cudaStream_t s;
-  explicit DeviceMem(cudaStream_t st) : s(st) { keep_pool_memory(); }
+  explicit DeviceMem(cudaStream_t st) : s(st) {}
   ~DeviceMem() {
     for (void* p : ptrs) cudaFreeAsync(p, s);
   }
   template <typename T>
   cudaError_t alloc(T** out, int64_t count) {
     void* p = nullptr;
-    const cudaError_t e = cudaMallocAsync(&p, static_cast<size_t>(std::max<int64_t>(count, 1)) * sizeof(T), s);
+    const cudaError_t e = pool_alloc(&p, static_cast<size_t>(std::max<int64_t>(count, 1)) * sizeof(T), s);
     if (e != cudaSuccess) return e;
     ptrs.push_back(p);
     *out = static_cast<T*>(p);
@@ -756,9 +756,8 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
   float* pts = nullptr;
   const size_t nb = static_cast<size_t>(slots) * sizeof(Node);
   const size_t bb = static_cast<size_t>(slots) * 8 * sizeof(float);
-  keep_pool_memory();
-  e = cudaMallocAsync(reinterpret_cast<void**>(&nodes), nb + bb, s);
-  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&pts), static_cast<size_t>(n) * 4 * sizeof(float), s);
+  e = pool_alloc(reinterpret_cast<void**>(&nodes), nb + bb, s);
+  if (e == cudaSuccess) e = pool_alloc(reinterpret_cast<void**>(&pts), static_cast<size_t>(n) * 4 * sizeof(float), s);
   auto release = [&]() {
     if (nodes) cudaFreeAsync(nodes, s);
     if (pts) cudaFreeAsync(pts, s);
