@@ -315,6 +315,32 @@ def run_ours(args):
              "n_in": int(big.shape[0]), "n_out": int(vout.shape[0]), "voxel_m": 0.1}
     del big
 
+    # ---- nearest-neighbour queries alone: 1M Gaussian-mixture queries against
+    # 1M points of the same mixture (leaf 16), in generation order and sorted
+    # along the Morton curve; query only (the tree is built once)
+    g = workloads.gmm_case()
+    g_tree = nn.kdtree_build_device(torch.from_numpy(g.reference).cuda(), g.leaf_size, stream=stream)
+    g_q = torch.from_numpy(g.queries).cuda()
+    g_idx = torch.empty(len(g.queries), dtype=torch.int32, device="cuda")
+    g_d2 = torch.empty(len(g.queries), dtype=torch.float32, device="cuda")
+    nn_only = {}
+    for label, qflags in (("generation_order", 0), ("morton_sorted", nn.MORTON_SORT)):
+        for _ in range(3):
+            nn.nn_query(g_tree, g_q, g_idx, g_d2, qflags, stream=stream)
+        q_ms = []
+        for _ in range(10):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            nn.nn_query(g_tree, g_q, g_idx, g_d2, qflags, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            q_ms.append(a.elapsed_time(b))
+        med = statistics.median(q_ms)
+        nn_only[label] = {"queries_per_s": len(g.queries) / (med / 1e3), "ms": med}
+    g_tree.free()
+    del g_q, g_idx, g_d2
+
     # ---- end to end from host buffers: target copy + device tree build +
     # source copy + registration + result read, through the C ABI
     pinned_src = torch.from_numpy(case.source).pin_memory()
@@ -417,6 +443,8 @@ def run_ours(args):
         "multi_frame_8": dict(multi, note="8 independent 100k sources of the scene against one "
                                           "resident tree, icpnn_icp_align_batch, wall clock"),
         "voxel_downsample_4M": voxel,
+        "nn_query_gmm_1M_x_1M": dict(nn_only, note="1M Gaussian-mixture queries against 1M points, leaf 16, "
+                                                   "device memory, L2 flushed before each, median of 10"),
         "uniform200k_30_iterations_ms": {"value": statistics.median(u_ms),
                                          "note": "section 6 regression, 200k<->200k, 30 iterations, "
                                                  "target H2D (pinned) + device tree build + "
