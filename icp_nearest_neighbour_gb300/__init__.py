@@ -102,6 +102,7 @@ def load(build_if_missing: bool = False):
         "icpnn_version": ([], i32),
         "icpnn_probe_l2_read": ([P, i64, i32, P, P], ctypes.c_int),
         "icpnn_probe_command_wait": ([P, P, i64, ctypes.c_uint64, i32, P, P], ctypes.c_int),
+        "icpnn_probe_delay_commands": ([i32, i32, ctypes.c_uint64], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -232,6 +233,12 @@ def probe_command_wait(tree: KDTree, src, wait_ns: int, mode: int, stream=None) 
     _check(load().icpnn_probe_command_wait(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
                                            int(wait_ns), int(mode), ctypes.byref(out), _stream(stream)))
     return out.value
+
+
+def probe_delay_commands(skip: int, count: int, delay_ns: int):
+    """Test helper: on this thread, write the next `count` transform commands to
+    pre-launched passes (after `skip` normal ones) only after sleeping delay_ns."""
+    _check(load().icpnn_probe_delay_commands(int(skip), int(count), int(delay_ns)))
 
 
 def kdtree_upload(tree: KDTree, stream=None):

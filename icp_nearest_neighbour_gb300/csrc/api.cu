@@ -7,11 +7,13 @@
 
 #include <atomic>
 #include <cfloat>
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "icpnn_internal.h"
@@ -388,10 +390,23 @@ int pass_prelaunch(const Pass& ps, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t 
   return ICPNN_OK;
 }
 
+// Host-side fault injection for tests (icpnn_probe_delay_commands): the
+// calling thread's next commands are written late.
+thread_local int64_t tl_cmd_skip = 0, tl_cmd_delayed = 0;
+thread_local uint64_t tl_cmd_delay_ns = 0;
+
 // Hand pre-launched pass `seq` its transform, or (R == nullptr) tell it to
 // return without work.  The values are stored before the word that names
 // the pass, with release order.
 void pass_command(const Pass& ps, unsigned long long seq, const float* R, const float* tr) {
+  if (R != nullptr && tl_cmd_delayed > 0) {
+    if (tl_cmd_skip > 0) {
+      --tl_cmd_skip;
+    } else {
+      --tl_cmd_delayed;
+      std::this_thread::sleep_for(std::chrono::nanoseconds(tl_cmd_delay_ns));
+    }
+  }
   PassCommand* c = command_block(ps.mb, false);
   if (R != nullptr) {
     std::memcpy(c->rt, R, 9 * sizeof(float));
@@ -1055,6 +1070,16 @@ int icpnn_probe_command_wait(const icpnn_tree* t, const float* src, int64_t n, u
   ICPNN_CUDA(cudaStreamSynchronize(s));
   const unsigned long long w = *reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
   *outcome = w == p.seq ? 2 : w == (p.seq | kPassAborted) ? 1 : 0;
+  return ICPNN_OK;
+}
+
+int icpnn_probe_delay_commands(int32_t skip, int32_t count, uint64_t delay_ns) {
+  clear_error();
+  if (skip < 0 || count < 0 || delay_ns > 10000000000ull)
+    return fail(ICPNN_ERR_INVALID_ARG, "probe_delay_commands: skip, count >= 0 and delay_ns <= 1e10");
+  tl_cmd_skip = skip;
+  tl_cmd_delayed = count;
+  tl_cmd_delay_ns = delay_ns;
   return ICPNN_OK;
 }
 

@@ -23,6 +23,13 @@
  * synchronise `stream`, and report what the pass published in *outcome:
  * 0 nothing, 1 the abort marker, 2 its result.  Expected: 1, 0, 2.
  * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY. */
+/* icpnn_probe_delay_commands -- host-side fault injection for tests: on the
+ * calling thread, after `skip` transform commands to pre-launched passes
+ * (icpnn_icp_align) have been written normally, write each of the next
+ * `count` only after sleeping delay_ns (<= 1e10).  A delay beyond the passes'
+ * 50 ms wait makes a pass give up, which the registration must survive by
+ * falling back to ordinary launches.  count = 0 switches it off.
+ * Errors: INVALID_ARG. */
 #ifndef ICPNN_PROBE_H
 #define ICPNN_PROBE_H
 
@@ -37,6 +44,7 @@ int icpnn_probe_l2_read(const void* buf, int64_t bytes, int32_t repeats, uint32_
 struct icpnn_tree;
 int icpnn_probe_command_wait(const struct icpnn_tree* tree, const float* src, int64_t n, uint64_t wait_ns,
                              int32_t mode, int32_t* outcome, void* stream);
+int icpnn_probe_delay_commands(int32_t skip, int32_t count, uint64_t delay_ns);
 
 #ifdef __cplusplus
 }

@@ -284,6 +284,38 @@ def test_pass_command_wait_is_bounded(nn):
     np.testing.assert_array_equal(a["T"], b["T"])
 
 
+@pytest.mark.parametrize("skip", [0, 5])
+def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip):
+    """Fault injected on the host: the transform command of one pre-launched
+    pass (the first, or the sixth) is written 80 ms late, beyond the pass's
+    50 ms wait.  The pass gives up and publishes its abort marker; the
+    registration runs that pass again as an ordinary launch, continues with
+    ordinary launches, and ends bit-identical to a run that never
+    pre-launched."""
+    import time
+    c = W.scene_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    src = dev(c.source)
+    dmax = c.max_corr_dist[0]
+    ref = nn.icp_align(t, src, 12, 0.0, dmax, trace=True, prelaunch=False)
+    nn.probe_delay_commands(skip, 1, 80_000_000)
+    try:
+        t0 = time.perf_counter()
+        res = nn.icp_align(t, src, 12, 0.0, dmax, trace=True)
+        elapsed = time.perf_counter() - t0
+    finally:
+        nn.probe_delay_commands(0, 0, 0)
+    assert elapsed > 0.05
+    np.testing.assert_array_equal(res["T"], ref["T"])
+    assert res["iters"] == ref["iters"] and res["final_mse"] == ref["final_mse"]
+    assert [r["mse"] for r in res["trace"]] == [r["mse"] for r in ref["trace"]]
+    again = nn.icp_align(t, src, 12, 0.0, dmax)   # the next registration pre-launches again
+    np.testing.assert_array_equal(again["T"], ref["T"])
+    with pytest.raises(nn.IcpnnError):
+        nn.probe_delay_commands(-1, 1, 0)
+
+
 def test_large_coarse_to_fine(nn, oracle_mod):
     """4M target / 2M source, two stages (2.0 m then 0.3 m).  The first pass of
     each stage is compared on a 20k-point source sample (the oracle's search is
