@@ -212,7 +212,9 @@ typedef struct icpnn_iter_record {
     double sigma2;       /* mean squared residual under the first solve (residual
                             rejection only, else 0) */
     double T[16];        /* row-major transform this pass used (before the solve) */
-    float kernel_ms;     /* device time of the pass (with ICPNN_TRACE_TIMING), else 0 */
+    float kernel_ms;     /* device time of the pass (with ICPNN_TRACE_TIMING), else 0;
+                            a pre-launched pass's time includes its wait for the
+                            transform (ICPNN_NO_PRELAUNCH times the kernel alone) */
     float reserved;
 } icpnn_iter_record;
 
