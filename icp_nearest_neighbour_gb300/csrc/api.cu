@@ -122,11 +122,15 @@ struct MappedBuffer {
   unsigned long long seq = 0;  // last sequence number handed to a pass
 };
 thread_local MappedBuffer tl_mapped;
-constexpr int kMappedDoubles = 64;
-// Doubles [0, kMomentSlots] hold a pass's result and its sequence word; the
-// host-written PassCommand of pre-launched passes starts at byte 256, on a
-// cache line of its own.
-constexpr int kCommandOffset = 32;
+// Layout, in doubles, each region on cache lines of its own:
+//   [0, kMomentSlots]                          a pass's result and its sequence word
+//   [kSecondSlot, kSecondSlot + kMomentSlots]  the other residual pass's result and word
+//   [kCommandOffset, + sizeof(PassCommand))    the host-written command of pre-launched passes
+constexpr int kSecondSlot = 32;
+constexpr int kCommandOffset = 64;
+constexpr int kMappedDoubles = 96;
+static_assert(kSecondSlot > kMomentSlots && kCommandOffset > kSecondSlot + kMomentSlots,
+              "mapped-buffer regions must not overlap");
 static_assert(kCommandOffset * sizeof(double) + sizeof(PassCommand) <= kMappedDoubles * sizeof(double),
               "command block must fit the mapped buffer");
 
@@ -462,9 +466,8 @@ int timing_events(size_t count, cudaEvent_t** out) {
 // Residual rejection of one iteration (page section 4.4), two passes back to
 // back on the stream: the first sums e2 over all matched pairs and leaves the
 // 3-sigma threshold in device memory, the second keeps the pairs within it
-// and sums their moments; the host waits once.  The first pass publishes in
-// the upper half of the mapped buffer.
-constexpr int kSecondSlot = 32;
+// and sums their moments; the host waits once.  The first pass publishes at
+// kSecondSlot of the mapped buffer.
 
 int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream_t s, double* sigma2,
                  icpnn_moments* kept) {

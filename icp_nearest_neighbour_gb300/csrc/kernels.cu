@@ -756,7 +756,7 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
                                                       const float4* __restrict__ q, int64_t n,
                                                       int32_t* __restrict__ out_idx,
                                                       float* __restrict__ out_d2) {
-  extern __shared__ uint2 s_nodes[];
+  extern __shared__ __align__(16) uint2 s_nodes[];
   stage_top(nodes, s_nodes, smem_slots);
   const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
   const int lane = threadIdx.x & 31;
@@ -1078,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_kernel(
     int smem_slots, const float4* __restrict__ src, int64_t n, IcpPassParams p, double* __restrict__ partials,
     unsigned int* __restrict__ counter, double* out, int32_t* __restrict__ out_idx,
     float* __restrict__ out_d2, int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of) {
-  extern __shared__ uint2 s_nodes[];
+  extern __shared__ __align__(16) uint2 s_nodes[];
   __shared__ float s_rt[12];
   __shared__ unsigned int s_skip;
   if (p.cmd == nullptr) {
@@ -1428,7 +1428,7 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_inplace_kernel(
     const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
     int smem_slots, const float* __restrict__ xyz, int64_t n, IcpPassParams p, double* __restrict__ scratch,
     int32_t* __restrict__ out_idx, float* __restrict__ out_d2) {
-  extern __shared__ uint2 s_nodes[];
+  extern __shared__ __align__(16) uint2 s_nodes[];
   double* partials = scratch;
   double* result = scratch + kNoAllocResult;
   unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kNoAllocCounter);

@@ -284,6 +284,23 @@ def test_pass_command_wait_is_bounded(nn):
     np.testing.assert_array_equal(a["T"], b["T"])
 
 
+def test_residual_and_prelaunched_registrations_alternate(nn):
+    """The residual passes publish in a second slot of the thread's mapped
+    buffer and the pre-launched passes read their commands from a third: a
+    registration of either kind leaves the other's region untouched."""
+    c = W.tiny_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    src = dev(c.source)
+    ref = nn.icp_align(t, src, 10, 0.0, math.inf, prelaunch=False)
+    ref_r = nn.icp_align(t, src, 10, 0.0, math.inf, residual_reject=True)
+    for _ in range(6):
+        r = nn.icp_align(t, src, 10, 0.0, math.inf, residual_reject=True)
+        np.testing.assert_array_equal(r["T"], ref_r["T"])
+        r = nn.icp_align(t, src, 10, 0.0, math.inf)
+        np.testing.assert_array_equal(r["T"], ref["T"])
+
+
 @pytest.mark.parametrize("skip", [0, 5])
 def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip):
     """Fault injected on the host: the transform command of one pre-launched
