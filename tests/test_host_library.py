@@ -193,6 +193,23 @@ def test_kabsch_degenerate(lib):
     assert e.value.status == "DEGENERATE"
 
 
+def test_probe_entry_points_check_arguments_without_a_device(lib):
+    """The test helpers behind the pre-launched passes validate on the host:
+    the command-delay injector takes its settings (and is switched off
+    again), the command-wait probe needs an uploaded tree."""
+    for bad in ((-1, 1, 0), (0, -1, 0), (0, 1, 10_000_000_001)):
+        with pytest.raises(lib.IcpnnError) as e:
+            lib.probe_delay_commands(*bad)
+        assert e.value.status == "INVALID_ARG"
+    lib.probe_delay_commands(2, 1, 1000)
+    lib.probe_delay_commands(0, 0, 0)
+    t = lib.kdtree_build(W.uniform_cloud(100, 3), 8)
+    with pytest.raises(lib.IcpnnError) as e:
+        lib.probe_command_wait(t, W.uniform_cloud(10, 4), 1_000_000, 0)
+    assert e.value.status == "NOT_UPLOADED"
+    assert lib.NO_PRELAUNCH == 16
+
+
 def test_query_without_upload_is_an_error(lib):
     t = lib.kdtree_build(W.uniform_cloud(100, 3), 8)
     q = W.uniform_cloud(10, 4)
@@ -201,6 +218,9 @@ def test_query_without_upload_is_an_error(lib):
     assert e.value.status == "NOT_UPLOADED"
     with pytest.raises(lib.IcpnnError) as e:
         lib.icp_align(t, q, 5, 1e-6)
+    assert e.value.status == "NOT_UPLOADED"
+    with pytest.raises(lib.IcpnnError) as e:
+        lib.icp_align(t, q, 5, 1e-6, prelaunch=False)
     assert e.value.status == "NOT_UPLOADED"
 
 
