@@ -24,7 +24,7 @@ __all__ = [
     "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
     "kabsch", "icp_align", "icp_align_batch", "voxel_downsample",
     "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "NO_PRELAUNCH", "MAX_DEPTH",
-    "NOALLOC_MAX_POINTS",
+    "NOALLOC_MAX_POINTS", "OVERLAP_WARN_RATIO", "LowOverlapWarning",
 ]
 
 MORTON_SORT = 1
@@ -34,6 +34,7 @@ SPLIT_ROUND_ROBIN = 8
 NO_PRELAUNCH = 16
 MAX_DEPTH = 20
 NOALLOC_MAX_POINTS = 1 << 20
+OVERLAP_WARN_RATIO = 0.8
 
 STATUS = {
     0: "OK", -1: "INVALID_ARG", -2: "NOT_UPLOADED", -3: "CUDA", -4: "DEGENERATE",
@@ -46,6 +47,11 @@ class IcpnnError(RuntimeError):
         super().__init__(f"{STATUS.get(code, code)}: {msg}")
         self.code = code
         self.status = STATUS.get(code, str(code))
+
+
+class LowOverlapWarning(UserWarning):
+    """A registration ended with fewer than OVERLAP_WARN_RATIO of the source
+    points matched within the maximum correspondence distance."""
 
 
 class Moments(ctypes.Structure):
@@ -94,8 +100,8 @@ def load(build_if_missing: bool = False):
         "icpnn_icp_step": ([P, P, i64, P, P, f64, P, P, P, P], ctypes.c_int),
         "icpnn_icp_step_noalloc": ([P, P, i64, P, P, f64, P, P, P, P], ctypes.c_int),
         "icpnn_kabsch": ([P, P], ctypes.c_int),
-        "icpnn_icp_align": ([P, P, i64, i32, f64, f64, P, P, P, P, P, i32, u32, P], ctypes.c_int),
-        "icpnn_icp_align_batch": ([P, i32, P, P, i32, f64, f64, P, P, P, P, P, u32, i32, P], ctypes.c_int),
+        "icpnn_icp_align": ([P, P, i64, i32, f64, f64, P, P, P, P, P, P, i32, u32, P], ctypes.c_int),
+        "icpnn_icp_align_batch": ([P, i32, P, P, i32, f64, f64, P, P, P, P, P, P, u32, i32, P], ctypes.c_int),
         "icpnn_voxel_downsample": ([P, i64, ctypes.c_float, P, P, P], ctypes.c_int),
         "icpnn_last_error": ([], ctypes.c_char_p),
         "icpnn_launch_count": ([], i64),
@@ -103,6 +109,7 @@ def load(build_if_missing: bool = False):
         "icpnn_probe_l2_read": ([P, i64, i32, P, P], ctypes.c_int),
         "icpnn_probe_command_wait": ([P, P, i64, ctypes.c_uint64, i32, P, P], ctypes.c_int),
         "icpnn_probe_delay_commands": ([i32, i32, ctypes.c_uint64], ctypes.c_int),
+        "icpnn_probe_delay_collect": ([i32, i32, ctypes.c_uint64], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -241,6 +248,13 @@ def probe_delay_commands(skip: int, count: int, delay_ns: int):
     _check(load().icpnn_probe_delay_commands(int(skip), int(count), int(delay_ns)))
 
 
+def probe_delay_collect(skip: int, count: int, delay_ns: int):
+    """Test helper: on this thread, start the next `count` reads of a
+    pre-launched pass's result (after `skip` normal ones) only after sleeping
+    delay_ns, between queuing the successor pass and reading the result."""
+    _check(load().icpnn_probe_delay_collect(int(skip), int(count), int(delay_ns)))
+
+
 def kdtree_upload(tree: KDTree, stream=None):
     _check(load().icpnn_kdtree_upload(tree.handle, _stream(stream)))
 
@@ -328,15 +342,29 @@ def kabsch(moments: dict) -> np.ndarray:
     return T.reshape(4, 4)
 
 
+def _overlap(n_accepted: int, n: int, warn: bool) -> dict:
+    ratio = n_accepted / n if n else float("nan")
+    low = bool(ratio < OVERLAP_WARN_RATIO)
+    if low and warn:
+        import warnings
+        warnings.warn(f"registration overlap {ratio:.3f} is below {OVERLAP_WARN_RATIO}: "
+                      f"{n_accepted} of {n} source points matched", LowOverlapWarning, stacklevel=3)
+    return {"final_n_accepted": int(n_accepted), "overlap": ratio, "low_overlap": low}
+
+
 def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
               init_T=None, trace: bool = False, timing: bool = False, residual_reject: bool = False,
-              prelaunch: bool = True, stream=None) -> dict:
-    """Register src onto the tree's points; returns dict(T, final_mse, iters, trace).
+              prelaunch: bool = True, warn_overlap: bool = True, stream=None) -> dict:
+    """Register src onto the tree's points; returns dict(T, final_mse, iters,
+    final_n_accepted, overlap, low_overlap, trace).
     residual_reject adds the 3-sigma residual rejection and re-solve to every iteration;
-    prelaunch=False launches each pass only after its transform is solved."""
+    prelaunch=False launches each pass only after its transform is solved.
+    overlap = final_n_accepted / n; below OVERLAP_WARN_RATIO a LowOverlapWarning is
+    issued (unless warn_overlap=False), as the page's section 6 advises."""
     T = np.zeros(16)
     fmse = ctypes.c_double()
     iters = ctypes.c_int32()
+    n_fin = ctypes.c_int64()
     init = None
     if init_T is not None:
         init_arr = np.ascontiguousarray(init_T, dtype=np.float64).reshape(16)
@@ -348,9 +376,10 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
     _check(load().icpnn_icp_align(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
                                   int(max_iter), float(eps), float(max_corr_dist), init,
                                   ctypes.c_void_p(T.ctypes.data), ctypes.byref(fmse), ctypes.byref(iters),
-                                  ctypes.cast(recs, ctypes.c_void_p) if cap else None, cap, flags,
-                                  _stream(stream)))
+                                  ctypes.byref(n_fin), ctypes.cast(recs, ctypes.c_void_p) if cap else None,
+                                  cap, flags, _stream(stream)))
     out = {"T": T.reshape(4, 4), "final_mse": fmse.value, "iters": iters.value}
+    out.update(_overlap(n_fin.value, int(src.shape[0]), warn_overlap))
     if cap:
         out["trace"] = [{"iter": r.iter, "n_accepted": r.n_accepted, "n_inliers": r.n_inliers,
                          "mse": r.mse, "sigma2": r.sigma2, "T": np.array(r.T[:]).reshape(4, 4),
@@ -364,13 +393,15 @@ def icp_align_batch(tree: KDTree, srcs, max_iter: int, eps: float, max_corr_dist
                     prelaunch: bool = True, stream=None) -> dict:
     """Register several sources against one tree, several frames in flight.
 
-    Returns dict(T (n, 4, 4), final_mse (n,), iters (n,), status (n,))."""
+    Returns dict(T (n, 4, 4), final_mse (n,), iters (n,), final_n_accepted (n,),
+    overlap (n,), status (n,))."""
     n = len(srcs)
     ptrs = (ctypes.c_void_p * n)(*[_ptr(x, np.float32, 3, f"srcs[{i}]").value for i, x in enumerate(srcs)])
     counts = np.ascontiguousarray([int(x.shape[0]) for x in srcs], dtype=np.int64)
     T = np.zeros((n, 16))
     fmse = np.zeros(n)
     iters = np.zeros(n, np.int32)
+    n_fin = np.zeros(n, np.int64)
     status = np.zeros(n, np.int32)
     init = None
     if init_T is not None:
@@ -380,11 +411,12 @@ def icp_align_batch(tree: KDTree, srcs, max_iter: int, eps: float, max_corr_dist
                                       ctypes.c_void_p(counts.ctypes.data), int(max_iter), float(eps),
                                       float(max_corr_dist), init, ctypes.c_void_p(T.ctypes.data),
                                       ctypes.c_void_p(fmse.ctypes.data), ctypes.c_void_p(iters.ctypes.data),
-                                      ctypes.c_void_p(status.ctypes.data),
+                                      ctypes.c_void_p(n_fin.ctypes.data), ctypes.c_void_p(status.ctypes.data),
                                       (RESIDUAL_REJECT if residual_reject else 0)
                                       | (0 if prelaunch else NO_PRELAUNCH), int(max_concurrent),
                                       _stream(stream))
-    out = {"T": T.reshape(n, 4, 4), "final_mse": fmse, "iters": iters, "status": status}
+    out = {"T": T.reshape(n, 4, 4), "final_mse": fmse, "iters": iters, "final_n_accepted": n_fin,
+           "overlap": n_fin / counts, "status": status}
     if rc != 0:
         err = IcpnnError(rc, last_error())
         err.result = out

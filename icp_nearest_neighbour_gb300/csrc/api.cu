@@ -123,13 +123,13 @@ struct MappedBuffer {
 };
 thread_local MappedBuffer tl_mapped;
 // Layout, in doubles, each region on cache lines of its own:
-//   [0, kMomentSlots]                          a pass's result and its sequence word
-//   [kSecondSlot, kSecondSlot + kMomentSlots]  the other residual pass's result and word
+//   [0, kMomentSlots + 1]                      a pass's result, its publish word, its abort word
+//   [kSecondSlot, kSecondSlot + kMomentSlots + 1]  the other residual pass's result and words
 //   [kCommandOffset, + sizeof(PassCommand))    the host-written command of pre-launched passes
 constexpr int kSecondSlot = 32;
 constexpr int kCommandOffset = 64;
 constexpr int kMappedDoubles = 96;
-static_assert(kSecondSlot > kMomentSlots && kCommandOffset > kSecondSlot + kMomentSlots,
+static_assert(kSecondSlot > kMomentSlots + 1 && kCommandOffset > kSecondSlot + kMomentSlots + 1,
               "mapped-buffer regions must not overlap");
 static_assert(kCommandOffset * sizeof(double) + sizeof(PassCommand) <= kMappedDoubles * sizeof(double),
               "command block must fit the mapped buffer");
@@ -332,29 +332,32 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
   return ICPNN_OK;
 }
 
-// Wait until the pass with sequence number `seq` has published its result (or
-// its abort marker, reported through *aborted) in mapped memory.  Bounded: the
-// stream is queried every few thousand polls, so a failed or finished kernel
-// ends the wait.
+// Wait until the pass with sequence number `seq` has published its result in
+// mapped memory, or -- for a pre-launched pass, with `aborted` given -- until
+// it is known to have given up waiting for its command.  `flag` is the
+// publish word; the abort word follows it.  A pass that gives up stores its
+// sequence number in the abort word, so a later pass that gives up too (the
+// one queued behind it, say, when launches are serialised or the host stalls)
+// cannot hide this pass's outcome: an abort word at or beyond `seq` means that
+// pass `seq` has finished, and the publish word then tells whether it
+// published.  Bounded: the stream is queried every few thousand polls, so a
+// failed or finished kernel ends the wait.
 int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s,
                    bool* aborted = nullptr) {
+  const volatile unsigned long long* abort_word = flag + 1;
   for (uint64_t spins = 1;; ++spins) {
-    unsigned long long w = *flag;
-    if ((w & ~kPassAborted) != seq && (spins & 4095u) == 0) {
-      const cudaError_t e = cudaStreamQuery(s);
-      w = *flag;
-      if ((w & ~kPassAborted) != seq) {
-        if (e == cudaSuccess) return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
-        if (e != cudaErrorNotReady)
-          return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
-      }
-    }
-    if ((w & ~kPassAborted) == seq) {
-      if (w & kPassAborted) {
-        if (aborted == nullptr) return fail(ICPNN_ERR_CUDA, "ICP pass aborted");
-        *aborted = true;
-      }
+    if (*flag == seq) return ICPNN_OK;
+    if (aborted != nullptr && *abort_word >= seq) {
+      std::atomic_thread_fence(std::memory_order_acquire);
+      if (*flag == seq) return ICPNN_OK;
+      *aborted = true;
       return ICPNN_OK;
+    }
+    if ((spins & 4095u) == 0) {
+      const cudaError_t e = cudaStreamQuery(s);
+      if (*flag == seq || (aborted != nullptr && *abort_word >= seq)) continue;
+      if (e == cudaSuccess) return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
+      if (e != cudaErrorNotReady) return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
     }
   }
 }
@@ -398,6 +401,20 @@ int pass_prelaunch(const Pass& ps, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t 
 // calling thread's next commands are written late.
 thread_local int64_t tl_cmd_skip = 0, tl_cmd_delayed = 0;
 thread_local uint64_t tl_cmd_delay_ns = 0;
+// ... and (icpnn_probe_delay_collect) its next reads of a pre-launched pass's
+// result start late, after the successor pass has been queued.
+thread_local int64_t tl_collect_skip = 0, tl_collect_delayed = 0;
+thread_local uint64_t tl_collect_delay_ns = 0;
+
+void injected_collect_delay() {
+  if (tl_collect_delayed <= 0) return;
+  if (tl_collect_skip > 0) {
+    --tl_collect_skip;
+    return;
+  }
+  --tl_collect_delayed;
+  std::this_thread::sleep_for(std::chrono::nanoseconds(tl_collect_delay_ns));
+}
 
 // Hand pre-launched pass `seq` its transform, or (R == nullptr) tell it to
 // return without work.  The values are stored before the word that names
@@ -843,8 +860,8 @@ int icpnn_kabsch(const icpnn_moments* m, double* T) {
 
 int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_t max_iter, double eps,
                     double max_corr_dist, const double* init_T, double* out_T, double* final_mse,
-                    int32_t* iters, icpnn_iter_record* trace, int32_t trace_cap, uint32_t flags,
-                    void* stream) {
+                    int32_t* iters, int64_t* final_n_accepted, icpnn_iter_record* trace, int32_t trace_cap,
+                    uint32_t flags, void* stream) {
   clear_error();
   if (int rc = check_tree_on_device(t)) return rc;
   if (!src || !out_T || !final_mse || !iters) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: NULL pointer");
@@ -895,6 +912,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   auto collect = [&](bool more, cudaEvent_t ev0, cudaEvent_t ev1, icpnn_moments* m) -> int {
     if (more)
       if (int rc = pass_prelaunch(ps, s, ev0, ev1, &next.seq)) return rc;
+    injected_collect_delay();
     const volatile unsigned long long* flag =
         reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
     bool aborted = false;
@@ -995,6 +1013,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   std::memcpy(out_T, T, sizeof(T));
   *final_mse = fin.mse;
   *iters = done;
+  if (final_n_accepted != nullptr) *final_n_accepted = fin.n_accepted;
   return ICPNN_OK;
 }
 
@@ -1071,8 +1090,9 @@ int icpnn_probe_command_wait(const icpnn_tree* t, const float* src, int64_t n, u
     pass_command(ps, p.seq, R, tr);
   }
   ICPNN_CUDA(cudaStreamSynchronize(s));
-  const unsigned long long w = *reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-  *outcome = w == p.seq ? 2 : w == (p.seq | kPassAborted) ? 1 : 0;
+  const volatile unsigned long long* words =
+      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
+  *outcome = words[0] == p.seq ? 2 : words[1] == p.seq ? 1 : 0;
   return ICPNN_OK;
 }
 
@@ -1083,6 +1103,16 @@ int icpnn_probe_delay_commands(int32_t skip, int32_t count, uint64_t delay_ns) {
   tl_cmd_skip = skip;
   tl_cmd_delayed = count;
   tl_cmd_delay_ns = delay_ns;
+  return ICPNN_OK;
+}
+
+int icpnn_probe_delay_collect(int32_t skip, int32_t count, uint64_t delay_ns) {
+  clear_error();
+  if (skip < 0 || count < 0 || delay_ns > 10000000000ull)
+    return fail(ICPNN_ERR_INVALID_ARG, "probe_delay_collect: skip, count >= 0 and delay_ns <= 1e10");
+  tl_collect_skip = skip;
+  tl_collect_delayed = count;
+  tl_collect_delay_ns = delay_ns;
   return ICPNN_OK;
 }
 

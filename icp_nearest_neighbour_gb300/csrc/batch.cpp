@@ -51,8 +51,8 @@ using namespace icpnn;
 extern "C" int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames, const float* const* srcs,
                                      const int64_t* n_src, int32_t max_iter, double eps,
                                      double max_corr_dist, const double* init_T, double* out_T,
-                                     double* final_mse, int32_t* iters, int32_t* status, uint32_t flags,
-                                     int32_t max_concurrent, void* stream) {
+                                     double* final_mse, int32_t* iters, int64_t* final_n_accepted,
+                                     int32_t* status, uint32_t flags, int32_t max_concurrent, void* stream) {
   clear_error();
   if (target == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "icp_align_batch: tree is NULL");
   if (target->dev.nodes == nullptr) return fail(ICPNN_ERR_NOT_UPLOADED, "icp_align_batch: tree has not been uploaded");
@@ -108,8 +108,8 @@ extern "C" int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames,
         if (r == ICPNN_OK)
           r = icpnn_icp_align(target, srcs[f], n_src[f], max_iter, eps, max_corr_dist,
                               init_T ? init_T + 16 * static_cast<int64_t>(f) : nullptr,
-                              out_T + 16 * static_cast<int64_t>(f), final_mse + f, iters + f, nullptr, 0,
-                              frame_flags, ws);
+                              out_T + 16 * static_cast<int64_t>(f), final_mse + f, iters + f,
+                              final_n_accepted ? final_n_accepted + f : nullptr, nullptr, 0, frame_flags, ws);
         status[f] = r;
         if (r != ICPNN_OK) sh.msg[static_cast<size_t>(f)] = rc != ICPNN_OK ? setup_msg : icpnn_last_error();
       }

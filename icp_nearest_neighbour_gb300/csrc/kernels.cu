@@ -784,7 +784,9 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
 // warps of a block in order in double, then the last block to finish sums
 // the block partials in block order.  out[0] = c0, out[1] = c1 (counts),
 // out[2 + v] = acc[v].  With kPublish the last block then publishes `seq`
-// in the word after the result, once the result is visible system-wide.
+// in the word after the result, once the result is visible system-wide; a
+// pass that gave up waiting for its command stores `seq` in the next word
+// instead (the abort word) and leaves the result and its word untouched.
 // The float threshold t with float(e2) <= t exactly when e2 <= limit in
 // double: the largest float not above limit (+inf stays +inf).
 __device__ __forceinline__ float float_threshold_dev(double limit) {
@@ -914,9 +916,12 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     *counter = 0u;
     const unsigned int skips = atomicExch(counter + 1, 0u);
     if (skips != 0u) {
+      // The abort marker has a word of its own: the pass queued behind this
+      // one may give up too, and its marker must not overwrite this pass's
+      // outcome, nor this marker a predecessor's published result.
       if (kPublish && skips >= kSkipTimedOut) {
         __threadfence_system();
-        *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq | kPassAborted;
+        *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots + 1) = seq;
       }
       return;
     }

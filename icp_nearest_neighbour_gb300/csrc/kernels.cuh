@@ -55,13 +55,13 @@ struct IcpPassParams {
   // most wait_ns of global time, until cmd->word names this pass's seq and
   // takes R and t from cmd->rt.  A block that finds the stop bit, a later
   // seq, or no command in time does no work; the pass then publishes nothing
-  // (stop, later seq) or, if any block ran out of time, seq | kPassAborted.
+  // (stop, later seq) or, if any block ran out of time, stores seq in the
+  // abort word (the word after the publish word).
   const PassCommand* cmd;
   CommandMirror* mirror;
   unsigned long long wait_ns;
 };
 
-constexpr unsigned long long kPassAborted = 1ull << 63;
 constexpr unsigned long long kCommandWaitNs = 50ull * 1000 * 1000;
 
 // Bounding box of n points as order-preserving int encodings
@@ -95,9 +95,14 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
 // One fused ICP pass: transform, search, reject, reduce.  `partials` holds
 // grid * kMomentSlots doubles, `counter` reduction_counter_words(grid) zeroed
 // words (left zeroed), `out`
-// kMomentSlots doubles followed by one 64-bit word (may be host-mapped): once
-// the result is complete and visible system-wide the kernel stores p.seq in
-// that word, so the host can poll it instead of synchronising the stream.
+// kMomentSlots doubles followed by two 64-bit words (may be host-mapped):
+// once the result is complete and visible system-wide the kernel stores p.seq
+// in the first (the publish word), so the host can poll it instead of
+// synchronising the stream; a pre-launched pass that gave up waiting for its
+// command stores p.seq in the second (the abort word) and nothing else.
+// Sequence numbers grow pass by pass, and a pass reaches its reduction only
+// after its predecessor on the stream has completed, so an abort word at or
+// beyond s proves that pass s has finished, published or not.
 // idx/dist2 optional.
 int icp_pass_grid(const icpnn_tree& t, int64_t n);
 // slot_of (optional): per source record, the record slot of its accepted

@@ -267,6 +267,13 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   out_T        host double[16]: the last solved transform (target ~ T src).
  *   final_mse    host: mse of the extra pass (NaN if nothing accepted).
  *   iters        host: number of solves performed.
+ *   final_n_accepted  optional host int64: pairs accepted by the extra pass.
+ *                final_n_accepted / n_src is the overlap ratio of page
+ *                section 6, which advises a warning when it falls below
+ *                ICPNN_OVERLAP_WARN_RATIO after registration (a symptom of
+ *                a wrong stopping rule or a failed registration).  With no
+ *                maximum distance every finite point is accepted and the
+ *                ratio is 1.
  *   trace        optional host array of trace_cap records (one per
  *                iteration, up to trace_cap).
  *   flags        ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT |
@@ -274,10 +281,11 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  * Synchronises `stream` once per iteration; scratch comes from the
  * stream-ordered allocator and is returned before the call ends.
  * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY, NONFINITE, DEGENERATE. */
+#define ICPNN_OVERLAP_WARN_RATIO 0.8
 int icpnn_icp_align(const icpnn_tree* target, const float* src, int64_t n_src, int32_t max_iter,
                     double eps, double max_corr_dist, const double* init_T, double* out_T,
-                    double* final_mse, int32_t* iters, icpnn_iter_record* trace,
-                    int32_t trace_cap, uint32_t flags, void* stream);
+                    double* final_mse, int32_t* iters, int64_t* final_n_accepted,
+                    icpnn_iter_record* trace, int32_t trace_cap, uint32_t flags, void* stream);
 
 /* icpnn_icp_align_batch -- register n_frames sources against one resident
  * target (page section 3.4: several frames in flight so that one frame's
@@ -292,6 +300,7 @@ int icpnn_icp_align(const icpnn_tree* target, const float* src, int64_t n_src, i
  *   out_T, final_mse, iters, status   per-frame outputs (host arrays of
  *                 16*n_frames, n_frames, n_frames, n_frames); status[f] is
  *                 frame f's icpnn_status.
+ *   final_n_accepted  optional host int64[n_frames]: as for icpnn_icp_align.
  *   flags         ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH, or 0; with more
  *                 than one frame in flight passes are never pre-launched
  *                 (a waiting pass would hold SM slots other frames can use).
@@ -304,7 +313,8 @@ int icpnn_icp_align(const icpnn_tree* target, const float* src, int64_t n_src, i
 int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames, const float* const* srcs,
                           const int64_t* n_src, int32_t max_iter, double eps, double max_corr_dist,
                           const double* init_T, double* out_T, double* final_mse, int32_t* iters,
-                          int32_t* status, uint32_t flags, int32_t max_concurrent, void* stream);
+                          int64_t* final_n_accepted, int32_t* status, uint32_t flags,
+                          int32_t max_concurrent, void* stream);
 
 /* ------------------------------------------------------ no allocation --
  * icpnn_icp_step_noalloc -- the fused correspondence pass of icpnn_icp_step

@@ -21,7 +21,8 @@
  *   1  write the stop command: the blocks return without work;
  *   2  write the identity transform: the pass runs normally;
  * synchronise `stream`, and report what the pass published in *outcome:
- * 0 nothing, 1 the abort marker, 2 its result.  Expected: 1, 0, 2.
+ * 0 nothing, 1 its sequence number in the abort word, 2 its result.
+ * Expected: 1, 0, 2.
  * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY. */
 /* icpnn_probe_delay_commands -- host-side fault injection for tests: on the
  * calling thread, after `skip` transform commands to pre-launched passes
@@ -29,6 +30,16 @@
  * `count` only after sleeping delay_ns (<= 1e10).  A delay beyond the passes'
  * 50 ms wait makes a pass give up, which the registration must survive by
  * falling back to ordinary launches.  count = 0 switches it off.
+ * Errors: INVALID_ARG. */
+/* icpnn_probe_delay_collect -- host-side fault injection for tests: on the
+ * calling thread, after `skip` reads of a pre-launched pass's result
+ * (icpnn_icp_align) have started normally, start each of the next `count`
+ * only after sleeping delay_ns (<= 1e10).  The sleep falls between queuing
+ * pass k+1 and reading pass k, as when the host thread is descheduled or a
+ * profiler serialises the launches: with a delay beyond twice the 50 ms
+ * command wait, pass k+1 gives up while pass k's result is still unread.
+ * The registration must still read pass k's outcome, then fall back to
+ * ordinary launches.  count = 0 switches it off.
  * Errors: INVALID_ARG. */
 #ifndef ICPNN_PROBE_H
 #define ICPNN_PROBE_H
@@ -45,6 +56,7 @@ struct icpnn_tree;
 int icpnn_probe_command_wait(const struct icpnn_tree* tree, const float* src, int64_t n, uint64_t wait_ns,
                              int32_t mode, int32_t* outcome, void* stream);
 int icpnn_probe_delay_commands(int32_t skip, int32_t count, uint64_t delay_ns);
+int icpnn_probe_delay_collect(int32_t skip, int32_t count, uint64_t delay_ns);
 
 #ifdef __cplusplus
 }

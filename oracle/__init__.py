@@ -238,25 +238,22 @@ class KDTree:
         q = _f32(queries)
         idx = np.empty(len(q), np.int32)
         d2 = np.empty(len(q), np.float32)
-        if workers > 1 and not counts and len(q) >= 2 * workers:
+        nodes = np.empty(len(q), np.int64) if counts else None
+        pts = np.empty(len(q), np.int64) if counts else None
+
+        def run_range(a, b):
+            # ctypes releases the GIL for the duration of the C call
+            _lib.orc_tree_nn(self._h, _ptr(q[a:b]), b - a, _ptr(idx[a:b]), _ptr(d2[a:b]),
+                             _ptr(nodes[a:b]) if counts else None, _ptr(pts[a:b]) if counts else None)
+
+        if workers > 1 and len(q) >= 2 * workers:
             from concurrent.futures import ThreadPoolExecutor
             bounds = np.linspace(0, len(q), workers + 1).astype(np.int64)
-
-            def run(k):
-                a, b = int(bounds[k]), int(bounds[k + 1])
-                # ctypes releases the GIL for the duration of the C call
-                _lib.orc_tree_nn(self._h, _ptr(q[a:b]), b - a, _ptr(idx[a:b]), _ptr(d2[a:b]), None, None)
-
             with ThreadPoolExecutor(workers) as ex:
-                list(ex.map(run, range(workers)))
-            return idx, d2
-        if counts:
-            nodes = np.empty(len(q), np.int64)
-            pts = np.empty(len(q), np.int64)
-            _lib.orc_tree_nn(self._h, _ptr(q), len(q), _ptr(idx), _ptr(d2), _ptr(nodes), _ptr(pts))
-            return idx, d2, nodes, pts
-        _lib.orc_tree_nn(self._h, _ptr(q), len(q), _ptr(idx), _ptr(d2), None, None)
-        return idx, d2
+                list(ex.map(lambda k: run_range(int(bounds[k]), int(bounds[k + 1])), range(workers)))
+        elif len(q):
+            run_range(0, len(q))
+        return (idx, d2, nodes, pts) if counts else (idx, d2)
 
 
 # -------------------------------------------------------------- Kabsch ----
@@ -297,17 +294,24 @@ def accept_mask(idx, d2, max_corr_dist):
 
 # ----------------------------------------------------------------- ICP ----
 
-def icp_step(tree: KDTree, source, T, max_corr_dist, workers: int = 1):
+def icp_step(tree: KDTree, source, T, max_corr_dist, workers: int = 1, nn=None):
     """One correspondence + reduction pass under transform T (double 4x4).
+
+    nn: optional (idx, d2) already found by this tree for exactly the points
+    this pass queries (the float32 transform of the source under T), to skip
+    the search.
 
     Returns a dict: idx, d2 (per source point), accepted mask, n_accepted,
     mse, mu_s, mu_q, H (None when nothing is accepted)."""
     src = _f32(source)
     if not np.all(np.isfinite(src)):
         raise NonFiniteError("non-finite source point")
-    R32, t32 = as_kernel_rt(T)
-    p = transform(R32, t32, src)
-    idx, d2 = tree.query(p, workers=workers)
+    if nn is not None:
+        idx, d2 = nn
+    else:
+        R32, t32 = as_kernel_rt(T)
+        p = transform(R32, t32, src)
+        idx, d2 = tree.query(p, workers=workers)
     acc = accept_mask(idx, d2, max_corr_dist)
     n_acc = int(acc.sum())
     out = {"idx": idx, "d2": d2, "accepted": acc, "n_accepted": n_acc,

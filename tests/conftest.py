@@ -31,3 +31,17 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def large_oracle(oracle_mod):
+    """The 4M-target / 2M-source workload with the oracle's tree and the
+    oracle's nearest neighbour of every raw source point (its searches split
+    over the host cores), computed once per session: the NN-only check and
+    the first ICP pass (identity transform) share it."""
+    import workloads as W
+    c = W.large_case()
+    ot = oracle_mod.KDTree(c.target, c.leaf_size)
+    workers = max(1, min(64, os.cpu_count() or 1))
+    idx, d2 = ot.query(c.source, workers=workers)
+    return {"case": c, "tree": ot, "workers": workers, "identity_nn": (idx, d2)}

@@ -162,16 +162,54 @@ def test_align_parity(nn, oracle_mod, name):
     dmax = c.max_corr_dist[0]
     res = nn.icp_align(t, dev(c.source), c.max_iter, c.eps, dmax, trace=True)
     _trace_parity(nn, oracle_mod, c, t, ot, c.source, dmax, res)
+    # the reported error is the oracle's pass under the returned transform
+    fin = oracle_mod.icp_step(ot, c.source, res["T"], dmax)
+    assert abs(res["final_mse"] - fin["mse"]) <= 1e-6 * fin["mse"]
+    assert res["final_n_accepted"] == fin["n_accepted"]
+    assert res["overlap"] == fin["n_accepted"] / len(c.source)
     ref = oracle_mod.icp_align(ot, c.source, c.max_iter, c.eps, dmax)
-    # independent end-to-end runs: the same transform; the iteration count may
-    # differ by one when |delta mse| lands within rounding of eps
+    # independent end-to-end runs: the same transform.  The iteration count
+    # may differ by one when |delta mse| lands within rounding of eps; the
+    # library's transform is then compared with the oracle run for exactly the
+    # library's number of iterations.
     assert abs(res["iters"] - ref["iters"]) <= 1
-    if res["iters"] == ref["iters"]:
-        check_transform(res["T"], ref["T"], c.extent)
-        assert abs(res["final_mse"] - ref["final_mse"]) <= 1e-5 * ref["final_mse"]
+    if res["iters"] != ref["iters"]:
+        ref = oracle_mod.icp_align(ot, c.source, res["iters"], 0.0, dmax)
+        assert ref["iters"] == res["iters"]
+    check_transform(res["T"], ref["T"], c.extent)
+    # when both transforms round to the same float32 (R, t) the final passes
+    # are the same computation on both sides
+    if all(np.array_equal(a, b) for a, b in zip(oracle_mod.as_kernel_rt(res["T"]),
+                                                oracle_mod.as_kernel_rt(ref["T"]))):
+        assert abs(res["final_mse"] - ref["final_mse"]) <= 1e-6 * ref["final_mse"]
     R = res["T"][:3, :3]
     np.testing.assert_allclose(R.T @ R, np.eye(3), atol=1e-12)
     assert abs(np.linalg.det(R) - 1) < 1e-12
+
+
+def test_overlap_ratio_and_warning(nn, oracle_mod):
+    """Page section 6: warn when the overlap after registration is below 80%.
+    Overlap = pairs accepted under the returned transform / source points.
+    The scene registration overlaps fully; the LiDAR scans (25% of each
+    sector unseen by the other, returns thinning out with range beyond the
+    0.5 m gate) stay near one half, and the call warns."""
+    import warnings
+    c = W.scene_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    with warnings.catch_warnings():
+        warnings.simplefilter("error", nn.LowOverlapWarning)
+        res = nn.icp_align(t, dev(c.source), c.max_iter, c.eps, c.max_corr_dist[0])
+    assert res["overlap"] >= nn.OVERLAP_WARN_RATIO and not res["low_overlap"]
+    c = W.lidar_case()
+    t, ot = setup(nn, oracle_mod, c)
+    with pytest.warns(nn.LowOverlapWarning):
+        res = nn.icp_align(t, dev(c.source), c.max_iter, c.eps, c.max_corr_dist[0])
+    assert res["low_overlap"] and res["overlap"] < nn.OVERLAP_WARN_RATIO
+    fin = oracle_mod.icp_step(ot, c.source, res["T"], c.max_corr_dist[0])
+    assert res["final_n_accepted"] == fin["n_accepted"]
+    b = nn.icp_align_batch(t, [dev(c.source)], c.max_iter, c.eps, c.max_corr_dist[0])
+    assert b["final_n_accepted"][0] == res["final_n_accepted"]
 
 
 def _residual_case(name):
@@ -333,27 +371,67 @@ def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip):
         nn.probe_delay_commands(-1, 1, 0)
 
 
-def test_large_coarse_to_fine(nn, oracle_mod):
-    """4M target / 2M source, two stages (2.0 m then 0.3 m).  The first pass of
-    each stage is compared on a 20k-point source sample (the oracle's search is
-    slow far from alignment); the last pass of each stage on the whole source:
-    same pairs, same mse, and a solve landing on the library's result."""
-    c = W.large_case()
-    t, ot = setup(nn, oracle_mod, c)
+@pytest.mark.parametrize("skip", [0, 4])
+def test_registration_survives_a_stalled_host(nn, skip):
+    """Fault injected on the host: between queuing pass k+1 and reading pass
+    k the host sleeps 250 ms, beyond twice the 50 ms command wait (as when the
+    host thread is descheduled, or a profiler serialises the launches).  Pass
+    k has published, pass k+1 gives up waiting; pass k's result must still be
+    read, pass k+1 run again as an ordinary launch, and the registration end
+    bit-identical to one that never pre-launched."""
+    import time
+    c = W.scene_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    src = dev(c.source)
+    dmax = c.max_corr_dist[0]
+    ref = nn.icp_align(t, src, 12, 0.0, dmax, trace=True, prelaunch=False)
+    nn.probe_delay_collect(skip, 1, 250_000_000)
+    try:
+        t0 = time.perf_counter()
+        res = nn.icp_align(t, src, 12, 0.0, dmax, trace=True)
+        elapsed = time.perf_counter() - t0
+    finally:
+        nn.probe_delay_collect(0, 0, 0)
+    assert elapsed > 0.25
+    np.testing.assert_array_equal(res["T"], ref["T"])
+    assert res["iters"] == ref["iters"] and res["final_mse"] == ref["final_mse"]
+    assert [r["mse"] for r in res["trace"]] == [r["mse"] for r in ref["trace"]]
+    assert [r["n_accepted"] for r in res["trace"]] == [r["n_accepted"] for r in ref["trace"]]
+    again = nn.icp_align(t, src, 12, 0.0, dmax)   # the next registration pre-launches again
+    np.testing.assert_array_equal(again["T"], ref["T"])
+
+
+def test_large_coarse_to_fine(nn, oracle_mod, large_oracle):
+    """4M target / 2M source, two stages (2.0 m then 0.3 m), at full size.
+    The first pass of each stage and its last pass are compared over the whole
+    2M-point source: per-point indices and distances bit-identical, same
+    accepted count and mse, moments within tolerance, and the oracle's solve
+    from the last pass lands on the library's result.  (The oracle's searches
+    are split over the host cores; each query's search is unchanged.)"""
+    c = large_oracle["case"]
+    ot = large_oracle["tree"]
+    workers = large_oracle["workers"]
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
     src_d = dev(c.source)
-    rng = np.random.default_rng(77)
-    sub = np.ascontiguousarray(c.source[np.sort(rng.choice(len(c.source), 20_000, replace=False))])
     T = None
     for dmax in c.max_corr_dist:
         res = nn.icp_align(t, src_d, c.max_iter, c.eps, dmax, init_T=T, trace=True)
-        T0 = res["trace"][0]["T"]
-        m, idx, d2 = lib_step(nn, t, sub, T0, dmax)
-        st = oracle_mod.icp_step(ot, sub, T0, dmax)
-        np.testing.assert_array_equal(idx, st["idx"])
-        np.testing.assert_array_equal(d2.view(np.uint32), st["d2"].view(np.uint32))
-        check_moments(m, st, c.extent)
-        _trace_parity(nn, oracle_mod, c, t, ot, c.source, dmax, res,
-                      sample_iters=[len(res["trace"]) - 1])
+        tr = res["trace"]
+        for k in sorted({0, len(tr) - 1}):
+            Tk = tr[k]["T"]
+            m, idx, d2 = lib_step(nn, t, c.source, Tk, dmax)
+            # the first pass evaluates the identity: the raw source's neighbours
+            pre = large_oracle["identity_nn"] if np.array_equal(Tk, np.eye(4)) else None
+            st = oracle_mod.icp_step(ot, c.source, Tk, dmax, workers=workers, nn=pre)
+            np.testing.assert_array_equal(idx, st["idx"])
+            np.testing.assert_array_equal(d2.view(np.uint32), st["d2"].view(np.uint32))
+            check_moments(m, st, c.extent)
+            assert tr[k]["n_accepted"] == st["n_accepted"]
+            assert abs(tr[k]["mse"] - st["mse"]) <= 1e-6 * st["mse"]
+            if k == len(tr) - 1:
+                check_transform(res["T"], oracle_mod.solve_from_step(st, c.source, ot), c.extent)
         T = res["T"]
     assert abs(np.linalg.det(T[:3, :3]) - 1) < 1e-12
 

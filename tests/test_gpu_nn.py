@@ -183,17 +183,15 @@ def test_full_workloads_every_query(nn, oracle_mod, name):
         assert_nn_equal(*gpu_nn(nn, t, q, flags), i_o, d_o)
 
 
-def test_large_workload_sampled(nn, oracle_mod):
-    """4M-point target, 2M queries: all GPU results, oracle on a 100k sample."""
-    c = W.large_case()
+def test_large_workload_every_query(nn, large_oracle):
+    """4M-point target, all 2M queries, both query orders, against the oracle."""
+    c = large_oracle["case"]
     t = make_tree(nn, c.target, c.leaf_size)
-    idx, d2 = gpu_nn(nn, t, c.source, 1)
-    rng = np.random.default_rng(55)
-    sample = np.sort(rng.choice(len(c.source), 100_000, replace=False))
-    ot = oracle_mod.KDTree(c.target, c.leaf_size)
-    i_o, d_o = ot.query(c.source[sample])
-    assert_nn_equal(idx[sample], d2[sample], i_o, d_o)
-    assert (idx >= 0).all() and np.isfinite(d2).all()
+    i_o, d_o = large_oracle["identity_nn"]
+    for flags in (0, 1):
+        idx, d2 = gpu_nn(nn, t, c.source, flags)
+        assert_nn_equal(idx, d2, i_o, d_o)
+    assert (i_o >= 0).all() and np.isfinite(d_o).all()
 
 
 @pytest.mark.parametrize("name", ["grid", "clustered", "line"])

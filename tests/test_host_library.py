@@ -195,14 +195,15 @@ def test_kabsch_degenerate(lib):
 
 def test_probe_entry_points_check_arguments_without_a_device(lib):
     """The test helpers behind the pre-launched passes validate on the host:
-    the command-delay injector takes its settings (and is switched off
-    again), the command-wait probe needs an uploaded tree."""
-    for bad in ((-1, 1, 0), (0, -1, 0), (0, 1, 10_000_000_001)):
-        with pytest.raises(lib.IcpnnError) as e:
-            lib.probe_delay_commands(*bad)
-        assert e.value.status == "INVALID_ARG"
-    lib.probe_delay_commands(2, 1, 1000)
-    lib.probe_delay_commands(0, 0, 0)
+    the command-delay and collect-delay injectors take their settings (and
+    are switched off again), the command-wait probe needs an uploaded tree."""
+    for probe in (lib.probe_delay_commands, lib.probe_delay_collect):
+        for bad in ((-1, 1, 0), (0, -1, 0), (0, 1, 10_000_000_001)):
+            with pytest.raises(lib.IcpnnError) as e:
+                probe(*bad)
+            assert e.value.status == "INVALID_ARG"
+        probe(2, 1, 1000)
+        probe(0, 0, 0)
     t = lib.kdtree_build(W.uniform_cloud(100, 3), 8)
     with pytest.raises(lib.IcpnnError) as e:
         lib.probe_command_wait(t, W.uniform_cloud(10, 4), 1_000_000, 0)
