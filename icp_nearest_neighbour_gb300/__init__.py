@@ -23,7 +23,7 @@ __all__ = [
     "IcpnnError", "KDTree", "Moments", "IterRecord", "load", "kdtree_build", "kdtree_upload",
     "kdtree_free", "kdtree_info", "kdtree_export", "nn_query", "icp_step", "icp_step_noalloc",
     "kabsch", "icp_align", "icp_align_batch", "voxel_downsample",
-    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "NO_PRELAUNCH", "MAX_DEPTH",
+    "last_error", "launch_count", "MORTON_SORT", "TRACE_TIMING", "RESIDUAL_REJECT", "NO_PRELAUNCH", "NO_PERSISTENT", "MAX_DEPTH",
     "NOALLOC_MAX_POINTS", "OVERLAP_WARN_RATIO", "LowOverlapWarning",
 ]
 
@@ -32,6 +32,7 @@ TRACE_TIMING = 2
 RESIDUAL_REJECT = 4
 SPLIT_ROUND_ROBIN = 8
 NO_PRELAUNCH = 16
+NO_PERSISTENT = 32
 MAX_DEPTH = 20
 NOALLOC_MAX_POINTS = 1 << 20
 OVERLAP_WARN_RATIO = 0.8
@@ -354,11 +355,14 @@ def _overlap(n_accepted: int, n: int, warn: bool) -> dict:
 
 def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float = float("inf"),
               init_T=None, trace: bool = False, timing: bool = False, residual_reject: bool = False,
-              prelaunch: bool = True, warn_overlap: bool = True, stream=None) -> dict:
+              prelaunch: bool = True, persistent: bool = True, warn_overlap: bool = True,
+              stream=None) -> dict:
     """Register src onto the tree's points; returns dict(T, final_mse, iters,
     final_n_accepted, overlap, low_overlap, trace).
     residual_reject adds the 3-sigma residual rejection and re-solve to every iteration;
-    prelaunch=False launches each pass only after its transform is solved.
+    by default the registration runs as one persistent kernel; persistent=False
+    pre-launches the passes one at a time instead, and prelaunch=False launches
+    each pass only after its transform is solved (the results are the same bits).
     overlap = final_n_accepted / n; below OVERLAP_WARN_RATIO a LowOverlapWarning is
     issued (unless warn_overlap=False), as the page's section 6 advises."""
     T = np.zeros(16)
@@ -372,7 +376,7 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
     cap = int(max_iter) if (trace or timing) else 0
     recs = (IterRecord * max(cap, 1))()
     flags = ((TRACE_TIMING if timing else 0) | (RESIDUAL_REJECT if residual_reject else 0)
-             | (0 if prelaunch else NO_PRELAUNCH))
+             | (0 if prelaunch else NO_PRELAUNCH) | (0 if persistent else NO_PERSISTENT))
     _check(load().icpnn_icp_align(tree.handle, _ptr(src, np.float32, 3, "src"), int(src.shape[0]),
                                   int(max_iter), float(eps), float(max_corr_dist), init,
                                   ctypes.c_void_p(T.ctypes.data), ctypes.byref(fmse), ctypes.byref(iters),

@@ -126,9 +126,18 @@ thread_local MappedBuffer tl_mapped;
 //   [0, kMomentSlots + 1]                      a pass's result, its publish word, its abort word
 //   [kSecondSlot, kSecondSlot + kMomentSlots + 1]  the other residual pass's result and words
 //   [kCommandOffset, + sizeof(PassCommand))    the host-written command of pre-launched passes
+//   [kTaggedOffset, + sizeof(TaggedCommand))   the host-written commands of the persistent kernel
+// A result slot holds the 18 moments, the publish word, the abort word and
+// (persistent kernel) the pass's start and end global times.
 constexpr int kSecondSlot = 32;
 constexpr int kCommandOffset = 64;
+constexpr int kTaggedOffset = 80;
 constexpr int kMappedDoubles = 96;
+static_assert(kSecondSlot >= kMomentSlots + 4, "result slot: moments + 4 words");
+static_assert(kTaggedOffset * sizeof(double) >= kCommandOffset * sizeof(double) + sizeof(PassCommand) &&
+                  kTaggedOffset * sizeof(double) + sizeof(TaggedCommand) <= kMappedDoubles * sizeof(double) &&
+                  (kTaggedOffset * sizeof(double)) % 16 == 0,
+              "tagged command block must fit the mapped buffer after the pass command");
 static_assert(kSecondSlot > kMomentSlots + 1 && kCommandOffset > kSecondSlot + kMomentSlots + 1,
               "mapped-buffer regions must not overlap");
 static_assert(kCommandOffset * sizeof(double) + sizeof(PassCommand) <= kMappedDoubles * sizeof(double),
@@ -298,6 +307,7 @@ struct Pass {
   double* partials = nullptr;
   uint32_t* counter = nullptr;
   CommandMirror* mirror = nullptr;  // device, zeroed: pre-launched passes' command copy
+  TaggedMirror* tmirror = nullptr;  // device, zeroed: the persistent kernel's command copy
   MappedBuffer* mb = nullptr;
   int32_t* slot_of = nullptr;  // per Morton-ordered source record: matched slot or -1
   uint32_t* leaf_of = nullptr; // per source record: leaf of the last best match (warm start)
@@ -326,6 +336,8 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
   ICPNN_CUDA(cudaMemsetAsync(ps->counter, 0, static_cast<size_t>(counter_words) * sizeof(uint32_t), s));
   ICPNN_CUDA(sc.alloc(&ps->mirror, 1));
   ICPNN_CUDA(cudaMemsetAsync(ps->mirror, 0, sizeof(CommandMirror), s));
+  ICPNN_CUDA(sc.alloc(&ps->tmirror, 1));
+  ICPNN_CUDA(cudaMemsetAsync(ps->tmirror, 0, sizeof(TaggedMirror), s));
   if (int rc = mapped_buffer(&ps->mb)) return rc;
   for (int d = 0; d < 3; ++d) ps->shift_q[d] = 0.5f * (t->bbox_lo[d] + t->bbox_hi[d]);
   ps->max_d2 = rejection_threshold(dmax);
@@ -435,6 +447,45 @@ void pass_command(const Pass& ps, unsigned long long seq, const float* R, const 
   }
   __atomic_store_n(&c->word, (seq << 1) | (R == nullptr ? 1ull : 0ull), __ATOMIC_RELEASE);
 }
+
+TaggedCommand* tagged_block(const MappedBuffer* mb) {
+  return reinterpret_cast<TaggedCommand*>(mb->host + kTaggedOffset);
+}
+
+// Hand pass `seq` of the persistent kernel its transform, or (R == nullptr)
+// tell the kernel to leave.  Every word carries the pass's tag; the control
+// word is stored last, with release order.
+void tagged_command(const MappedBuffer* mb, unsigned long long seq, const float* R, const float* tr) {
+  if (R != nullptr && tl_cmd_delayed > 0) {
+    if (tl_cmd_skip > 0) {
+      --tl_cmd_skip;
+    } else {
+      --tl_cmd_delayed;
+      std::this_thread::sleep_for(std::chrono::nanoseconds(tl_cmd_delay_ns));
+    }
+  }
+  TaggedCommand* c = tagged_block(mb);
+  if (R != nullptr) {
+    const unsigned long long high = (seq & 0xffffffffull) << 32;
+    for (int j = 0; j < 12; ++j) {
+      uint32_t bits;
+      std::memcpy(&bits, j < 9 ? &R[j] : &tr[j - 9], sizeof(bits));
+      __atomic_store_n(&c->words[j], high | bits, __ATOMIC_RELAXED);
+    }
+  }
+  __atomic_store_n(&c->ctrl, (seq << 2) | (R == nullptr ? 1ull : 0ull), __ATOMIC_RELEASE);
+}
+
+// A running persistent kernel; told to leave when the owner leaves early.
+struct PersistentRun {
+  const MappedBuffer* mb = nullptr;
+  bool active = false;
+  void stop() {
+    if (active) tagged_command(mb, mb->seq + 1, nullptr, nullptr);
+    active = false;
+  }
+  ~PersistentRun() { stop(); }
+};
 
 // A pre-launched pass that has no transform yet; stopped when the owner
 // leaves early, so that its blocks return at once.
@@ -871,7 +922,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_align: max_corr_dist is NaN");
   if (trace_cap < 0 || (trace_cap > 0 && trace == nullptr))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_align: bad trace buffer");
-  if (flags & ~(ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH))
+  if (flags & ~(ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH | ICPNN_NO_PERSISTENT))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_align: unknown flag");
   const bool residual = (flags & ICPNN_RESIDUAL_REJECT) != 0;
   // the residual passes run between a pass and the next one's transform, so
@@ -885,13 +936,36 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   } else {
     for (int k = 0; k < 16; ++k) T[k] = (k % 5 == 0) ? 1.0 : 0.0;
   }
-  cudaEvent_t* ev = nullptr;
-  const int32_t timed = (flags & ICPNN_TRACE_TIMING) ? std::min(trace_cap, max_iter) : 0;
-  if (timed > 0)
-    if (int rc = timing_events(2 * static_cast<size_t>(timed), &ev)) return rc;
   Scratch sc(s);
   Pass ps;
   if (int rc = pass_setup(t, src, n_src, max_corr_dist, residual, true, s, sc, &ps)) return rc;
+
+  // Default: the whole registration as one persistent kernel; else passes
+  // pre-launched one at a time (ICPNN_NO_PERSISTENT, or a grid that cannot be
+  // resident at once), else ordinary launches.
+  PersistentRun run;
+  run.mb = ps.mb;
+  if (prelaunch && (flags & ICPNN_NO_PERSISTENT) == 0 && registration_kernel_fits(*t, ps.grid)) {
+    IcpPassParams p = pass_params(ps);
+    --ps.mb->seq;  // pass_params took a number; the first pass uses it below
+    p.wait_ns = kCommandWaitNs;
+    const TaggedCommand* dev_cmd = reinterpret_cast<const TaggedCommand*>(ps.mb->dev + kTaggedOffset);
+    const cudaError_t e = launch_registration(*ps.tree, ps.src.recs, ps.n, p, dev_cmd,
+                                              ps.tmirror, ps.partials, ps.counter, ps.mb->dev, ps.slot_of,
+                                              ps.leaf_of, ps.grid, s);
+    if (e == cudaSuccess) {
+      run.active = true;
+      prelaunch = false;
+    } else if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
+      cudaGetLastError();
+    } else {
+      return fail(ICPNN_ERR_CUDA, std::string("icp_align: persistent kernel launch: ") + cudaGetErrorString(e));
+    }
+  }
+  cudaEvent_t* ev = nullptr;
+  const int32_t timed = (flags & ICPNN_TRACE_TIMING) ? std::min(trace_cap, max_iter) : 0;
+  if (timed > 0 && !run.active)
+    if (int rc = timing_events(2 * static_cast<size_t>(timed), &ev)) return rc;
 
   // Pre-launched passes: `cur` evaluates T; `next` is queued behind it
   // before its result is read and gets the solved transform as its command.
@@ -931,13 +1005,44 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     return pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, m);
   };
 
+  // The persistent kernel's pass under T: command, wait, read.  If the kernel
+  // gave up waiting (a profiler that serialises launches, a host thread
+  // descheduled for the whole wait) it is told to leave, the counters it may
+  // have left behind are cleared, and the pass and the rest of the
+  // registration run as ordinary launches.  *pass_ms: the pass's device time
+  // (command seen to result published), 0 after a fallback.
+  const volatile unsigned long long* flag0 =
+      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
+  auto persistent_pass = [&](icpnn_moments* m, float* pass_ms) -> int {
+    float R32[9], t32[3];
+    transform_to_f32(T, R32, t32);
+    const unsigned long long seq = ++ps.mb->seq;
+    tagged_command(ps.mb, seq, R32, t32);
+    injected_collect_delay();
+    bool aborted = false;
+    if (int rc = wait_published(flag0, seq, s, &aborted)) return rc;
+    if (!aborted) {
+      read_moments(ps, m);
+      const unsigned long long t0 = flag0[2], t1 = flag0[3];
+      *pass_ms = t1 > t0 ? static_cast<float>(static_cast<double>(t1 - t0) * 1e-6) : 0.f;
+      return ICPNN_OK;
+    }
+    run.stop();
+    ICPNN_CUDA(cudaMemsetAsync(ps.counter, 0, static_cast<size_t>(reduction_counter_words(ps.grid)) * sizeof(uint32_t), s));
+    *pass_ms = 0.f;
+    return pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, m);
+  };
+
   double mse_hist[3] = {0, 0, 0};
   int32_t done = 0;
   for (int32_t k = 0; k < max_iter; ++k) {
     float R32[9], t32[3];
     transform_to_f32(T, R32, t32);
     icpnn_moments m;
-    if (prelaunch) {
+    float pass_ms = 0.f;
+    if (run.active) {
+      if (int rc = persistent_pass(&m, &pass_ms)) return rc;
+    } else if (prelaunch) {
       const bool time_next = k + 1 < timed;
       if (int rc = collect(true, time_next ? ev[2 * k + 2] : nullptr, time_next ? ev[2 * k + 3] : nullptr, &m))
         return rc;
@@ -979,7 +1084,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       r.mse = m.mse;
       r.sigma2 = sigma2;
       std::memcpy(r.T, T, sizeof(T));
-      r.kernel_ms = 0.f;
+      r.kernel_ms = pass_ms;
       r.reserved = 0.f;
     }
     std::memcpy(T, Tn, sizeof(T));
@@ -997,7 +1102,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     if (k >= 2 && std::fabs(mse_hist[1] - mse_hist[2]) < eps && std::fabs(mse_hist[0] - mse_hist[1]) < eps)
       break;
   }
-  if (timed > 0) {
+  if (timed > 0 && ev != nullptr) {
     const int32_t recorded = std::min(timed, done);
     ICPNN_CUDA(cudaEventSynchronize(ev[2 * (recorded - 1) + 1]));
     for (int32_t k = 0; k < recorded; ++k) ICPNN_CUDA(cudaEventElapsedTime(&trace[k].kernel_ms, ev[2 * k], ev[2 * k + 1]));
@@ -1005,7 +1110,11 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   float R32[9], t32[3];
   transform_to_f32(T, R32, t32);
   icpnn_moments fin;
-  if (prelaunch) {
+  if (run.active) {
+    float ms = 0.f;
+    if (int rc = persistent_pass(&fin, &ms)) return rc;
+    run.stop();
+  } else if (prelaunch) {
     if (int rc = collect(false, nullptr, nullptr, &fin)) return rc;
   } else {
     if (int rc = pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, &fin)) return rc;

@@ -818,12 +818,35 @@ constexpr unsigned int kSkipStopped = 1u, kSkipTimedOut = 1u << 16;
 constexpr unsigned int kSingleLevelBlocks = 4 * kGroupBlocks;
 static_assert(kGroupBlocks * kMomentSlots <= kThreads, "one thread per partial of a group");
 
-template <bool kPublish>
+// Release-only increment: orders this thread's earlier stores before the
+// increment without the acquire half, which would invalidate the SM's L1 (a
+// persistent kernel keeps the tree in L1 from one pass to the next).
+__device__ __forceinline__ unsigned int atom_add_release_gpu(unsigned int* a, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// kPersistent: the block's stores to partials are made by thread 0, which
+// then increments the counters with release atomics; only a block that finds
+// itself last takes the acquire fence.  The sums are the same in the same
+// order either way.  *t_start (if given) is the global time at which the pass
+// received its command; the last block stores it and the publish time in the
+// two words after the abort word.
+template <bool kPublish, bool kPersistent = false>
 __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
                                                double* __restrict__ partials,
                                                unsigned int* __restrict__ counter, double* out,
                                                unsigned long long seq, float* thr_out = nullptr,
-                                               unsigned int skipped = 0u) {
+                                               unsigned int skipped = 0u,
+                                               const unsigned long long* t_start = nullptr) {
   __shared__ double s_warp[kThreads / 32][kMomentSlots];
   __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
   __shared__ bool s_last;
@@ -844,16 +867,27 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   __syncthreads();
   // every thread of the block is past its search: a kernel launched as a
   // programmatic dependent of this one may start once all blocks are here
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!kPersistent) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x < kMomentSlots) {
     double s = 0.0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
-    partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
+    if (kPersistent)
+      s_fin[0][threadIdx.x] = s;
+    else
+      partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
   }
-  if (threadIdx.x == 0 && skipped != 0u) atomicAdd(counter + 1, skipped);
-  __threadfence();
+  if (!kPersistent) {
+    if (threadIdx.x == 0 && skipped != 0u) atomicAdd(counter + 1, skipped);
+    __threadfence();
+  }
   __syncthreads();
+  if (kPersistent && threadIdx.x == 0) {
+#pragma unroll
+    for (int v = 0; v < kMomentSlots; ++v)
+      partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + v] = s_fin[0][v];
+    if (skipped != 0u) atomicAdd(counter + 1, skipped);
+  }
   const int r = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
   // rows of partials the final block adds: every block's (one level) or every
   // group's sum, stored over the group's first partial (two levels)
@@ -861,10 +895,17 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   if (gridDim.x > kSingleLevelBlocks) {
     const unsigned int group = blockIdx.x / kGroupBlocks, g0 = group * kGroupBlocks;
     const unsigned int in_group = min(static_cast<unsigned int>(kGroupBlocks), gridDim.x - g0);
-    if (threadIdx.x == 0) s_last = (atomicAdd(counter + 2 + group, 1u) == in_group - 1);
+    if (threadIdx.x == 0)
+      s_last = ((kPersistent ? atom_add_release_gpu(counter + 2 + group, 1u)
+                             : atomicAdd(counter + 2 + group, 1u)) == in_group - 1);
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
+    if (kPersistent) {
+      if (threadIdx.x == 0) fence_acq_rel_gpu();
+      __syncthreads();
+    } else {
+      __threadfence();
+    }
     if (threadIdx.x < kGroupBlocks * kMomentSlots)
       s_fin[r][v] = static_cast<unsigned int>(r) < in_group
                         ? __ldcg(&partials[static_cast<int64_t>(g0 + r) * kMomentSlots + v]) : 0.0;
@@ -872,18 +913,34 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     if (threadIdx.x < kMomentSlots) {
       double s = 0.0;
       for (unsigned int k = 0; k < in_group; ++k) s += s_fin[k][threadIdx.x];
-      partials[static_cast<int64_t>(g0) * kMomentSlots + threadIdx.x] = s;
+      if (kPersistent)
+        s_warp[0][threadIdx.x] = s;
+      else
+        partials[static_cast<int64_t>(g0) * kMomentSlots + threadIdx.x] = s;
     }
-    if (threadIdx.x == 0) counter[2 + group] = 0u;
-    __threadfence();
+    if (!kPersistent) {
+      if (threadIdx.x == 0) counter[2 + group] = 0u;
+      __threadfence();
+    }
     __syncthreads();
+    if (kPersistent && threadIdx.x == 0) {
+#pragma unroll
+      for (int u = 0; u < kMomentSlots; ++u) partials[static_cast<int64_t>(g0) * kMomentSlots + u] = s_warp[0][u];
+      atomicExch(counter + 2 + group, 0u);
+    }
     rows = (gridDim.x + kGroupBlocks - 1) / kGroupBlocks;
     row_stride = kGroupBlocks;
   }
-  if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == rows - 1);
+  if (threadIdx.x == 0)
+    s_last = ((kPersistent ? atom_add_release_gpu(counter, 1u) : atomicAdd(counter, 1u)) == rows - 1);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
+  if (kPersistent) {
+    if (threadIdx.x == 0) fence_acq_rel_gpu();
+    __syncthreads();
+  } else {
+    __threadfence();
+  }
   constexpr int kGroups = kThreads / kMomentSlots;
   if (threadIdx.x < kGroups * kMomentSlots) {
     // rows r, r + 14, ... in order, up to four loads in flight
@@ -913,7 +970,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // orders its own stores, the sequence word: the host never sees the new
   // sequence before the values.
   if (threadIdx.x == 0) {
-    *counter = 0u;
+    if (kPersistent)
+      atomicExch(counter, 0u);
+    else
+      *counter = 0u;
     const unsigned int skips = atomicExch(counter + 1, 0u);
     if (skips != 0u) {
       // The abort marker has a word of its own: the pass queued behind this
@@ -933,6 +993,11 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
       *thr_out = float_threshold_dev(9.0 * sigma2);
     }
     if (kPublish) {
+      if (t_start != nullptr) {
+        unsigned long long* tw = reinterpret_cast<unsigned long long*>(out + kMomentSlots + 2);
+        tw[0] = __ldcg(t_start);
+        tw[1] = global_ns();
+      }
       __threadfence_system();
       *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq;
     }
@@ -940,6 +1005,31 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
 }
 
 // Accumulate one accepted pair (original source s, matched target q).
+//
+// Precision of the sums.  Each thread adds its pairs' moments in float32, a
+// warp adds its 32 lanes in a five-level float32 butterfly, and everything
+// above (warps, blocks, groups) is added in double.  A thread sums at most
+// k = ceil(n / resident threads) pairs (1 on the 100k scene, 18 on the 2M
+// source), so a float32 partial carries an error of at most
+// gamma_(k+4) * sum |terms| with gamma_m = m u / (1 - m u), u = 2^-24: for
+// k = 18 about 1.3e-6 of the absolute sum, which the double levels then
+// preserve.  The centroids and H are compared with 1e-5 bounds, which this
+// meets with room for the cancellation between the shifted second moments
+// and the product of the means.  The distance sum (acc[15], whose mean is
+// compared at 1e-6) is kept compensated per thread instead: the rounding
+// error of each addition is recovered exactly (TwoSum) and carried in a
+// second float, folded in before the butterfly, which leaves at most
+// about (1 + gamma_5) u ~ 3.6e-7 of it.  (Doubles from the thread level up
+// would cost the FP64 pipe, about 4 operations per clock per SM on this part,
+// 16 values x 5 butterfly levels per lane on every pass's critical tail.)
+__device__ __forceinline__ void add_compensated(float& sum, float& err, float x) {
+  const float s = __fadd_rn(sum, x);
+  const float xv = __fsub_rn(s, sum);
+  const float sv = __fsub_rn(s, xv);
+  err = __fadd_rn(err, __fadd_rn(__fsub_rn(sum, sv), __fsub_rn(x, xv)));
+  sum = s;
+}
+
 __device__ __forceinline__ void add_pair(float (&acc)[16], float sx, float sy, float sz,
                                          const float4& qr, float d2, const IcpPassParams& p) {
   const float ds[3] = {__fsub_rn(sx, p.shift_s[0]), __fsub_rn(sy, p.shift_s[1]),
@@ -953,7 +1043,7 @@ __device__ __forceinline__ void add_pair(float (&acc)[16], float sx, float sy, f
 #pragma unroll
     for (int c = 0; c < 3; ++c) acc[6 + 3 * a + c] = __fadd_rn(acc[6 + 3 * a + c], __fmul_rn(ds[a], dq[c]));
   }
-  acc[15] = __fadd_rn(acc[15], d2);
+  (void)d2;
 }
 
 // p = R s + t, each row ((R_a0 s_x + R_a1 s_y) + R_a2 s_z) + t_a; rt holds R
@@ -975,12 +1065,6 @@ __device__ __forceinline__ void transform_point(const IcpPassParams& p, float sx
     v = __fadd_rn(v, __fmul_rn(p.R[3 * a + 2], sz));
     q[a] = __fadd_rn(v, p.t[a]);
   }
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // Polls use relaxed loads (an acquire load would invalidate the SM's L1 on
@@ -1075,6 +1159,61 @@ __device__ __forceinline__ unsigned int await_command(const IcpPassParams& p, fl
   return outcome == kRun ? 0u : outcome == kStop ? kSkipStopped : kSkipTimedOut;
 }
 
+// The work of one pass for this thread: its queries (chunks of 32 consecutive
+// source records per warp, see first_chunk) transformed by rt, searched,
+// tested against the rejection threshold and added to the thread's moments.
+// Shared by the per-pass kernel and the persistent registration kernel, so
+// both compute the same bits.
+template <bool kPerPoint, bool kSlot>
+__device__ __forceinline__ void pass_chunks(const TreeView& tv, const float* rt, const float4* __restrict__ src,
+                                            int64_t n_run, int64_t n, const IcpPassParams& p,
+                                            int32_t* __restrict__ out_idx, float* __restrict__ out_d2,
+                                            int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of,
+                                            float (&acc)[16], uint32_t& n_acc, uint32_t& n_bad) {
+  float d2_err = 0.f;  // compensation of the distance sum acc[15]
+  for (int64_t c = first_chunk(); c * 32 < n_run; c += chunk_stride()) {
+    const int64_t i = c * 32 + (threadIdx.x & 31);
+    if (i >= n) continue;
+    const float4 s = src[i];
+    const int32_t slot = __float_as_int(s.w);
+    int32_t idx = -1, matched = -1;
+    float d2 = __int_as_float(0x7fc00000);
+    if (!finite3(s.x, s.y, s.z)) {
+      ++n_bad;
+    } else {
+      float q[3];
+      transform_point(rt, s.x, s.y, s.z, q);
+      if (finite3(q[0], q[1], q[2])) {
+        // Without per-point outputs only accepted pairs matter, so the search
+        // starts with the rejection radius as its best distance (the page's
+        // section 4.4 fuses max_dist into the tree query): it returns the
+        // exact nearest point when one lies within the radius, else nothing.
+        Best b = make_best(kPerPoint ? __int_as_float(0x7f800000) : p.max_d2);
+        if (leaf_of != nullptr) {
+          const uint32_t prev = leaf_of[i];
+          leaf_of[i] = search_from(tv, q[0], q[1], q[2], b, prev);
+        } else {
+          search(tv, q[0], q[1], q[2], b);
+        }
+        idx = b.idx() == INT_MAX ? -1 : b.idx();
+        d2 = b.d2();
+        if (b.idx() != INT_MAX && b.d2() <= p.max_d2) {
+          ++n_acc;
+          matched = static_cast<int32_t>(b.slot);
+          add_pair(acc, s.x, s.y, s.z, __ldg(&tv.pts[b.slot]), b.d2(), p);
+          add_compensated(acc[15], d2_err, b.d2());
+        }
+      }
+    }
+    if (kPerPoint) {
+      out_idx[slot] = idx;
+      out_d2[slot] = d2;
+    }
+    if (kSlot) slot_of[i] = matched;
+  }
+  acc[15] = __fadd_rn(acc[15], d2_err);
+}
+
 // Three resident blocks per SM: without the bound the command wait makes
 // the register allocator settle on 64 registers and spill.
 template <bool kPerPoint, bool kSlot>
@@ -1111,47 +1250,126 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_kernel(
 #pragma unroll
   for (int v = 0; v < 16; ++v) acc[v] = 0.f;
   uint32_t n_acc = 0, n_bad = 0;
-
-  for (int64_t c = first_chunk(); c * 32 < n_run; c += chunk_stride()) {
-    const int64_t i = c * 32 + (threadIdx.x & 31);
-    if (i >= n) continue;
-    const float4 s = src[i];
-    const int32_t slot = __float_as_int(s.w);
-    int32_t idx = -1, matched = -1;
-    float d2 = __int_as_float(0x7fc00000);
-    if (!finite3(s.x, s.y, s.z)) {
-      ++n_bad;
-    } else {
-      float q[3];
-      transform_point(s_rt, s.x, s.y, s.z, q);
-      if (finite3(q[0], q[1], q[2])) {
-        // Without per-point outputs only accepted pairs matter, so the search
-        // starts with the rejection radius as its best distance (the page's
-        // section 4.4 fuses max_dist into the tree query): it returns the
-        // exact nearest point when one lies within the radius, else nothing.
-        Best b = make_best(kPerPoint ? __int_as_float(0x7f800000) : p.max_d2);
-        if (leaf_of != nullptr) {
-          const uint32_t prev = leaf_of[i];
-          leaf_of[i] = search_from(tv, q[0], q[1], q[2], b, prev);
-        } else {
-          search(tv, q[0], q[1], q[2], b);
-        }
-        idx = b.idx() == INT_MAX ? -1 : b.idx();
-        d2 = b.d2();
-        if (b.idx() != INT_MAX && b.d2() <= p.max_d2) {
-          ++n_acc;
-          matched = static_cast<int32_t>(b.slot);
-          add_pair(acc, s.x, s.y, s.z, __ldg(&pts[b.slot]), b.d2(), p);
-        }
-      }
-    }
-    if (kPerPoint) {
-      out_idx[slot] = idx;
-      out_d2[slot] = d2;
-    }
-    if (kSlot) slot_of[i] = matched;
-  }
+  pass_chunks<kPerPoint, kSlot>(tv, s_rt, src, n_run, n, p, out_idx, out_d2, slot_of, leaf_of, acc, n_acc, n_bad);
   reduce_moments<true>(acc, n_acc, n_bad, partials, counter, out, p.seq, nullptr, skipped);
+}
+
+// ------------------------------------------------ persistent registration
+
+__device__ __forceinline__ void store_relaxed_gpu(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(a), "l"(v) : "memory");
+}
+
+// Read the 12 tagged words at `a` into rt (two at a time); true if every tag
+// names the pass.
+template <bool kSystem>
+__device__ __forceinline__ bool load_tagged(const unsigned long long* a, uint32_t tag, float* rt) {
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 6; ++k) {
+    unsigned long long w0, w1;
+    if (kSystem)
+      asm volatile("ld.relaxed.sys.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a + 2 * k) : "memory");
+    else
+      asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a + 2 * k) : "memory");
+    ok = ok && static_cast<uint32_t>(w0 >> 32) == tag && static_cast<uint32_t>(w1 >> 32) == tag;
+    rt[2 * k] = __uint_as_float(static_cast<uint32_t>(w0));
+    rt[2 * k + 1] = __uint_as_float(static_cast<uint32_t>(w1));
+  }
+  return ok;
+}
+
+// One thread per block: wait until the tagged command names pass `seq` and
+// copy its R and t to rt.  Returns 0 (run), kSkipStopped (stop, or a later
+// pass named) or kSkipTimedOut.  The first block to arrive polls host memory
+// for at most wait_ns and forwards what it found through the mirror; the
+// others poll the mirror for at most 2 * wait_ns.  No acquire fence: a reader
+// re-reads the payload until all its tags name the pass (bounded).
+__device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, TaggedMirror* m,
+                                                     unsigned long long seq, unsigned long long wait_ns,
+                                                     float* rt) {
+  constexpr unsigned long long kRun = 0, kStop = 1, kTimeout = 2;
+  const uint32_t tag = static_cast<uint32_t>(seq);
+  const unsigned long long t0 = global_ns();
+  unsigned long long outcome = kTimeout;
+  if (atomicMax(&m->elect, seq) < seq) {
+    for (;;) {
+      const unsigned long long c = load_relaxed_sys(&cmd->ctrl);
+      const uint32_t ctag = static_cast<uint32_t>(c >> 2);
+      if (ctag == tag) {
+        outcome = c & 3ull;
+        if (outcome == kRun) {
+          while (!load_tagged<true>(cmd->words, tag, rt)) {
+            if (global_ns() - t0 > wait_ns) {
+              outcome = kTimeout;
+              break;
+            }
+          }
+        }
+        break;
+      }
+      if (static_cast<int32_t>(ctag - tag) > 0) {
+        outcome = kStop;
+        break;
+      }
+      if (global_ns() - t0 > wait_ns) break;
+      __nanosleep(200);
+    }
+    if (outcome == kRun) {
+      const unsigned long long high = static_cast<unsigned long long>(tag) << 32;
+#pragma unroll
+      for (int k = 0; k < 12; ++k) store_relaxed_gpu(&m->words[k], high | __float_as_uint(rt[k]));
+    }
+    store_relaxed_gpu(&m->t_cmd, global_ns());
+    store_relaxed_gpu(&m->ctrl, (seq << 2) | outcome);
+  } else {
+    for (;;) {
+      const unsigned long long c = load_relaxed_gpu(&m->ctrl);
+      if ((c >> 2) >= seq) {
+        outcome = (c >> 2) == seq ? (c & 3ull) : kStop;
+        if (outcome == kRun) {
+          while (!load_tagged<false>(m->words, tag, rt)) {
+            if (global_ns() - t0 > 2 * wait_ns) {
+              outcome = kTimeout;
+              break;
+            }
+          }
+        }
+        break;
+      }
+      if (global_ns() - t0 > 2 * wait_ns) break;
+      __nanosleep(100);
+    }
+  }
+  return outcome == kRun ? 0u : outcome == kStop ? kSkipStopped : kSkipTimedOut;
+}
+
+template <bool kSlot>
+__global__ void __launch_bounds__(kThreads, 3) icp_registration_kernel(
+    const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
+    int smem_slots, const float4* __restrict__ src, int64_t n, IcpPassParams p, const TaggedCommand* cmd,
+    TaggedMirror* mirror, double* __restrict__ partials, unsigned int* __restrict__ counter, double* out,
+    int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of) {
+  extern __shared__ __align__(16) uint2 s_nodes[];
+  __shared__ float s_rt[12];
+  __shared__ unsigned int s_skip;
+  stage_top(nodes, s_nodes, smem_slots);  // once for the whole registration
+  const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
+  for (unsigned long long seq = p.seq;; ++seq) {
+    if (threadIdx.x == 0) s_skip = await_tagged(cmd, mirror, seq, p.wait_ns, s_rt);
+    __syncthreads();
+    const unsigned int skipped = s_skip;
+    if (skipped == kSkipStopped) return;
+    float acc[16];
+#pragma unroll
+    for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+    uint32_t n_acc = 0, n_bad = 0;
+    if (skipped == 0u)
+      pass_chunks<false, kSlot>(tv, s_rt, src, n, n, p, nullptr, nullptr, slot_of, leaf_of, acc, n_acc, n_bad);
+    reduce_moments<true, true>(acc, n_acc, n_bad, partials, counter, out, seq, nullptr, skipped, &mirror->t_cmd);
+    if (skipped != 0u) return;  // gave up waiting: the pass reports its abort, this block leaves
+    __syncthreads();            // s_rt and s_skip are rewritten for the next pass
+  }
 }
 
 // Residual pass of the section 4.4 rejection: for every source record with a
@@ -1313,6 +1531,50 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+bool registration_kernel_fits(const icpnn_tree& t, int grid) {
+  const size_t smem = static_cast<size_t>(smem_slots_for(t)) * sizeof(uint2);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, icp_registration_kernel<false>, kThreads, smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  int per_sm_slot = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_slot, icp_registration_kernel<true>, kThreads, smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return static_cast<int64_t>(std::min(per_sm, per_sm_slot)) * num_sms() >= grid;
+}
+
+cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t n, const IcpPassParams& p,
+                                const TaggedCommand* cmd, TaggedMirror* mirror, double* partials,
+                                uint32_t* counter, double* out, int32_t* slot_of, uint32_t* leaf_of,
+                                int grid, cudaStream_t s) {
+  const int slots = smem_slots_for(t);
+  const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
+  const float4* boxes = reinterpret_cast<const float4*>(t.dev.boxes);
+  const float4* pts = reinterpret_cast<const float4*>(t.dev.points);
+  auto kernel = slot_of != nullptr ? icp_registration_kernel<true> : icp_registration_kernel<false>;
+  // every block must be resident at once: they wait for the host, which waits
+  // for every block's share of each pass
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(slots) * sizeof(uint2);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, nodes, boxes, pts, slots, src, n, p, cmd, mirror,
+                                           partials, counter, out, slot_of, leaf_of);
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,
                                  int64_t n, const IcpPassParams& p, double* partials,
                                  uint32_t* counter, double* out, int grid, cudaStream_t s,
@@ -1463,6 +1725,7 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_inplace_kernel(
         if (b.d2() <= p.max_d2) {
           ++n_acc;
           add_pair(acc, sx, sy, sz, __ldg(&pts[b.slot]), b.d2(), p);
+          acc[15] = __fadd_rn(acc[15], b.d2());  // one point per thread: exact
         }
       }
     }

@@ -44,6 +44,32 @@ struct alignas(16) CommandMirror {
   float rt[12];  // at byte 16: read with 16-byte vector loads
 };
 
+// Command of the persistent registration kernel (host-mapped, written by the
+// host).  Every word carries the low 32 bits of the pass's sequence number in
+// its high half, so that a reader can tell a complete command from one caught
+// half-written without an acquire fence (which would invalidate the reader's
+// L1 cache, where the persistent kernel keeps the tree from pass to pass):
+// words[j] = (tag << 32) | float bits of rt[j] (R row-major, then t);
+// ctrl = (seq << 2) | kind, kind 0 = run the pass, 1 = leave the kernel.  The
+// host writes the words first, then ctrl.
+struct alignas(16) TaggedCommand {
+  unsigned long long words[12];
+  unsigned long long ctrl;
+};
+
+// Device copy of the tagged commands (zeroed before the kernel starts): the
+// first block to wait for a pass (elect) polls the host's command and forwards
+// it here; the other blocks poll this copy in L2.  ctrl = (seq << 2) |
+// outcome (0 run, 1 stop, 2 gave up); t_cmd = global time (ns) at which the
+// command was seen.
+struct alignas(16) TaggedMirror {
+  unsigned long long elect;
+  unsigned long long ctrl;
+  unsigned long long t_cmd;
+  unsigned long long pad;
+  unsigned long long words[12];
+};
+
 struct IcpPassParams {
   float R[9];
   float t[3];
@@ -113,6 +139,26 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
                             const IcpPassParams& p, double* partials, uint32_t* counter,
                             double* out, int32_t* idx, float* dist2, int32_t* slot_of,
                             uint32_t* leaf_of, int grid, cudaStream_t s);
+
+// The whole registration as one persistent, cooperatively launched kernel
+// (every block resident at once): it stages the top of the tree in shared
+// memory once, then loops: wait for the tagged command of pass p.seq, p.seq +
+// 1, ... (bounded by p.wait_ns, see IcpPassParams), run the pass exactly as
+// launch_icp_pass does with the same grid (same partition of the work, same
+// reduction order, so the same bits), publish the result in `out` with the
+// pass's start and end global times in the two words after the abort word,
+// and wait for the next command.  A stop command (or a later sequence number)
+// ends the kernel; a block that gives up waiting reports the pass aborted and
+// leaves.  The tree is read-only for the kernel's lifetime, so the L1 cache of
+// each SM keeps the part of it its queries touched in the previous pass; the
+// reduction takes an acquire fence only in the blocks that finish a level.
+// Returns cudaErrorCooperativeLaunchTooLarge (and launches nothing) when the
+// grid cannot be resident at once.
+bool registration_kernel_fits(const icpnn_tree& t, int grid);
+cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t n, const IcpPassParams& p,
+                                const TaggedCommand* cmd, TaggedMirror* mirror, double* partials,
+                                uint32_t* counter, double* out, int32_t* slot_of, uint32_t* leaf_of,
+                                int grid, cudaStream_t s);
 
 // Residual pass of the residual rejection (same grid, partials, counter and
 // published result layout as the ICP pass): out[0] = pairs with

@@ -76,6 +76,8 @@ typedef enum icpnn_status {
                                      residual exceeds 3 sigma and solve again */
 #define ICPNN_NO_PRELAUNCH 16u    /* launch each pass only once its transform is solved
                                      (see icpnn_icp_align) */
+#define ICPNN_NO_PERSISTENT 32u   /* pre-launch the passes one at a time instead of running
+                                     the registration as one persistent kernel */
 
 typedef struct icpnn_tree icpnn_tree; /* opaque; owned by the library */
 

@@ -285,17 +285,21 @@ def test_prelaunched_passes_match_plain_launches(nn, name):
     init = np.eye(4)
     init[:3, 3] = [0.01, -0.02, 0.005]
     for kw in ({}, {"timing": True}, {"init_T": init}):
-        a = nn.icp_align(t, src, c.max_iter, c.eps, dmax, trace=True, prelaunch=False, **kw)
-        b = nn.icp_align(t, src, c.max_iter, c.eps, dmax, trace=True, **kw)
-        np.testing.assert_array_equal(a["T"], b["T"])
-        assert a["iters"] == b["iters"] and a["final_mse"] == b["final_mse"]
-        for ra, rb in zip(a["trace"], b["trace"]):
-            assert (ra["mse"], ra["n_accepted"]) == (rb["mse"], rb["n_accepted"])
-            np.testing.assert_array_equal(ra["T"], rb["T"])
-        if kw.get("timing"):
-            assert all(r["kernel_ms"] > 0 for r in b["trace"])
+        a = nn.icp_align(t, src, c.max_iter, c.eps, dmax, trace=True, prelaunch=False, warn_overlap=False, **kw)
+        for mode in ({"persistent": False}, {}):      # passes pre-launched one by one; one persistent kernel
+            b = nn.icp_align(t, src, c.max_iter, c.eps, dmax, trace=True, warn_overlap=False, **mode, **kw)
+            np.testing.assert_array_equal(a["T"], b["T"])
+            assert a["iters"] == b["iters"] and a["final_mse"] == b["final_mse"]
+            assert a["final_n_accepted"] == b["final_n_accepted"]
+            for ra, rb in zip(a["trace"], b["trace"]):
+                assert (ra["mse"], ra["n_accepted"]) == (rb["mse"], rb["n_accepted"])
+                np.testing.assert_array_equal(ra["T"], rb["T"])
+            if kw.get("timing"):
+                assert all(r["kernel_ms"] > 0 for r in b["trace"])
     s = torch.cuda.Stream()
-    outs = [nn.icp_align(t, src, 8, 0.0, dmax, stream=s) for _ in range(3)]
+    outs = [nn.icp_align(t, src, 8, 0.0, dmax, stream=s, warn_overlap=False) for _ in range(3)]
+    s2 = torch.cuda.Stream()
+    outs += [nn.icp_align(t, src, 8, 0.0, dmax, stream=x, warn_overlap=False) for x in (s, s2, s, s2)]
     torch.cuda.synchronize()
     for o in outs[1:]:
         np.testing.assert_array_equal(o["T"], outs[0]["T"])
@@ -339,8 +343,9 @@ def test_residual_and_prelaunched_registrations_alternate(nn):
         np.testing.assert_array_equal(r["T"], ref["T"])
 
 
+@pytest.mark.parametrize("persistent", [True, False])
 @pytest.mark.parametrize("skip", [0, 5])
-def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip):
+def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip, persistent):
     """Fault injected on the host: the transform command of one pre-launched
     pass (the first, or the sixth) is written 80 ms late, beyond the pass's
     50 ms wait.  The pass gives up and publishes its abort marker; the
@@ -357,7 +362,7 @@ def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip):
     nn.probe_delay_commands(skip, 1, 80_000_000)
     try:
         t0 = time.perf_counter()
-        res = nn.icp_align(t, src, 12, 0.0, dmax, trace=True)
+        res = nn.icp_align(t, src, 12, 0.0, dmax, trace=True, persistent=persistent)
         elapsed = time.perf_counter() - t0
     finally:
         nn.probe_delay_commands(0, 0, 0)
@@ -365,14 +370,15 @@ def test_registration_survives_a_pass_that_gives_up_waiting(nn, skip):
     np.testing.assert_array_equal(res["T"], ref["T"])
     assert res["iters"] == ref["iters"] and res["final_mse"] == ref["final_mse"]
     assert [r["mse"] for r in res["trace"]] == [r["mse"] for r in ref["trace"]]
-    again = nn.icp_align(t, src, 12, 0.0, dmax)   # the next registration pre-launches again
+    again = nn.icp_align(t, src, 12, 0.0, dmax, persistent=persistent)   # pre-launches again
     np.testing.assert_array_equal(again["T"], ref["T"])
     with pytest.raises(nn.IcpnnError):
         nn.probe_delay_commands(-1, 1, 0)
 
 
+@pytest.mark.parametrize("persistent", [True, False])
 @pytest.mark.parametrize("skip", [0, 4])
-def test_registration_survives_a_stalled_host(nn, skip):
+def test_registration_survives_a_stalled_host(nn, skip, persistent):
     """Fault injected on the host: between queuing pass k+1 and reading pass
     k the host sleeps 250 ms, beyond twice the 50 ms command wait (as when the
     host thread is descheduled, or a profiler serialises the launches).  Pass
@@ -389,7 +395,7 @@ def test_registration_survives_a_stalled_host(nn, skip):
     nn.probe_delay_collect(skip, 1, 250_000_000)
     try:
         t0 = time.perf_counter()
-        res = nn.icp_align(t, src, 12, 0.0, dmax, trace=True)
+        res = nn.icp_align(t, src, 12, 0.0, dmax, trace=True, persistent=persistent)
         elapsed = time.perf_counter() - t0
     finally:
         nn.probe_delay_collect(0, 0, 0)
@@ -398,8 +404,31 @@ def test_registration_survives_a_stalled_host(nn, skip):
     assert res["iters"] == ref["iters"] and res["final_mse"] == ref["final_mse"]
     assert [r["mse"] for r in res["trace"]] == [r["mse"] for r in ref["trace"]]
     assert [r["n_accepted"] for r in res["trace"]] == [r["n_accepted"] for r in ref["trace"]]
-    again = nn.icp_align(t, src, 12, 0.0, dmax)   # the next registration pre-launches again
+    again = nn.icp_align(t, src, 12, 0.0, dmax, persistent=persistent)   # pre-launches again
     np.testing.assert_array_equal(again["T"], ref["T"])
+
+
+def test_persistent_registration_on_many_sizes(nn):
+    """The persistent kernel runs the per-pass kernel's grid (one partial per
+    block, the same reduction levels), so its registration is bit-identical
+    to ordinary launches for one-level reductions (<= 56 blocks), two-level
+    ones with a ragged last group, and grids that loop over chunks."""
+    c = W.scene_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    for n in (5, 300, 14 * 256 * 8 + 1, 57 * 256, 100_000):
+        src = dev(c.source[:n])
+        dmax = math.inf if n < 1000 else 1.0
+        a = nn.icp_align(t, src, 6, 0.0, dmax, trace=True, prelaunch=False, warn_overlap=False)
+        b = nn.icp_align(t, src, 6, 0.0, dmax, trace=True, warn_overlap=False)
+        np.testing.assert_array_equal(a["T"], b["T"])
+        assert a["final_mse"] == b["final_mse"]
+        assert [r["mse"] for r in a["trace"]] == [r["mse"] for r in b["trace"]]
+    big = np.ascontiguousarray(np.tile(c.source, (8, 1)) + np.float32(0.001))    # 800k: chunks per warp > 1
+    a = nn.icp_align(t, dev(big), 4, 0.0, 1.0, prelaunch=False, warn_overlap=False)
+    b = nn.icp_align(t, dev(big), 4, 0.0, 1.0, warn_overlap=False)
+    np.testing.assert_array_equal(a["T"], b["T"])
+    assert a["final_mse"] == b["final_mse"]
 
 
 def test_large_coarse_to_fine(nn, oracle_mod, large_oracle):
