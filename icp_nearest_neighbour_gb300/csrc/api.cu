@@ -314,6 +314,7 @@ struct Pass {
   float shift_q[3] = {0, 0, 0};
   float max_d2 = INFINITY;
   float* thr = nullptr;  // device: the 3-sigma threshold handed from one residual pass to the next
+  unsigned long long* thr_word = nullptr;  // device, zeroed: the same, tagged, in the persistent kernel
 };
 
 int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bool want_slots,
@@ -323,6 +324,8 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
   if (want_slots) {
     ICPNN_CUDA(sc.alloc(&ps->slot_of, n));
     ICPNN_CUDA(sc.alloc(&ps->thr, 1));
+    ICPNN_CUDA(sc.alloc(&ps->thr_word, 1));
+    ICPNN_CUDA(cudaMemsetAsync(ps->thr_word, 0, sizeof(unsigned long long), s));
   }
   if (warm_start) {
     ICPNN_CUDA(sc.alloc(&ps->leaf_of, n));
@@ -352,11 +355,13 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
 // one queued behind it, say, when launches are serialised or the host stalls)
 // cannot hide this pass's outcome: an abort word at or beyond `seq` means that
 // pass `seq` has finished, and the publish word then tells whether it
-// published.  Bounded: the stream is queried every few thousand polls, so a
-// failed or finished kernel ends the wait.
+// published.  (`abort_word`, if given, replaces the word after `flag`: the
+// persistent kernel records every give-up in the first slot's abort word.)
+// Bounded: the stream is queried every few thousand polls, so a failed or
+// finished kernel ends the wait.
 int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s,
-                   bool* aborted = nullptr) {
-  const volatile unsigned long long* abort_word = flag + 1;
+                   bool* aborted = nullptr, const volatile unsigned long long* abort_word = nullptr) {
+  if (abort_word == nullptr) abort_word = flag + 1;
   for (uint64_t spins = 1;; ++spins) {
     if (*flag == seq) return ICPNN_OK;
     if (aborted != nullptr && *abort_word >= seq) {
@@ -452,10 +457,12 @@ TaggedCommand* tagged_block(const MappedBuffer* mb) {
   return reinterpret_cast<TaggedCommand*>(mb->host + kTaggedOffset);
 }
 
-// Hand pass `seq` of the persistent kernel its transform, or (R == nullptr)
-// tell the kernel to leave.  Every word carries the pass's tag; the control
-// word is stored last, with release order.
-void tagged_command(const MappedBuffer* mb, unsigned long long seq, const float* R, const float* tr) {
+// Hand pass `seq` of the persistent kernel its transform (kind kCmdPass, or
+// kCmdResidual for the iteration's residual passes), or (R == nullptr) tell
+// the kernel to leave.  Every word carries the pass's tag; the control word
+// is stored last, with release order.
+void tagged_command(const MappedBuffer* mb, unsigned long long seq, const float* R, const float* tr,
+                    unsigned long long kind = kCmdPass) {
   if (R != nullptr && tl_cmd_delayed > 0) {
     if (tl_cmd_skip > 0) {
       --tl_cmd_skip;
@@ -473,15 +480,18 @@ void tagged_command(const MappedBuffer* mb, unsigned long long seq, const float*
       __atomic_store_n(&c->words[j], high | bits, __ATOMIC_RELAXED);
     }
   }
-  __atomic_store_n(&c->ctrl, (seq << 2) | (R == nullptr ? 1ull : 0ull), __ATOMIC_RELEASE);
+  __atomic_store_n(&c->ctrl, (seq << 2) | (R == nullptr ? kCmdStop : kind), __ATOMIC_RELEASE);
 }
 
 // A running persistent kernel; told to leave when the owner leaves early.
+// The stop command takes a sequence number of its own: the next registration
+// on this thread starts after it, so its kernel can never read this stop,
+// still in the command block, as addressed to its own first pass.
 struct PersistentRun {
-  const MappedBuffer* mb = nullptr;
+  MappedBuffer* mb = nullptr;
   bool active = false;
   void stop() {
-    if (active) tagged_command(mb, mb->seq + 1, nullptr, nullptr);
+    if (active) tagged_command(mb, ++mb->seq, nullptr, nullptr);
     active = false;
   }
   ~PersistentRun() { stop(); }
@@ -925,8 +935,9 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   if (flags & ~(ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT | ICPNN_NO_PRELAUNCH | ICPNN_NO_PERSISTENT))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_align: unknown flag");
   const bool residual = (flags & ICPNN_RESIDUAL_REJECT) != 0;
-  // the residual passes run between a pass and the next one's transform, so
-  // the next pass cannot be queued ahead of them
+  // one-at-a-time pre-launch: the residual passes run between a pass and the
+  // next one's transform, so the next pass cannot be queued ahead of them
+  // (the persistent kernel runs them itself)
   bool prelaunch = !residual && (flags & ICPNN_NO_PRELAUNCH) == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -945,14 +956,14 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   // resident at once), else ordinary launches.
   PersistentRun run;
   run.mb = ps.mb;
-  if (prelaunch && (flags & ICPNN_NO_PERSISTENT) == 0 && registration_kernel_fits(*t, ps.grid)) {
+  if ((flags & (ICPNN_NO_PRELAUNCH | ICPNN_NO_PERSISTENT)) == 0 && registration_kernel_fits(*t, ps.grid)) {
     IcpPassParams p = pass_params(ps);
     --ps.mb->seq;  // pass_params took a number; the first pass uses it below
     p.wait_ns = kCommandWaitNs;
     const TaggedCommand* dev_cmd = reinterpret_cast<const TaggedCommand*>(ps.mb->dev + kTaggedOffset);
-    const cudaError_t e = launch_registration(*ps.tree, ps.src.recs, ps.n, p, dev_cmd,
-                                              ps.tmirror, ps.partials, ps.counter, ps.mb->dev, ps.slot_of,
-                                              ps.leaf_of, ps.grid, s);
+    const cudaError_t e = launch_registration(*ps.tree, ps.src.recs, ps.n, p, dev_cmd, ps.tmirror, ps.partials,
+                                              ps.counter, ps.mb->dev, ps.mb->dev + kSecondSlot, ps.thr_word,
+                                              ps.slot_of, ps.leaf_of, ps.grid, s);
     if (e == cudaSuccess) {
       run.active = true;
       prelaunch = false;
@@ -1033,6 +1044,40 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     return pass_run(ps, R32, t32, nullptr, nullptr, s, nullptr, nullptr, m);
   };
 
+  // The persistent kernel's residual passes of one iteration under (R1, t1):
+  // one command, the first pass's sums (second slot) and the kept pairs'
+  // moments (first slot) read back; the same fallback as persistent_pass.
+  auto persistent_residual = [&](const float R1[9], const float t1[3], double* sigma2,
+                                 icpnn_moments* kept) -> int {
+    const unsigned long long seq_a = ++ps.mb->seq;
+    const unsigned long long seq_b = ++ps.mb->seq;
+    tagged_command(ps.mb, seq_a, R1, t1, kCmdResidual);
+    const volatile unsigned long long* flag_a =
+        reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kSecondSlot + kMomentSlots);
+    // a kernel that gave up -- waiting for this command, or for the threshold
+    // between the two passes -- records it in the first slot's abort word
+    bool aborted = false;
+    if (int rc = wait_published(flag_a, seq_a, s, &aborted, flag0 + 1)) return rc;
+    if (!aborted)
+      if (int rc = wait_published(flag0, seq_b, s, &aborted)) return rc;
+    if (!aborted) {
+      std::atomic_thread_fence(std::memory_order_acquire);
+      double raw[kMomentSlots];
+      std::memcpy(raw, const_cast<const double*>(ps.mb->host + kSecondSlot), sizeof(raw));
+      const double pairs = raw[1];
+      *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
+      std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
+      decode_moments(raw, ps.src.shift, ps.shift_q, kept);
+      kept->n_nonfinite = 0;
+      kept->sum_d2 = 0.0;
+      kept->mse = NAN;
+      return ICPNN_OK;
+    }
+    run.stop();
+    ICPNN_CUDA(cudaMemsetAsync(ps.counter, 0, static_cast<size_t>(reduction_counter_words(ps.grid)) * sizeof(uint32_t), s));
+    return residual_run(ps, R1, t1, s, sigma2, kept);
+  };
+
   double mse_hist[3] = {0, 0, 0};
   int32_t done = 0;
   for (int32_t k = 0; k < max_iter; ++k) {
@@ -1069,7 +1114,11 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       float R1[9], t1[3];
       transform_to_f32(Tn, R1, t1);
       icpnn_moments kept;
-      if (int rc = residual_run(ps, R1, t1, s, &sigma2, &kept)) return rc;
+      if (run.active) {
+        if (int rc = persistent_residual(R1, t1, &sigma2, &kept)) return rc;
+      } else {
+        if (int rc = residual_run(ps, R1, t1, s, &sigma2, &kept)) return rc;
+      }
       n_inliers = kept.n_accepted;
       if (n_inliers < 3 || kabsch_solve(kept, Tn) != ICPNN_OK)
         return fail(ICPNN_ERR_DEGENERATE, "icp_align: residual rejection left a degenerate pair set at "

@@ -846,7 +846,8 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
                                                unsigned int* __restrict__ counter, double* out,
                                                unsigned long long seq, float* thr_out = nullptr,
                                                unsigned int skipped = 0u,
-                                               const unsigned long long* t_start = nullptr) {
+                                               const unsigned long long* t_start = nullptr,
+                                               unsigned long long* thr_word = nullptr) {
   __shared__ double s_warp[kThreads / 32][kMomentSlots];
   __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
   __shared__ bool s_last;
@@ -987,10 +988,17 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     }
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
-    if (thr_out != nullptr) {
+    if (thr_out != nullptr || thr_word != nullptr) {
       const double pairs = s_fin[0][1];
       const double sigma2 = pairs > 0.0 ? s_fin[0][17] / pairs : 0.0;
-      *thr_out = float_threshold_dev(9.0 * sigma2);
+      const float thr = float_threshold_dev(9.0 * sigma2);
+      if (thr_out != nullptr) *thr_out = thr;
+      // release: the counters reset above are in place before any block that
+      // reads this word starts the next pass's reduction
+      if (thr_word != nullptr)
+        asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(thr_word),
+                     "l"((static_cast<unsigned long long>(static_cast<uint32_t>(seq)) << 32) | __float_as_uint(thr))
+                     : "memory");
     }
     if (kPublish) {
       if (t_start != nullptr) {
@@ -1254,6 +1262,59 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_kernel(
   reduce_moments<true>(acc, n_acc, n_bad, partials, counter, out, p.seq, nullptr, skipped);
 }
 
+// This thread's share of a residual pass: for each of its source records with
+// a match (slot_of >= 0), the squared residual e2 of the pair under rt, with
+// the search's float arithmetic; every pair is counted in n_pair and its e2
+// summed in acc[15]; pairs with e2 <= max_d2 are counted in n_keep and their
+// moments accumulated.  Shared by the residual kernel and the persistent
+// registration kernel.
+__device__ __forceinline__ void residual_chunks(const float4* __restrict__ pts, const float4* __restrict__ src,
+                                                const int32_t* __restrict__ slot_of, int64_t n, const float* rt,
+                                                float max_d2, const IcpPassParams& p, float (&acc)[16],
+                                                uint32_t& n_keep, uint32_t& n_pair) {
+  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
+    const int64_t i = c * 32 + (threadIdx.x & 31);
+    if (i >= n) continue;
+    const int32_t sl = slot_of[i];
+    if (sl < 0) continue;
+    const float4 s = src[i];
+    const float4 r = __ldg(&pts[sl]);
+    float q[3];
+    transform_point(rt, s.x, s.y, s.z, q);
+    const float e2 = dist2(r, q[0], q[1], q[2]);
+    ++n_pair;
+    const float sum_e2 = __fadd_rn(acc[15], e2);
+    if (e2 <= max_d2) {
+      ++n_keep;
+      add_pair(acc, s.x, s.y, s.z, r, 0.f, p);
+    }
+    acc[15] = sum_e2;
+  }
+}
+
+// Residual pass of the section 4.4 rejection: for every source record with a
+// match from the last correspondence pass (slot_of >= 0), the squared residual
+// e2 of the pair under the transform in p (same float arithmetic as the search
+// distance).  Counts every pair in c1 and sums its e2 in acc[15]; pairs with
+// e2 <= p.max_d2 are counted in c0 and their moments accumulated in acc[0..14].
+__global__ void __launch_bounds__(kThreads) residual_pass_kernel(
+    const float4* __restrict__ pts, const float4* __restrict__ src, const int32_t* __restrict__ slot_of,
+    int64_t n, IcpPassParams p, double* __restrict__ partials, unsigned int* __restrict__ counter,
+    double* out, const float* thr_in, float* thr_out) {
+  if (thr_in != nullptr) p.max_d2 = *thr_in;  // written by the previous pass on this stream
+  float rt[12];
+#pragma unroll
+  for (int k = 0; k < 9; ++k) rt[k] = p.R[k];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) rt[9 + k] = p.t[k];
+  float acc[16];
+#pragma unroll
+  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+  uint32_t n_keep = 0, n_pair = 0;
+  residual_chunks(pts, src, slot_of, n, rt, p.max_d2, p, acc, n_keep, n_pair);
+  reduce_moments<true>(acc, n_keep, n_pair, partials, counter, out, p.seq, thr_out);
+}
+
 // ------------------------------------------------ persistent registration
 
 __device__ __forceinline__ void store_relaxed_gpu(unsigned long long* a, unsigned long long v) {
@@ -1280,15 +1341,17 @@ __device__ __forceinline__ bool load_tagged(const unsigned long long* a, uint32_
 }
 
 // One thread per block: wait until the tagged command names pass `seq` and
-// copy its R and t to rt.  Returns 0 (run), kSkipStopped (stop, or a later
-// pass named) or kSkipTimedOut.  The first block to arrive polls host memory
-// for at most wait_ns and forwards what it found through the mirror; the
-// others poll the mirror for at most 2 * wait_ns.  No acquire fence: a reader
-// re-reads the payload until all its tags name the pass (bounded).
+// copy its R and t to rt.  Returns kRunPass, kRunResidual, kSkipStopped
+// (stop, or a later pass named) or kSkipTimedOut.  The first block to arrive
+// polls host memory for at most wait_ns and forwards what it found through
+// the mirror as (seq << 3) | code (codes: the host's kinds, or 3 = gave up);
+// the others poll the mirror for at most 2 * wait_ns.  No acquire fence: a
+// reader re-reads the payload until all its tags name the pass (bounded).
+constexpr unsigned int kRunPass = 0u, kRunResidual = 2u;
 __device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, TaggedMirror* m,
                                                      unsigned long long seq, unsigned long long wait_ns,
                                                      float* rt) {
-  constexpr unsigned long long kRun = 0, kStop = 1, kTimeout = 2;
+  constexpr unsigned long long kRun = kCmdPass, kStop = kCmdStop, kResidual = kCmdResidual, kTimeout = 3;
   const uint32_t tag = static_cast<uint32_t>(seq);
   const unsigned long long t0 = global_ns();
   unsigned long long outcome = kTimeout;
@@ -1298,7 +1361,7 @@ __device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, T
       const uint32_t ctag = static_cast<uint32_t>(c >> 2);
       if (ctag == tag) {
         outcome = c & 3ull;
-        if (outcome == kRun) {
+        if (outcome == kRun || outcome == kResidual) {
           while (!load_tagged<true>(cmd->words, tag, rt)) {
             if (global_ns() - t0 > wait_ns) {
               outcome = kTimeout;
@@ -1315,19 +1378,19 @@ __device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, T
       if (global_ns() - t0 > wait_ns) break;
       __nanosleep(200);
     }
-    if (outcome == kRun) {
+    if (outcome == kRun || outcome == kResidual) {
       const unsigned long long high = static_cast<unsigned long long>(tag) << 32;
 #pragma unroll
       for (int k = 0; k < 12; ++k) store_relaxed_gpu(&m->words[k], high | __float_as_uint(rt[k]));
     }
     store_relaxed_gpu(&m->t_cmd, global_ns());
-    store_relaxed_gpu(&m->ctrl, (seq << 2) | outcome);
+    store_relaxed_gpu(&m->ctrl, (seq << 3) | outcome);
   } else {
     for (;;) {
       const unsigned long long c = load_relaxed_gpu(&m->ctrl);
-      if ((c >> 2) >= seq) {
-        outcome = (c >> 2) == seq ? (c & 3ull) : kStop;
-        if (outcome == kRun) {
+      if ((c >> 3) >= seq) {
+        outcome = (c >> 3) == seq ? (c & 7ull) : kStop;
+        if (outcome == kRun || outcome == kResidual) {
           while (!load_tagged<false>(m->words, tag, rt)) {
             if (global_ns() - t0 > 2 * wait_ns) {
               outcome = kTimeout;
@@ -1341,70 +1404,85 @@ __device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, T
       __nanosleep(100);
     }
   }
-  return outcome == kRun ? 0u : outcome == kStop ? kSkipStopped : kSkipTimedOut;
+  return outcome == kRun ? kRunPass : outcome == kResidual ? kRunResidual
+                                   : outcome == kStop ? kSkipStopped : kSkipTimedOut;
 }
 
+// Every block of the persistent kernel: wait (thread 0, bounded) until the
+// residual threshold of pass `seq` has been stored -- one 64-bit word, the
+// pass's tag above the float's bits -- and copy it to *out.
+__device__ __forceinline__ bool await_threshold(const unsigned long long* word, unsigned long long seq,
+                                                unsigned long long wait_ns, float* out) {
+  const uint32_t tag = static_cast<uint32_t>(seq);
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    const unsigned long long w = load_relaxed_gpu(word);
+    if (static_cast<uint32_t>(w >> 32) == tag) {
+      *out = __uint_as_float(static_cast<uint32_t>(w));
+      return true;
+    }
+    if (global_ns() - t0 > 2 * wait_ns) return false;
+    __nanosleep(32);
+  }
+}
+
+// kSlot: the registration uses the residual rejection -- correspondence
+// passes record each source record's matched slot, and a residual command
+// runs the two residual passes of the iteration back to back: A (sums e2
+// under the command's transform, publishes in the second result slot with
+// sequence number seq, and stores the 3-sigma threshold as a tagged word in
+// thr_word), then, once every block has read that threshold, B (the kept
+// pairs' moments, published in the first slot with seq + 1).  A residual
+// command thus uses two sequence numbers.
 template <bool kSlot>
 __global__ void __launch_bounds__(kThreads, 3) icp_registration_kernel(
     const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
     int smem_slots, const float4* __restrict__ src, int64_t n, IcpPassParams p, const TaggedCommand* cmd,
     TaggedMirror* mirror, double* __restrict__ partials, unsigned int* __restrict__ counter, double* out,
-    int32_t* __restrict__ slot_of, uint32_t* __restrict__ leaf_of) {
+    double* out_second, unsigned long long* thr_word, int32_t* __restrict__ slot_of,
+    uint32_t* __restrict__ leaf_of) {
   extern __shared__ __align__(16) uint2 s_nodes[];
   __shared__ float s_rt[12];
+  __shared__ float s_thr;
   __shared__ unsigned int s_skip;
   stage_top(nodes, s_nodes, smem_slots);  // once for the whole registration
   const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
-  for (unsigned long long seq = p.seq;; ++seq) {
+  for (unsigned long long seq = p.seq;;) {
     if (threadIdx.x == 0) s_skip = await_tagged(cmd, mirror, seq, p.wait_ns, s_rt);
     __syncthreads();
-    const unsigned int skipped = s_skip;
-    if (skipped == kSkipStopped) return;
+    const unsigned int code = s_skip;
+    if (code == kSkipStopped) return;
     float acc[16];
 #pragma unroll
     for (int v = 0; v < 16; ++v) acc[v] = 0.f;
-    uint32_t n_acc = 0, n_bad = 0;
-    if (skipped == 0u)
-      pass_chunks<false, kSlot>(tv, s_rt, src, n, n, p, nullptr, nullptr, slot_of, leaf_of, acc, n_acc, n_bad);
-    reduce_moments<true, true>(acc, n_acc, n_bad, partials, counter, out, seq, nullptr, skipped, &mirror->t_cmd);
-    if (skipped != 0u) return;  // gave up waiting: the pass reports its abort, this block leaves
-    __syncthreads();            // s_rt and s_skip are rewritten for the next pass
-  }
-}
-
-// Residual pass of the section 4.4 rejection: for every source record with a
-// match from the last correspondence pass (slot_of >= 0), the squared residual
-// e2 of the pair under the transform in p (same float arithmetic as the search
-// distance).  Counts every pair in c1 and sums its e2 in acc[15]; pairs with
-// e2 <= p.max_d2 are counted in c0 and their moments accumulated in acc[0..14].
-__global__ void __launch_bounds__(kThreads) residual_pass_kernel(
-    const float4* __restrict__ pts, const float4* __restrict__ src, const int32_t* __restrict__ slot_of,
-    int64_t n, IcpPassParams p, double* __restrict__ partials, unsigned int* __restrict__ counter,
-    double* out, const float* thr_in, float* thr_out) {
-  if (thr_in != nullptr) p.max_d2 = *thr_in;  // written by the previous pass on this stream
-  float acc[16];
+    if (kSlot && code == kRunResidual) {
+      uint32_t n_keep = 0, n_pair = 0;
+      residual_chunks(pts, src, slot_of, n, s_rt, __int_as_float(0x7f800000), p, acc, n_keep, n_pair);
+      reduce_moments<true, true>(acc, n_keep, n_pair, partials, counter, out_second, seq, nullptr, 0u,
+                                 &mirror->t_cmd, thr_word);
+      if (threadIdx.x == 0) s_skip = await_threshold(thr_word, seq, p.wait_ns, &s_thr) ? 0u : kSkipTimedOut;
+      __syncthreads();
+      const unsigned int skipped = s_skip;
 #pragma unroll
-  for (int v = 0; v < 16; ++v) acc[v] = 0.f;
-  uint32_t n_keep = 0, n_pair = 0;
-  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
-    const int64_t i = c * 32 + (threadIdx.x & 31);
-    if (i >= n) continue;
-    const int32_t sl = slot_of[i];
-    if (sl < 0) continue;
-    const float4 s = src[i];
-    const float4 r = __ldg(&pts[sl]);
-    float q[3];
-    transform_point(p, s.x, s.y, s.z, q);
-    const float e2 = dist2(r, q[0], q[1], q[2]);
-    ++n_pair;
-    const float sum_e2 = __fadd_rn(acc[15], e2);
-    if (e2 <= p.max_d2) {
-      ++n_keep;
-      add_pair(acc, s.x, s.y, s.z, r, 0.f, p);
+      for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+      n_keep = n_pair = 0;
+      if (skipped == 0u) residual_chunks(pts, src, slot_of, n, s_rt, s_thr, p, acc, n_keep, n_pair);
+      reduce_moments<true, true>(acc, n_keep, n_pair, partials, counter, out, seq + 1, nullptr, skipped,
+                                 &mirror->t_cmd);
+      if (skipped != 0u) return;
+      seq += 2;
+    } else {
+      const unsigned int skipped = code == kRunPass ? 0u : kSkipTimedOut;
+      uint32_t n_acc = 0, n_bad = 0;
+      if (skipped == 0u)
+        pass_chunks<false, kSlot>(tv, s_rt, src, n, n, p, nullptr, nullptr, slot_of, leaf_of, acc, n_acc, n_bad);
+      reduce_moments<true, true>(acc, n_acc, n_bad, partials, counter, out, seq, nullptr, skipped,
+                                 &mirror->t_cmd);
+      if (skipped != 0u) return;  // gave up waiting: the pass reports its abort, this block leaves
+      seq += 1;
     }
-    acc[15] = sum_e2;
+    __syncthreads();  // s_rt, s_thr and s_skip are rewritten for the next command
   }
-  reduce_moments<true>(acc, n_keep, n_pair, partials, counter, out, p.seq, thr_out);
 }
 
 inline int smem_slots_for(const icpnn_tree& t) {
@@ -1550,8 +1628,9 @@ bool registration_kernel_fits(const icpnn_tree& t, int grid) {
 
 cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t n, const IcpPassParams& p,
                                 const TaggedCommand* cmd, TaggedMirror* mirror, double* partials,
-                                uint32_t* counter, double* out, int32_t* slot_of, uint32_t* leaf_of,
-                                int grid, cudaStream_t s) {
+                                uint32_t* counter, double* out, double* out_second,
+                                unsigned long long* thr_word, int32_t* slot_of, uint32_t* leaf_of, int grid,
+                                cudaStream_t s) {
   const int slots = smem_slots_for(t);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
   const float4* boxes = reinterpret_cast<const float4*>(t.dev.boxes);
@@ -1570,7 +1649,7 @@ cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, nodes, boxes, pts, slots, src, n, p, cmd, mirror,
-                                           partials, counter, out, slot_of, leaf_of);
+                                           partials, counter, out, out_second, thr_word, slot_of, leaf_of);
   if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

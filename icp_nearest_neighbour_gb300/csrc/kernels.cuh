@@ -44,14 +44,19 @@ struct alignas(16) CommandMirror {
   float rt[12];  // at byte 16: read with 16-byte vector loads
 };
 
+// Kinds of a tagged command (the low two bits of its control word).
+constexpr unsigned long long kCmdPass = 0, kCmdStop = 1, kCmdResidual = 2;
+
 // Command of the persistent registration kernel (host-mapped, written by the
 // host).  Every word carries the low 32 bits of the pass's sequence number in
 // its high half, so that a reader can tell a complete command from one caught
 // half-written without an acquire fence (which would invalidate the reader's
 // L1 cache, where the persistent kernel keeps the tree from pass to pass):
 // words[j] = (tag << 32) | float bits of rt[j] (R row-major, then t);
-// ctrl = (seq << 2) | kind, kind 0 = run the pass, 1 = leave the kernel.  The
-// host writes the words first, then ctrl.
+// ctrl = (seq << 2) | kind: kCmdPass (a correspondence pass), kCmdStop (leave
+// the kernel) or kCmdResidual (the iteration's two residual passes, which use
+// sequence numbers seq and seq + 1).  The host writes the words first, then
+// ctrl.
 struct alignas(16) TaggedCommand {
   unsigned long long words[12];
   unsigned long long ctrl;
@@ -59,9 +64,9 @@ struct alignas(16) TaggedCommand {
 
 // Device copy of the tagged commands (zeroed before the kernel starts): the
 // first block to wait for a pass (elect) polls the host's command and forwards
-// it here; the other blocks poll this copy in L2.  ctrl = (seq << 2) |
-// outcome (0 run, 1 stop, 2 gave up); t_cmd = global time (ns) at which the
-// command was seen.
+// it here; the other blocks poll this copy in L2.  ctrl = (seq << 3) | code
+// (the command's kind, or 3 = gave up waiting); t_cmd = global time (ns) at
+// which the command was seen.
 struct alignas(16) TaggedMirror {
   unsigned long long elect;
   unsigned long long ctrl;
@@ -147,9 +152,14 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
 // launch_icp_pass does with the same grid (same partition of the work, same
 // reduction order, so the same bits), publish the result in `out` with the
 // pass's start and end global times in the two words after the abort word,
-// and wait for the next command.  A stop command (or a later sequence number)
-// ends the kernel; a block that gives up waiting reports the pass aborted and
-// leaves.  The tree is read-only for the kernel's lifetime, so the L1 cache of
+// and wait for the next command.  With slot_of (the residual rejection) the
+// correspondence passes record each record's matched slot, and a residual
+// command runs the iteration's two residual passes (see
+// launch_residual_pass) back to back: the first publishes in out_second with
+// seq and hands the 3-sigma threshold to the second through thr_word (a
+// device word, the pass's tag above the float's bits), the second publishes
+// in out with seq + 1.  A stop command (or a later sequence number) ends the
+// kernel; a block that gives up waiting reports the pass aborted and leaves.  The tree is read-only for the kernel's lifetime, so the L1 cache of
 // each SM keeps the part of it its queries touched in the previous pass; the
 // reduction takes an acquire fence only in the blocks that finish a level.
 // Returns cudaErrorCooperativeLaunchTooLarge (and launches nothing) when the
@@ -157,8 +167,9 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
 bool registration_kernel_fits(const icpnn_tree& t, int grid);
 cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t n, const IcpPassParams& p,
                                 const TaggedCommand* cmd, TaggedMirror* mirror, double* partials,
-                                uint32_t* counter, double* out, int32_t* slot_of, uint32_t* leaf_of,
-                                int grid, cudaStream_t s);
+                                uint32_t* counter, double* out, double* out_second,
+                                unsigned long long* thr_word, int32_t* slot_of, uint32_t* leaf_of, int grid,
+                                cudaStream_t s);
 
 // Residual pass of the residual rejection (same grid, partials, counter and
 // published result layout as the ICP pass): out[0] = pairs with

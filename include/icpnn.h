@@ -256,14 +256,23 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   kept pairs (DEGENERATE if fewer than 3 remain).  The stopping rule still
  *   uses mse_k of the correspondence pass.
  *   Then one more pass (no solve) under the returned transform.
- *   Pass launches: without ICPNN_RESIDUAL_REJECT or ICPNN_NO_PRELAUNCH each
- *   pass is queued on `stream` while the previous one runs; its blocks wait
- *   on the GPU for the transform the host writes to pinned memory after the
- *   solve, so the launch latency overlaps the previous pass.  The wait is
- *   bounded (50 ms): a pass that runs out (a profiler that serialises
- *   launches, a host thread descheduled that long) is run again as an
- *   ordinary launch and so is the rest of the registration.  Results are
- *   bit-identical either way.
+ *   Pass launches: by default the whole registration is one persistent
+ *   kernel on `stream` (a cooperative launch: every block resident at once),
+ *   which stages the top of the tree once and keeps each SM's cache of the
+ *   tree from one pass to the next; between passes its blocks wait on the GPU
+ *   for the transform the host writes to pinned memory after each solve.
+ *   With ICPNN_RESIDUAL_REJECT it also runs each iteration's two residual
+ *   passes, handing the threshold from one to the other on the GPU.  With
+ *   ICPNN_NO_PERSISTENT (or when the grid cannot be resident at once) each
+ *   pass is instead queued while the previous one runs and waits the same
+ *   way (not with ICPNN_RESIDUAL_REJECT); with ICPNN_NO_PRELAUNCH every pass
+ *   is an ordinary launch after its solve.  Every wait is bounded (50 ms): a
+ *   pass that runs out (a profiler that serialises launches, a host thread
+ *   descheduled that long) is run again as an ordinary launch and so is the
+ *   rest of the registration.  Results are bit-identical in every mode.
+ *   With ICPNN_TRACE_TIMING, kernel_ms is the pass's time on the persistent
+ *   kernel's clock (command seen to result published), or CUDA events around
+ *   the pass otherwise (0 for passes run after a fallback).
  *   src          n_src x 3 float32 (device, or host: copied in once).
  *   max_iter     >= 1.  eps >= 0 (0: run max_iter iterations).
  *   out_T        host double[16]: the last solved transform (target ~ T src).
@@ -279,7 +288,7 @@ int icpnn_kabsch(const icpnn_moments* m, double* T);
  *   trace        optional host array of trace_cap records (one per
  *                iteration, up to trace_cap).
  *   flags        ICPNN_TRACE_TIMING | ICPNN_RESIDUAL_REJECT |
- *                ICPNN_NO_PRELAUNCH, or 0.
+ *                ICPNN_NO_PRELAUNCH | ICPNN_NO_PERSISTENT, or 0.
  * Synchronises `stream` once per iteration; scratch comes from the
  * stream-ordered allocator and is returned before the call ends.
  * Errors: INVALID_ARG, NOT_UPLOADED, CUDA, NO_MEMORY, NONFINITE, DEGENERATE. */

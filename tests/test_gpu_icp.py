@@ -250,6 +250,32 @@ def test_residual_rejection_parity(nn, oracle_mod, name):
         assert rot_angle(res["T"][:3, :3], c.T_gt[:3, :3]) < rot_angle(plain["T"][:3, :3], c.T_gt[:3, :3])
 
 
+@pytest.mark.parametrize("name", ["tiny_outliers", "scene"])
+def test_persistent_residual_registration_matches_ordinary_launches(nn, name):
+    """The persistent kernel runs each iteration's residual passes itself (the
+    threshold handed over on the GPU); the registration is bit-identical to
+    one with ordinary launches, also when one residual command arrives after
+    the kernel gave up waiting for it (80 ms late: the host falls back)."""
+    c, src, dmax = _residual_case(name)
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    s = dev(src)
+    kw = dict(trace=True, residual_reject=True, warn_overlap=False)
+    a = nn.icp_align(t, s, c.max_iter, c.eps, dmax, prelaunch=False, **kw)
+    b = nn.icp_align(t, s, c.max_iter, c.eps, dmax, **kw)
+    nn.probe_delay_commands(3, 1, 80_000_000)     # the second iteration's residual command
+    try:
+        d = nn.icp_align(t, s, c.max_iter, c.eps, dmax, **kw)
+    finally:
+        nn.probe_delay_commands(0, 0, 0)
+    for r in (b, d):
+        np.testing.assert_array_equal(a["T"], r["T"])
+        assert a["iters"] == r["iters"] and a["final_mse"] == r["final_mse"]
+        for ra, rb in zip(a["trace"], r["trace"]):
+            assert (ra["mse"], ra["n_accepted"], ra["n_inliers"], ra["sigma2"]) == \
+                (rb["mse"], rb["n_accepted"], rb["n_inliers"], rb["sigma2"])
+
+
 def test_tiny_recovers_ground_truth(nn):
     c = W.tiny_case()
     t = nn.kdtree_build(c.target, c.leaf_size)
@@ -406,6 +432,30 @@ def test_registration_survives_a_stalled_host(nn, skip, persistent):
     assert [r["n_accepted"] for r in res["trace"]] == [r["n_accepted"] for r in ref["trace"]]
     again = nn.icp_align(t, src, 12, 0.0, dmax, persistent=persistent)   # pre-launches again
     np.testing.assert_array_equal(again["T"], ref["T"])
+
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_back_to_back_registrations_with_a_late_first_command(nn, residual):
+    """A registration ends by telling its persistent kernel to stop; that stop
+    stays in the thread's command block.  The next registration's kernel must
+    not take it for its own first command: here the first command is written
+    5 ms after the launch (inside the 50 ms wait), so the new kernel certainly
+    polls before it arrives."""
+    c = W.tiny_case()
+    t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(t)
+    src = dev(c.source)
+    kw = dict(residual_reject=residual, warn_overlap=False)
+    ref = nn.icp_align(t, src, 8, 0.0, math.inf, prelaunch=False, **kw)
+    for _ in range(3):
+        nn.icp_align(t, src, 8, 0.0, math.inf, **kw)
+        nn.probe_delay_commands(0, 1, 5_000_000)
+        try:
+            r = nn.icp_align(t, src, 8, 0.0, math.inf, **kw)
+        finally:
+            nn.probe_delay_commands(0, 0, 0)
+        np.testing.assert_array_equal(r["T"], ref["T"])
+        assert r["final_mse"] == ref["final_mse"]
 
 
 def test_persistent_registration_on_many_sizes(nn):
