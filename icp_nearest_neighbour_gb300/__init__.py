@@ -69,7 +69,7 @@ class Moments(ctypes.Structure):
 class IterRecord(ctypes.Structure):
     _fields_ = [("iter", ctypes.c_int32), ("flags", ctypes.c_int32), ("n_accepted", ctypes.c_int64),
                 ("n_inliers", ctypes.c_int64), ("mse", ctypes.c_double), ("sigma2", ctypes.c_double),
-                ("T", ctypes.c_double * 16), ("kernel_ms", ctypes.c_float), ("reserved", ctypes.c_float)]
+                ("T", ctypes.c_double * 16), ("kernel_ms", ctypes.c_float), ("residual_ms", ctypes.c_float)]
 
 
 _lib = None
@@ -387,7 +387,7 @@ def icp_align(tree: KDTree, src, max_iter: int, eps: float, max_corr_dist: float
     if cap:
         out["trace"] = [{"iter": r.iter, "n_accepted": r.n_accepted, "n_inliers": r.n_inliers,
                          "mse": r.mse, "sigma2": r.sigma2, "T": np.array(r.T[:]).reshape(4, 4),
-                         "kernel_ms": r.kernel_ms}
+                         "kernel_ms": r.kernel_ms, "residual_ms": r.residual_ms}
                         for r in recs[:min(iters.value, cap)]]
     return out
 

@@ -91,6 +91,23 @@ bool is_device_pointer(const void* p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// Device memory that the current device's kernels may read and write:
+// allocated on that device (or managed memory).
+bool is_current_device_pointer(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeManaged) return true;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == cur;
+}
+
 // Device allocations from the stream-ordered pool, returned on the same stream.
 class Scratch {
  public:
@@ -874,11 +891,11 @@ int icpnn_icp_step_noalloc(const icpnn_tree* t, const float* src, int64_t n, con
                     std::to_string(ICPNN_NOALLOC_MAX_POINTS) +
                     "], the most points its fixed scratch array can reduce; use icpnn_icp_step");
   if (std::isnan(max_corr_dist)) return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: max_corr_dist is NaN");
-  if (!is_device_pointer(src))
-    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: src must be device memory (a host buffer would "
-                                       "need a staging allocation)");
-  if (idx != nullptr && (!is_device_pointer(idx) || !is_device_pointer(dist2)))
-    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: idx and dist2 must be device memory");
+  if (!is_current_device_pointer(src))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: src must be memory of the current device (a host "
+                                       "buffer would need a staging allocation)");
+  if (idx != nullptr && (!is_current_device_pointer(idx) || !is_current_device_pointer(dist2)))
+    return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: idx and dist2 must be memory of the current device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   double* scratch = nullptr;
   ICPNN_CUDA(noalloc_scratch(&scratch));
@@ -1048,7 +1065,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   // one command, the first pass's sums (second slot) and the kept pairs'
   // moments (first slot) read back; the same fallback as persistent_pass.
   auto persistent_residual = [&](const float R1[9], const float t1[3], double* sigma2,
-                                 icpnn_moments* kept) -> int {
+                                 icpnn_moments* kept, float* resid_ms) -> int {
     const unsigned long long seq_a = ++ps.mb->seq;
     const unsigned long long seq_b = ++ps.mb->seq;
     tagged_command(ps.mb, seq_a, R1, t1, kCmdResidual);
@@ -1071,8 +1088,11 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       kept->n_nonfinite = 0;
       kept->sum_d2 = 0.0;
       kept->mse = NAN;
+      const unsigned long long t0 = flag_a[2], t1 = flag0[3];
+      *resid_ms = t1 > t0 ? static_cast<float>(static_cast<double>(t1 - t0) * 1e-6) : 0.f;
       return ICPNN_OK;
     }
+    *resid_ms = 0.f;
     run.stop();
     ICPNN_CUDA(cudaMemsetAsync(ps.counter, 0, static_cast<size_t>(reduction_counter_words(ps.grid)) * sizeof(uint32_t), s));
     return residual_run(ps, R1, t1, s, sigma2, kept);
@@ -1109,13 +1129,14 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
                                             std::to_string(k));
     int64_t n_inliers = m.n_accepted;
     double sigma2 = 0.0;
+    float resid_ms = 0.f;
     if (residual) {
       // page section 4.4: residuals under the first solve, 3-sigma rule, re-solve
       float R1[9], t1[3];
       transform_to_f32(Tn, R1, t1);
       icpnn_moments kept;
       if (run.active) {
-        if (int rc = persistent_residual(R1, t1, &sigma2, &kept)) return rc;
+        if (int rc = persistent_residual(R1, t1, &sigma2, &kept, &resid_ms)) return rc;
       } else {
         if (int rc = residual_run(ps, R1, t1, s, &sigma2, &kept)) return rc;
       }
@@ -1133,8 +1154,9 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       r.mse = m.mse;
       r.sigma2 = sigma2;
       std::memcpy(r.T, T, sizeof(T));
-      r.kernel_ms = pass_ms;
-      r.reserved = 0.f;
+      const bool timing = (flags & ICPNN_TRACE_TIMING) != 0;
+      r.kernel_ms = timing ? pass_ms : 0.f;
+      r.residual_ms = timing ? resid_ms : 0.f;
     }
     std::memcpy(T, Tn, sizeof(T));
     mse_hist[0] = mse_hist[1];

@@ -927,7 +927,7 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     if (kPersistent && threadIdx.x == 0) {
 #pragma unroll
       for (int u = 0; u < kMomentSlots; ++u) partials[static_cast<int64_t>(g0) * kMomentSlots + u] = s_warp[0][u];
-      atomicExch(counter + 2 + group, 0u);
+      counter[2 + group] = 0u;  // ordered before the next level's release increment
     }
     rows = (gridDim.x + kGroupBlocks - 1) / kGroupBlocks;
     row_stride = kGroupBlocks;
@@ -936,8 +936,18 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     s_last = ((kPersistent ? atom_add_release_gpu(counter, 1u) : atomicAdd(counter, 1u)) == rows - 1);
   __syncthreads();
   if (!s_last) return;
+  // the last block: in the persistent kernel, thread 0 starts the reads it
+  // needs at the end (skipped blocks, the pass's start time) now, so that
+  // their latency overlaps the sum below
+  unsigned int skips = 0u;
+  unsigned long long t_cmd = 0ull;
   if (kPersistent) {
-    if (threadIdx.x == 0) fence_acq_rel_gpu();
+    if (threadIdx.x == 0) {
+      fence_acq_rel_gpu();
+      skips = atomicExch(counter + 1, 0u);
+      if (t_start != nullptr) t_cmd = __ldcg(t_start);
+      counter[0] = 0u;
+    }
     __syncthreads();
   } else {
     __threadfence();
@@ -971,11 +981,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // orders its own stores, the sequence word: the host never sees the new
   // sequence before the values.
   if (threadIdx.x == 0) {
-    if (kPersistent)
-      atomicExch(counter, 0u);
-    else
+    if (!kPersistent) {
       *counter = 0u;
-    const unsigned int skips = atomicExch(counter + 1, 0u);
+      skips = atomicExch(counter + 1, 0u);
+    }
     if (skips != 0u) {
       // The abort marker has a word of its own: the pass queued behind this
       // one may give up too, and its marker must not overwrite this pass's
@@ -986,24 +995,26 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
       }
       return;
     }
-#pragma unroll
-    for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
     if (thr_out != nullptr || thr_word != nullptr) {
       const double pairs = s_fin[0][1];
       const double sigma2 = pairs > 0.0 ? s_fin[0][17] / pairs : 0.0;
       const float thr = float_threshold_dev(9.0 * sigma2);
       if (thr_out != nullptr) *thr_out = thr;
       // release: the counters reset above are in place before any block that
-      // reads this word starts the next pass's reduction
+      // reads this word starts the next pass's reduction.  Stored before the
+      // result goes to (possibly host-mapped) `out`, so that the release does
+      // not wait for those writes to cross to the host.
       if (thr_word != nullptr)
         asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(thr_word),
                      "l"((static_cast<unsigned long long>(static_cast<uint32_t>(seq)) << 32) | __float_as_uint(thr))
                      : "memory");
     }
+#pragma unroll
+    for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
     if (kPublish) {
       if (t_start != nullptr) {
         unsigned long long* tw = reinterpret_cast<unsigned long long*>(out + kMomentSlots + 2);
-        tw[0] = __ldcg(t_start);
+        tw[0] = t_cmd;
         tw[1] = global_ns();
       }
       __threadfence_system();

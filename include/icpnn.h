@@ -214,10 +214,16 @@ typedef struct icpnn_iter_record {
     double sigma2;       /* mean squared residual under the first solve (residual
                             rejection only, else 0) */
     double T[16];        /* row-major transform this pass used (before the solve) */
-    float kernel_ms;     /* device time of the pass (with ICPNN_TRACE_TIMING), else 0;
-                            a pre-launched pass's time includes its wait for the
+    float kernel_ms;     /* device time of the pass (with ICPNN_TRACE_TIMING), else 0:
+                            on the persistent kernel's clock from the command
+                            reaching the GPU to the result published; CUDA events
+                            around the launch otherwise, where a one-at-a-time
+                            pre-launched pass's time includes its wait for the
                             transform (ICPNN_NO_PRELAUNCH times the kernel alone) */
-    float reserved;
+    float residual_ms;   /* with ICPNN_TRACE_TIMING and ICPNN_RESIDUAL_REJECT in the
+                            persistent kernel: device time of the iteration's two
+                            residual passes (command seen to the second's result
+                            published), else 0 */
 } icpnn_iter_record;
 
 /* icpnn_icp_step -- one fused correspondence pass under a given float32
@@ -340,12 +346,14 @@ int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames, const floa
  *   the same moments up to float rounding order (the points are visited in
  *   the caller's order, not Morton order, so partial sums associate
  *   differently).
- *   src          n x 3 float32, DEVICE memory (host pointers are rejected).
+ *   src          n x 3 float32, memory of the current device (host pointers
+ *                and other GPUs' memory are rejected).
  *   n            1 .. ICPNN_NOALLOC_MAX_POINTS; larger n is rejected with
  *                ICPNN_ERR_INVALID_ARG (one thread per point; one partial
  *                record per 256 points must fit the scratch array).
  *   R, t, max_corr_dist, out   as for icpnn_icp_step.
- *   idx, dist2   both NULL or both DEVICE buffers of n entries.
+ *   idx, dist2   both NULL or both buffers of n entries in the current
+ *                device's memory.
  * Scratch: a fixed file-scope device array of ICPNN_NOALLOC_MAX_POINTS/256
  * partial records plus a few words (about 576 KB), created when the library
  * is loaded and held by every GPU that loads it until the process exits.  No

@@ -85,3 +85,26 @@ def test_noalloc_limits(setup):
     # a rejected call leaves the shared scratch usable
     m = nn.icp_step_noalloc(tree, src, R, t, c.max_corr_dist[0])
     _close(m, nn.icp_step(tree, src, R, t, c.max_corr_dist[0]), c.extent)
+
+
+def test_noalloc_pass_at_its_largest_size(setup):
+    """n = NOALLOC_MAX_POINTS uses the scratch array to its last partial
+    record and counter word: the same results as icp_step, twice in a row."""
+    import torch
+    nn, c, tree, _ = setup
+    n = nn.NOALLOC_MAX_POINTS
+    reps = -(-n // len(c.source))
+    jitter = np.repeat(np.arange(reps, dtype=np.float32) * np.float32(1e-3), len(c.source))[:, None]
+    pts = np.ascontiguousarray((np.tile(c.source, (reps, 1)) + jitter)[:n], np.float32)
+    src = torch.from_numpy(pts).cuda()
+    R = c.T_gt[:3, :3].astype(np.float32)
+    t = c.T_gt[:3, 3].astype(np.float32)
+    idx_r, d2_r = _outputs(n)
+    ref = nn.icp_step(tree, src, R, t, c.max_corr_dist[0], idx_r, d2_r)
+    for _ in range(2):
+        idx, d2 = _outputs(n)
+        m = nn.icp_step_noalloc(tree, src, R, t, c.max_corr_dist[0], idx, d2)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(idx.cpu().numpy(), idx_r.cpu().numpy())
+        np.testing.assert_array_equal(d2.cpu().numpy().view(np.uint32), d2_r.cpu().numpy().view(np.uint32))
+        _close(m, ref, c.extent)
