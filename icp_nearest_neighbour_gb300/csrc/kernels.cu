@@ -806,16 +806,20 @@ __device__ __forceinline__ float float_threshold_dev(double limit) {
 // found no command in time.  counter[1] collects them; the last block
 // publishes the result only if every block ran.
 //
-// Grids of more than kSingleLevelBlocks blocks reduce in two fixed-order
-// levels: the last block to finish of each group of kGroupBlocks consecutive
-// blocks (counter[2 + group]) adds the group's partials in block order, one
-// load per thread, and stores the sum over the group's first partial; the
-// last group to finish (counter[0]) adds the group sums in a fixed order.
-// (One level over a 391-block grid, the last block adding every partial, put
-// ~28 L2 loads per thread on the critical path: 4.2 us.)  Smaller grids keep
-// one level: the last block (counter[0]) adds at most four rows per thread.
+// Grids of up to kSingleLevelBlocks blocks (every grid of the search kernels:
+// at most three blocks per SM) reduce in one level: the last block to finish
+// (counter[0]) adds every block's partial, each thread loading its (up to
+// kRowsPerThread) rows at once, so the whole sum costs one round trip to L2.
+// (Issued four at a time, the 28 rows per thread of a 391-block grid took
+// 4.2 us; a two-level scheme took 3.6 us for its two levels.)  Larger grids
+// reduce in two fixed-order levels: the last block to finish of each group of
+// kGroupBlocks consecutive blocks (counter[2 + group]) adds the group's
+// partials in block order, one load per thread, and stores the sum over the
+// group's first partial; the last group to finish (counter[0]) adds the group
+// sums.
 constexpr unsigned int kSkipStopped = 1u, kSkipTimedOut = 1u << 16;
-constexpr unsigned int kSingleLevelBlocks = 4 * kGroupBlocks;
+constexpr int kRowsPerThread = 33;
+constexpr unsigned int kSingleLevelBlocks = kRowsPerThread * (kThreads / kMomentSlots);
 static_assert(kGroupBlocks * kMomentSlots <= kThreads, "one thread per partial of a group");
 
 // Release-only increment: orders this thread's earlier stores before the
@@ -873,17 +877,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     double s = 0.0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
-    if (kPersistent)
-      s_fin[0][threadIdx.x] = s;
-    else
-      partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + threadIdx.x] = s;
-  }
-  if (!kPersistent) {
-    if (threadIdx.x == 0 && skipped != 0u) atomicAdd(counter + 1, skipped);
-    __threadfence();
+    s_fin[0][threadIdx.x] = s;
   }
   __syncthreads();
-  if (kPersistent && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v)
       partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + v] = s_fin[0][v];
@@ -897,16 +894,11 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     const unsigned int group = blockIdx.x / kGroupBlocks, g0 = group * kGroupBlocks;
     const unsigned int in_group = min(static_cast<unsigned int>(kGroupBlocks), gridDim.x - g0);
     if (threadIdx.x == 0)
-      s_last = ((kPersistent ? atom_add_release_gpu(counter + 2 + group, 1u)
-                             : atomicAdd(counter + 2 + group, 1u)) == in_group - 1);
+      s_last = (atom_add_release_gpu(counter + 2 + group, 1u) == in_group - 1);
     __syncthreads();
     if (!s_last) return;
-    if (kPersistent) {
-      if (threadIdx.x == 0) fence_acq_rel_gpu();
-      __syncthreads();
-    } else {
-      __threadfence();
-    }
+    if (threadIdx.x == 0) fence_acq_rel_gpu();
+    __syncthreads();
     if (threadIdx.x < kGroupBlocks * kMomentSlots)
       s_fin[r][v] = static_cast<unsigned int>(r) < in_group
                         ? __ldcg(&partials[static_cast<int64_t>(g0 + r) * kMomentSlots + v]) : 0.0;
@@ -914,17 +906,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     if (threadIdx.x < kMomentSlots) {
       double s = 0.0;
       for (unsigned int k = 0; k < in_group; ++k) s += s_fin[k][threadIdx.x];
-      if (kPersistent)
-        s_warp[0][threadIdx.x] = s;
-      else
-        partials[static_cast<int64_t>(g0) * kMomentSlots + threadIdx.x] = s;
-    }
-    if (!kPersistent) {
-      if (threadIdx.x == 0) counter[2 + group] = 0u;
-      __threadfence();
+      s_warp[0][threadIdx.x] = s;
     }
     __syncthreads();
-    if (kPersistent && threadIdx.x == 0) {
+    if (threadIdx.x == 0) {
 #pragma unroll
       for (int u = 0; u < kMomentSlots; ++u) partials[static_cast<int64_t>(g0) * kMomentSlots + u] = s_warp[0][u];
       counter[2 + group] = 0u;  // ordered before the next level's release increment
@@ -933,38 +918,34 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     row_stride = kGroupBlocks;
   }
   if (threadIdx.x == 0)
-    s_last = ((kPersistent ? atom_add_release_gpu(counter, 1u) : atomicAdd(counter, 1u)) == rows - 1);
+    s_last = (atom_add_release_gpu(counter, 1u) == rows - 1);
   __syncthreads();
   if (!s_last) return;
-  // the last block: in the persistent kernel, thread 0 starts the reads it
-  // needs at the end (skipped blocks, the pass's start time) now, so that
-  // their latency overlaps the sum below
+  // the last block: thread 0 starts the reads it needs at the end (skipped
+  // blocks, the pass's start time) now, so that their latency overlaps the
+  // sum below
   unsigned int skips = 0u;
   unsigned long long t_cmd = 0ull;
-  if (kPersistent) {
-    if (threadIdx.x == 0) {
-      fence_acq_rel_gpu();
-      skips = atomicExch(counter + 1, 0u);
-      if (t_start != nullptr) t_cmd = __ldcg(t_start);
-      counter[0] = 0u;
-    }
-    __syncthreads();
-  } else {
-    __threadfence();
+  if (threadIdx.x == 0) {
+    fence_acq_rel_gpu();
+    skips = atomicExch(counter + 1, 0u);
+    if (t_start != nullptr) t_cmd = __ldcg(t_start);
+    counter[0] = 0u;
   }
+  __syncthreads();
   constexpr int kGroups = kThreads / kMomentSlots;
   if (threadIdx.x < kGroups * kMomentSlots) {
-    // rows r, r + 14, ... in order, up to four loads in flight
+    // rows r, r + 14, ... added in order; all of a batch's loads in flight at once
     double s = 0.0;
-    for (unsigned int j = r; j < rows; j += 4 * kGroups) {
-      double x[4];
+    for (unsigned int j = r; j < rows; j += kRowsPerThread * kGroups) {
+      double x[kRowsPerThread];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kRowsPerThread; ++u) {
         const unsigned int row = j + u * kGroups;
         x[u] = row < rows ? __ldcg(&partials[static_cast<int64_t>(row) * row_stride * kMomentSlots + v]) : 0.0;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kRowsPerThread; ++u)
         if (j + u * kGroups < rows) s += x[u];
     }
     s_fin[r][v] = s;
@@ -981,10 +962,6 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // orders its own stores, the sequence word: the host never sees the new
   // sequence before the values.
   if (threadIdx.x == 0) {
-    if (!kPersistent) {
-      *counter = 0u;
-      skips = atomicExch(counter + 1, 0u);
-    }
     if (skips != 0u) {
       // The abort marker has a word of its own: the pass queued behind this
       // one may give up too, and its marker must not overwrite this pass's
