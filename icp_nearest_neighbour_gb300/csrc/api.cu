@@ -844,7 +844,9 @@ int icpnn_nn_query(const icpnn_tree* t, const float* xyz, int64_t n, int32_t* id
     Source src;
     if (int rc = prepare_source(xyz, n, (flags & ICPNN_MORTON_SORT) != 0, false, s, sc, &src)) return rc;
     if (int rc = bind_point_outputs(idx, dist2, n, sc, &po)) return rc;
-    ICPNN_CUDA(launch_nn(*t, src.recs, n, po.idx, po.d2, s));
+    uint32_t* chunk_counter = nullptr;
+    ICPNN_CUDA(sc.alloc(&chunk_counter, 1));
+    ICPNN_CUDA(launch_nn(*t, src.recs, n, po.idx, po.d2, chunk_counter, s));
     if (int rc = copy_back(po, n, s)) return rc;
   }
   return ICPNN_OK;

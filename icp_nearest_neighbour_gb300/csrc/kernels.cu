@@ -755,25 +755,34 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
                                                       const float4* __restrict__ pts, int smem_slots,
                                                       const float4* __restrict__ q, int64_t n,
                                                       int32_t* __restrict__ out_idx,
-                                                      float* __restrict__ out_d2) {
+                                                      float* __restrict__ out_d2,
+                                                      unsigned int* __restrict__ chunk_counter) {
   extern __shared__ __align__(16) uint2 s_nodes[];
   stage_top(nodes, s_nodes, smem_slots);
   const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
   const int lane = threadIdx.x & 31;
-  for (int64_t c = first_chunk(); c * 32 < n; c += chunk_stride()) {
+  // The grid is one wave; with more queries than resident warps each warp
+  // starts at its own chunk (warps of a block on consecutive chunks) and then
+  // takes the next unclaimed chunk from a counter, so that warps whose chunks
+  // were cheap take over the rest instead of waiting for a fixed share.
+  for (int64_t c = first_chunk(); c * 32 < n;) {
     const int64_t i = c * 32 + lane;
-    if (i >= n) continue;
-    const float4 r = q[i];
-    const int32_t slot = __float_as_int(r.w);
-    if (!finite3(r.x, r.y, r.z)) {
-      out_idx[slot] = -1;
-      out_d2[slot] = __int_as_float(0x7fc00000);
-      continue;
+    if (i < n) {
+      const float4 r = q[i];
+      const int32_t slot = __float_as_int(r.w);
+      if (!finite3(r.x, r.y, r.z)) {
+        out_idx[slot] = -1;
+        out_d2[slot] = __int_as_float(0x7fc00000);
+      } else {
+        Best b = make_best(__int_as_float(0x7f800000));
+        search(tv, r.x, r.y, r.z, b);
+        out_idx[slot] = b.idx() == INT_MAX ? -1 : b.idx();
+        out_d2[slot] = b.d2();
+      }
     }
-    Best b = make_best(__int_as_float(0x7f800000));
-    search(tv, r.x, r.y, r.z, b);
-    out_idx[slot] = b.idx() == INT_MAX ? -1 : b.idx();
-    out_d2[slot] = b.d2();
+    unsigned int next = 0;
+    if (lane == 0) next = atomicAdd(chunk_counter, 1u);
+    c = chunk_stride() + __shfl_sync(kFull, next, 0);
   }
 }
 
@@ -1545,8 +1554,10 @@ cudaError_t launch_gather(const float* xyz, int64_t n, const uint32_t* perm, flo
 }
 
 cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int32_t* idx,
-                      float* dist2, cudaStream_t s) {
+                      float* dist2, uint32_t* chunk_counter, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
+  const cudaError_t ze = cudaMemsetAsync(chunk_counter, 0, sizeof(uint32_t), s);
+  if (ze != cudaSuccess) return ze;
   const int slots = smem_slots_for(t);
   const size_t smem = static_cast<size_t>(slots) * sizeof(uint2);
   int per_sm = 0;
@@ -1555,7 +1566,7 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
   nn_kernel<<<grid, kThreads, smem, s>>>(reinterpret_cast<const uint2*>(t.dev.nodes),
                                           reinterpret_cast<const float4*>(t.dev.boxes),
                                           reinterpret_cast<const float4*>(t.dev.points), slots,
-                                          queries, n, idx, dist2);
+                                          queries, n, idx, dist2, chunk_counter);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

@@ -120,8 +120,10 @@ cudaError_t launch_gather(const float* xyz, int64_t n, const uint32_t* perm, flo
                           cudaStream_t s);
 
 // Exact 1-NN of every record; writes idx/dist2 at the record's original slot.
+// chunk_counter: one device word (zeroed here, on the stream) from which the
+// warps take chunks of queries beyond their first.
 cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int32_t* idx,
-                      float* dist2, cudaStream_t s);
+                      float* dist2, uint32_t* chunk_counter, cudaStream_t s);
 
 // One fused ICP pass: transform, search, reject, reduce.  `partials` holds
 // grid * kMomentSlots doubles, `counter` reduction_counter_words(grid) zeroed
