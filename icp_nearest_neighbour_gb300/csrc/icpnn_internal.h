@@ -5,7 +5,9 @@
 
 #include <cstdint>
 #include <functional>
+#include <memory>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "icpnn.h"
@@ -57,6 +59,33 @@ struct DeviceTree {
 
 }  // namespace icpnn
 
+namespace icpnn {
+
+// Allocator whose value-less construct leaves the element uninitialised, so
+// that resizing a vector the caller is about to overwrite costs no fill.
+template <class T>
+struct UninitAllocator : std::allocator<T> {
+  template <class U>
+  struct rebind {
+    using other = UninitAllocator<U>;
+  };
+  UninitAllocator() = default;
+  template <class U>
+  UninitAllocator(const UninitAllocator<U>&) noexcept {}
+  template <class U>
+  void construct(U* p) noexcept {
+    ::new (static_cast<void*>(p)) U;
+  }
+  template <class U, class... A>
+  void construct(U* p, A&&... a) {
+    ::new (static_cast<void*>(p)) U(std::forward<A>(a)...);
+  }
+};
+template <class T>
+using UninitVector = std::vector<T, UninitAllocator<T>>;
+
+}  // namespace icpnn
+
 struct icpnn_tree {
   int64_t n = 0;
   int32_t leaf_size = 0;
@@ -67,11 +96,11 @@ struct icpnn_tree {
   int64_t heap_slots = 0;     // 2^(depth+1)
   float bbox_lo[3] = {0, 0, 0};
   float bbox_hi[3] = {0, 0, 0};
-  std::vector<icpnn::Node> nodes;   // heap layout, heap_slots entries
-  std::vector<float> records;       // 4 floats per point, leaf order
+  icpnn::UninitVector<icpnn::Node> nodes;   // heap layout, heap_slots entries
+  icpnn::UninitVector<float> records;       // 4 floats per point, leaf order
   // Tight bounding box of each node's points, 8 floats per heap slot:
   // lo.x, lo.y, lo.z, 0, hi.x, hi.y, hi.z, 0 (unused slots zero).
-  std::vector<float> boxes;
+  icpnn::UninitVector<float> boxes;
   icpnn::DeviceTree dev;
   // Built on the device: nodes, boxes and records exist there only until a
   // caller needs them on the host (export, upload to another device).

@@ -14,15 +14,15 @@
 // deviation of the node, which always holds the median; outside values clamp
 // to the end bins) and one scatter pass that writes the records below, inside
 // and above the median's bin to the node's range of a second buffer; an
-// nth_element over that bin alone then places the median.  The scatter pass
-// also sums the two children's coordinates and squares, so a child knows its
-// mean and variance without reading its records again.  Smaller nodes use
-// nth_element and one pass for the children's sums.
+// nth_element over that bin alone then places the median.  Smaller nodes use
+// nth_element.  One more pass sums the two children's coordinates and squares,
+// so a child knows its mean and variance without reading its records again.
 //
 // Variance: sums of x - c and (x - c)^2 in double about the parent's mean c,
 // var = q/n - (s/n)^2.  The page fixes no formula; the rounding differs from
 // a two-pass sum by parts in 1e15, far inside the relative 1e-9 within which
-// axes count as tied (the lowest tied axis wins).
+// axes count as tied (the lowest tied axis wins).  The root's sums are taken
+// about its first point, in the same pass that writes the records.
 //
 // Each node also gets the tight bounding box of its points (leaves from their
 // records, inner nodes as the union of their children's) for the search's
@@ -34,9 +34,9 @@
 // The chunking depends on the node's size only, so the tree is the same on
 // every machine and thread count.
 #include <algorithm>
-#include <atomic>
 #include <cmath>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <thread>
 #include <vector>
@@ -52,15 +52,16 @@ struct Rec {
 };
 static_assert(sizeof(Rec) == 16, "record must match the device float4 layout");
 
-constexpr int64_t kChunk = 16384;    // records per chunk of a parallel node pass
+constexpr int64_t kChunk = 8192;    // records per chunk of a parallel node pass
 constexpr int64_t kMaxChunks = 64;
-constexpr int64_t kBucketMin = 32;  // smaller nodes use nth_element
+constexpr int64_t kBucketMin = 16;  // smaller nodes use nth_element
 
 int64_t chunks_for(int64_t count) { return std::min<int64_t>(kMaxChunks, count / kChunk); }
 
 // Sums over a set of records of x - c and (x - c)^2 per axis, c a fixed
-// centre, and the coordinate range per axis.
-struct Sums {
+// centre, and (kRange) the coordinate range per axis.
+template <bool kRange>
+struct SumsT {
   double n = 0.0;
   double s[3] = {0.0, 0.0, 0.0};
   double q[3] = {0.0, 0.0, 0.0};
@@ -72,40 +73,51 @@ struct Sums {
       const double x = static_cast<double>(r.c[d]) - c[d];
       s[d] += x;
       q[d] += x * x;
-      mn[d] = std::min(mn[d], r.c[d]);
-      mx[d] = std::max(mx[d], r.c[d]);
+      if (kRange) {
+        mn[d] = std::min(mn[d], r.c[d]);
+        mx[d] = std::max(mx[d], r.c[d]);
+      }
     }
   }
-  void add(const Sums& o) {
+  void add(const SumsT& o) {
     n += o.n;
     for (int d = 0; d < 3; ++d) {
       s[d] += o.s[d];
       q[d] += o.q[d];
-      mn[d] = std::min(mn[d], o.mn[d]);
-      mx[d] = std::max(mx[d], o.mx[d]);
+      if (kRange) {
+        mn[d] = std::min(mn[d], o.mn[d]);
+        mx[d] = std::max(mx[d], o.mx[d]);
+      }
     }
   }
 };
+using Sums = SumsT<true>;
+using FastSums = SumsT<false>;  // the children's sums, the build's hottest pass
 
 // A node's mean and population variance per axis.  An axis on which all
 // coordinates are equal has variance exactly 0 (as a direct two-pass sum of
 // float coordinates gives), not the rounding left over by q/n - (s/n)^2.
 // `accurate` is false when the subtraction lost too much: the mean of
 // (x - c)^2 is more than 16 times the variance, i.e. c lies far from the
-// records; the caller then sums again about the mean just found.
+// records; the caller then sums again about the mean just found.  Sums
+// without the range cannot tell an axis of equal coordinates (unless all
+// equal c) from a narrow one: its variance comes out as rounding, is flagged
+// as not accurate, and the second sum, which has the range, settles it.
 struct Moments {
   double mean[3];
   double var[3];
   bool accurate;
-  static Moments from(const Sums& u, const double c[3]) {
+  template <bool kRange>
+  static Moments from(const SumsT<kRange>& u, const double c[3]) {
     Moments m;
     m.accurate = true;
     for (int d = 0; d < 3; ++d) {
       const double a = u.s[d] / u.n;
       const double q = u.q[d] / u.n;
+      const bool flat = kRange && u.mn[d] == u.mx[d];
       m.mean[d] = c[d] + a;
-      m.var[d] = u.mn[d] == u.mx[d] ? 0.0 : std::max(0.0, q - a * a);
-      if (u.mn[d] != u.mx[d] && !(q <= 16.0 * m.var[d])) m.accurate = false;
+      m.var[d] = flat ? 0.0 : std::max(0.0, q - a * a);
+      if (!flat && !(q <= 16.0 * m.var[d])) m.accurate = false;
     }
     return m;
   }
@@ -123,7 +135,6 @@ struct Builder {
   float* box = nullptr;  // 8 floats per heap slot
   int parallel_depth = 0;
   bool round_robin = false;  // axis = depth mod 3 instead of largest variance
-  std::atomic<int64_t> n_nodes{0};
 
   bool is_leaf(int64_t count, int depth) const { return count <= leaf_size || depth >= max_depth; }
 
@@ -150,14 +161,17 @@ struct Builder {
     int nb = 16;
     while (nb < count / 4 && nb < 4096) nb *= 2;
     const double sd = std::sqrt(mo.var[axis]);
-    const double base = mo.mean[axis] - sd;
+    const float base = static_cast<float>(mo.mean[axis] - sd);
     // a spread too small to scale (or none) puts every record in one bin
-    const double scale = sd > 0.0 && nb / (2.0 * sd) < 1e300 ? nb / (2.0 * sd) : 0.0;
-    const double top = nb - 1;
-    // monotone in v: a lower bin never holds a larger coordinate
+    const double scale_d = nb / (2.0 * sd);
+    const float scale = sd > 0.0 && scale_d < 1e30 ? static_cast<float>(scale_d) : 0.f;
+    const float top = static_cast<float>(nb - 1);
+    // Monotone in v, since float rounding is monotone and the scale is not
+    // negative: a lower bin never holds a larger coordinate.  A difference
+    // that overflows clamps to an end bin.
     auto bin = [=](float v) {
-      const double x = (static_cast<double>(v) - base) * scale;
-      return static_cast<int>(std::min(std::max(x, 0.0), top));
+      const float x = scale == 0.f ? 0.f : (v - base) * scale;
+      return static_cast<int>(std::min(std::max(x, 0.f), top));
     };
     const int64_t C = std::max<int64_t>(1, chunks_for(count));
     auto chunk_lo = [=](int64_t k) { return lo + count * k / C; };
@@ -227,16 +241,16 @@ struct Builder {
   }
 
   // Sums about c of the records [lo, lo + m) and [lo + m, hi) of buf[b].
-  void child_sums(int b, int64_t lo, int64_t hi, int64_t m, const double c[3], Sums* left, Sums* right) const {
+  void child_sums(int b, int64_t lo, int64_t hi, int64_t m, const double c[3], FastSums* left, FastSums* right) const {
     const int64_t count = hi - lo;
     const Rec* r = buf[b];
     const int64_t C = std::max<int64_t>(1, chunks_for(count));
-    Sums part_small[2];
-    std::vector<Sums> part_big(C > 1 ? static_cast<size_t>(2 * C) : 0);
-    Sums* part = C > 1 ? part_big.data() : part_small;
+    FastSums part_small[2];
+    std::vector<FastSums> part_big(C > 1 ? static_cast<size_t>(2 * C) : 0);
+    FastSums* part = C > 1 ? part_big.data() : part_small;
     auto body = [=](int k) {
       const int64_t b0 = lo + count * k / C, b1 = lo + count * (k + 1) / C, mid = lo + m;
-      Sums sl, sr;
+      FastSums sl, sr;
       for (int64_t i = b0; i < std::min(b1, mid); ++i) sl.add(r[i], c);
       for (int64_t i = std::max(b0, mid); i < b1; ++i) sr.add(r[i], c);
       part[2 * k] = sl;
@@ -251,8 +265,10 @@ struct Builder {
 
   // Builds the subtree of `node` over [lo, hi) of buf[b]; mo are the node's
   // moments.  Leaves copy their records into buf[0] if they sit in buf[1].
-  void build(uint64_t node, int b, int64_t lo, int64_t hi, int depth, const Moments& mo) {
-    n_nodes.fetch_add(1, std::memory_order_relaxed);
+  // Returns the number of nodes in the subtree.  (Not a shared atomic
+  // counter: on the 16 Arm cores of a GB300 host, every thread incrementing
+  // one cache line per node made the build three times slower.)
+  int64_t build(uint64_t node, int b, int64_t lo, int64_t hi, int depth, const Moments& mo) {
     const int64_t count = hi - lo;
     if (is_leaf(count, depth)) {
       if (b == 1) std::memcpy(buf[0] + lo, buf[1] + lo, static_cast<size_t>(count) * sizeof(Rec));
@@ -268,7 +284,7 @@ struct Builder {
           bx[d] = std::min(bx[d], buf[0][i].c[d]);
           bx[4 + d] = std::max(bx[4 + d], buf[0][i].c[d]);
         }
-      return;
+      return 1;
     }
     const int axis = round_robin ? depth % 3 : widest_axis(mo);
     const int64_t m = count / 2;
@@ -281,21 +297,22 @@ struct Builder {
     // the children's moments, unless both are leaves (which need none)
     Moments ml{}, mr{};
     if (!is_leaf(count - m, depth + 1)) {
-      Sums sl, sr;
+      FastSums sl, sr;
       child_sums(nb, lo, hi, m, mo.mean, &sl, &sr);
       ml = Moments::from(sl, mo.mean);
       mr = Moments::from(sr, mo.mean);
       if (!ml.accurate) ml = moments_about(nb, lo, lo + m, ml.mean);
       if (!mr.accurate) mr = moments_about(nb, lo + m, hi, mr.mean);
     }
+    int64_t below[2];
     if (depth < parallel_depth && count >= (1 << 13)) {
       parallel_for(2, [&](int side) {
-        if (side == 0) build(2 * node, nb, lo, lo + m, depth + 1, ml);
-        else build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
+        if (side == 0) below[0] = build(2 * node, nb, lo, lo + m, depth + 1, ml);
+        else below[1] = build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
       });
     } else {
-      build(2 * node, nb, lo, lo + m, depth + 1, ml);
-      build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
+      below[0] = build(2 * node, nb, lo, lo + m, depth + 1, ml);
+      below[1] = build(2 * node + 1, nb, lo + m, hi, depth + 1, mr);
     }
     float* bx = box + 8 * node;
     const float* l = box + 16 * node;
@@ -304,6 +321,7 @@ struct Builder {
       bx[d] = std::min(l[d], r[d]);
       bx[4 + d] = std::max(l[4 + d], r[4 + d]);
     }
+    return 1 + below[0] + below[1];
   }
 
   // Moments of the records [lo, hi) of buf[b] from sums about c.
@@ -326,13 +344,6 @@ struct Builder {
     return Moments::from(tot, c);
   }
 
-  // Moments of the whole cloud: sums about the origin give the mean, then
-  // sums about the mean.
-  Moments root_moments(int64_t n) const {
-    const double zero[3] = {0.0, 0.0, 0.0};
-    const Moments first = moments_about(0, 0, n, zero);
-    return moments_about(0, 0, n, first.mean);
-  }
 };
 
 }  // namespace
@@ -352,65 +363,66 @@ int32_t tree_depth(int64_t n, int32_t leaf_size, int32_t max_depth) {
 
 int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth, bool round_robin,
                icpnn_tree* t) {
-  // one pass, chunked over the pool: finiteness check, records and bounding box
-  const int64_t C = std::max<int64_t>(1, std::min<int64_t>(kMaxChunks, n / (4 * kChunk)));
+  // One pass, chunked over the pool: finiteness check, records, the root's
+  // sums (about the first point) and range, and the zeroing of the node and
+  // box arrays.  Chunk sums are added in chunk order.
+  const int64_t C = std::max<int64_t>(1, std::min<int64_t>(kMaxChunks, n / kChunk));
   try {
     std::vector<int64_t> first_bad(static_cast<size_t>(C), -1);
-    std::vector<float> box(static_cast<size_t>(6 * C));
+    std::vector<Sums> part(static_cast<size_t>(C));
     const int32_t depth = tree_depth(n, leaf_size, max_depth);
     const int64_t largest_leaf = (n + (int64_t{1} << depth) - 1) >> depth;
     if (largest_leaf >= (int64_t{1} << 30))
       return fail(ICPNN_ERR_INVALID_ARG, "kdtree_build: a leaf would hold 2^30 points or more");
+    const int64_t slots = int64_t{1} << (depth + 1);
     t->records.resize(static_cast<size_t>(4 * n));
+    t->nodes.resize(static_cast<size_t>(slots));
+    t->boxes.resize(static_cast<size_t>(8 * slots));
     Rec* recs = reinterpret_cast<Rec*>(t->records.data());
+    const double c0[3] = {xyz[0], xyz[1], xyz[2]};
     parallel_for(static_cast<int>(C), [&](int c) {
-      float lo[3] = {INFINITY, INFINITY, INFINITY};
-      float hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+      const int64_t s0 = slots * c / C, s1 = slots * (c + 1) / C;
+      std::memset(t->nodes.data() + s0, 0, static_cast<size_t>(s1 - s0) * sizeof(Node));
+      std::memset(t->boxes.data() + 8 * s0, 0, static_cast<size_t>(s1 - s0) * 8 * sizeof(float));
+      Sums u;
       for (int64_t i = n * c / C; i < n * (c + 1) / C; ++i) {
+        Rec r;
         for (int d = 0; d < 3; ++d) {
-          const float v = xyz[3 * i + d];
-          if (!std::isfinite(v)) {
+          r.c[d] = xyz[3 * i + d];
+          if (!std::isfinite(r.c[d])) {
             first_bad[static_cast<size_t>(c)] = i;
             return;
           }
-          recs[i].c[d] = v;
-          lo[d] = std::min(lo[d], v);
-          hi[d] = std::max(hi[d], v);
         }
-        recs[i].idx = static_cast<int32_t>(i);
+        r.idx = static_cast<int32_t>(i);
+        recs[i] = r;
+        u.add(r, c0);
       }
-      for (int d = 0; d < 3; ++d) {
-        box[static_cast<size_t>(6 * c + d)] = lo[d];
-        box[static_cast<size_t>(6 * c + 3 + d)] = hi[d];
-      }
+      part[static_cast<size_t>(c)] = u;
     });
     for (int64_t c = 0; c < C; ++c)
       if (first_bad[static_cast<size_t>(c)] >= 0)
         return fail(ICPNN_ERR_NONFINITE, "kdtree_build: non-finite coordinate at point " +
                                              std::to_string(first_bad[static_cast<size_t>(c)]));
+    Sums root;
+    for (int64_t c = 0; c < C; ++c) root.add(part[static_cast<size_t>(c)]);
     for (int d = 0; d < 3; ++d) {
-      t->bbox_lo[d] = INFINITY;
-      t->bbox_hi[d] = -INFINITY;
-      for (int64_t c = 0; c < C; ++c) {
-        t->bbox_lo[d] = std::min(t->bbox_lo[d], box[static_cast<size_t>(6 * c + d)]);
-        t->bbox_hi[d] = std::max(t->bbox_hi[d], box[static_cast<size_t>(6 * c + 3 + d)]);
-      }
+      t->bbox_lo[d] = root.mn[d];
+      t->bbox_hi[d] = root.mx[d];
     }
     t->n = n;
     t->leaf_size = leaf_size;
     t->max_depth = max_depth;
     t->round_robin = round_robin;
     t->depth = depth;
-    t->heap_slots = int64_t{1} << (depth + 1);
-    t->nodes.assign(static_cast<size_t>(t->heap_slots), Node{0u, 0u});
-    t->boxes.assign(static_cast<size_t>(8 * t->heap_slots), 0.f);
+    t->heap_slots = slots;
 
-    std::vector<Rec> temp(static_cast<size_t>(n));
+    std::unique_ptr<Rec[]> temp(new Rec[static_cast<size_t>(n)]);
     Builder b;
     b.leaf_size = leaf_size;
     b.max_depth = max_depth;
     b.buf[0] = recs;
-    b.buf[1] = temp.data();
+    b.buf[1] = temp.get();
     b.heap = t->nodes.data();
     b.box = t->boxes.data();
     b.round_robin = round_robin;
@@ -418,8 +430,9 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
     int pd = 0;
     while ((1u << pd) < 4 * hw && pd < 8) ++pd;
     b.parallel_depth = pd;
-    b.build(1, 0, 0, n, 0, b.root_moments(n));
-    t->n_nodes = b.n_nodes.load();
+    Moments mo = Moments::from(root, c0);
+    if (!mo.accurate) mo = b.moments_about(0, 0, n, mo.mean);
+    t->n_nodes = b.build(1, 0, 0, n, 0, mo);
   } catch (const std::bad_alloc&) {
     return fail(ICPNN_ERR_NO_MEMORY, "kdtree_build: host allocation failed");
   }

@@ -50,6 +50,11 @@ def _tree_clouds():
         "single": (np.array([[1.0, 2.0, 3.0]], np.float32), 8),
         "scene": (W.scene_case(20_000, 10).target, 12),
         "tiny_case": (W.tiny_case().target, 8),
+        # the root's variance is first summed about the first point: far from
+        # the rest it leaves too little precision and the sum is taken again
+        "outlier_first": (np.vstack([[[4e4, -3e4, 2e4]], W.uniform_cloud(3000, 5)]).astype(np.float32), 8),
+        "all_same": (np.tile(np.float32([[0.3, -1.7, 2.5]]), (200, 1)), 4),
+        "two_flat_axes": (np.c_[rng.uniform(-1, 1, 2000), np.full(2000, 0.7), np.full(2000, -2.0)].astype(np.float32), 6),
     }
 
 
