@@ -159,7 +159,7 @@ struct Builder {
     }
     Rec* dst = buf[b ^ 1];
     int nb = 16;
-    while (nb < count / 4 && nb < 4096) nb *= 2;
+    while (nb < count / 4 && nb < 1024) nb *= 2;
     const double sd = std::sqrt(mo.var[axis]);
     const float base = static_cast<float>(mo.mean[axis] - sd);
     // a spread too small to scale (or none) puts every record in one bin
