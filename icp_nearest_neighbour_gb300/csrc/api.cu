@@ -490,7 +490,8 @@ void tagged_command(const MappedBuffer* mb, unsigned long long seq, const float*
   }
   TaggedCommand* c = tagged_block(mb);
   if (R != nullptr) {
-    const unsigned long long high = (seq & 0xffffffffull) << 32;
+    const unsigned long long high = static_cast<unsigned long long>(
+                                        static_cast<uint32_t>((seq << 2) | kind) | 0x80000000u) << 32;
     for (int j = 0; j < 12; ++j) {
       uint32_t bits;
       std::memcpy(&bits, j < 9 ? &R[j] : &tr[j - 9], sizeof(bits));

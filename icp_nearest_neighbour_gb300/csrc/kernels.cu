@@ -1318,32 +1318,47 @@ __device__ __forceinline__ void store_relaxed_gpu(unsigned long long* a, unsigne
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(a), "l"(v) : "memory");
 }
 
-// Read the 12 tagged words at `a` into rt (two at a time); true if every tag
-// names the pass.
+// Tag of a command's words: the pass's sequence number and the command's kind,
+// with the top bit set so that zeroed memory never carries a valid tag.
+__device__ __forceinline__ uint32_t command_tag(unsigned long long seq, unsigned long long kind) {
+  return static_cast<uint32_t>((seq << 2) | kind) | 0x80000000u;
+}
+
+// Read the 12 tagged words at `a` into rt (all six 16-byte loads in flight at
+// once).  Returns the kind of command they name for pass seq (kCmdPass or
+// kCmdResidual) when all twelve carry that one tag, else -1.
 template <bool kSystem>
-__device__ __forceinline__ bool load_tagged(const unsigned long long* a, uint32_t tag, float* rt) {
-  bool ok = true;
+__device__ __forceinline__ int load_tagged(const unsigned long long* a, unsigned long long seq, float* rt) {
+  unsigned long long w[12];
 #pragma unroll
   for (int k = 0; k < 6; ++k) {
-    unsigned long long w0, w1;
     if (kSystem)
-      asm volatile("ld.relaxed.sys.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a + 2 * k) : "memory");
+      asm volatile("ld.relaxed.sys.global.v2.u64 {%0, %1}, [%2];" : "=l"(w[2 * k]), "=l"(w[2 * k + 1]) : "l"(a + 2 * k) : "memory");
     else
-      asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a + 2 * k) : "memory");
-    ok = ok && static_cast<uint32_t>(w0 >> 32) == tag && static_cast<uint32_t>(w1 >> 32) == tag;
-    rt[2 * k] = __uint_as_float(static_cast<uint32_t>(w0));
-    rt[2 * k + 1] = __uint_as_float(static_cast<uint32_t>(w1));
+      asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w[2 * k]), "=l"(w[2 * k + 1]) : "l"(a + 2 * k) : "memory");
   }
-  return ok;
+  const uint32_t t0 = static_cast<uint32_t>(w[0] >> 32);
+  bool same = true;
+#pragma unroll
+  for (int k = 0; k < 12; ++k) {
+    same = same && static_cast<uint32_t>(w[k] >> 32) == t0;
+    rt[k] = __uint_as_float(static_cast<uint32_t>(w[k]));
+  }
+  if (!same) return -1;
+  if (t0 == command_tag(seq, kCmdPass)) return static_cast<int>(kCmdPass);
+  if (t0 == command_tag(seq, kCmdResidual)) return static_cast<int>(kCmdResidual);
+  return -1;
 }
 
 // One thread per block: wait until the tagged command names pass `seq` and
 // copy its R and t to rt.  Returns kRunPass, kRunResidual, kSkipStopped
 // (stop, or a later pass named) or kSkipTimedOut.  The first block to arrive
-// polls host memory for at most wait_ns and forwards what it found through
-// the mirror as (seq << 3) | code (codes: the host's kinds, or 3 = gave up);
-// the others poll the mirror for at most 2 * wait_ns.  No acquire fence: a
-// reader re-reads the payload until all its tags name the pass (bounded).
+// polls host memory for at most wait_ns, reading the control word and the
+// tagged payload together (one round trip over the CPU link per poll), and
+// forwards what it found through the mirror as (seq << 3) | code (codes: the
+// host's kinds, or 3 = gave up); the others poll the mirror's control word
+// for at most 2 * wait_ns, then read its payload.  No acquire fence: a reader
+// accepts the payload once all its tags name the pass and the kind.
 constexpr unsigned int kRunPass = 0u, kRunResidual = 2u;
 __device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, TaggedMirror* m,
                                                      unsigned long long seq, unsigned long long wait_ns,
@@ -1355,40 +1370,35 @@ __device__ __forceinline__ unsigned int await_tagged(const TaggedCommand* cmd, T
   if (atomicMax(&m->elect, seq) < seq) {
     for (;;) {
       const unsigned long long c = load_relaxed_sys(&cmd->ctrl);
+      const int kind = load_tagged<true>(cmd->words, seq, rt);
       const uint32_t ctag = static_cast<uint32_t>(c >> 2);
-      if (ctag == tag) {
-        outcome = c & 3ull;
-        if (outcome == kRun || outcome == kResidual) {
-          while (!load_tagged<true>(cmd->words, tag, rt)) {
-            if (global_ns() - t0 > wait_ns) {
-              outcome = kTimeout;
-              break;
-            }
-          }
-        }
-        break;
-      }
-      if (static_cast<int32_t>(ctag - tag) > 0) {
+      if (static_cast<int32_t>(ctag - tag) > 0 || (ctag == tag && (c & 3ull) == kStop)) {
         outcome = kStop;
         break;
       }
+      if (kind >= 0) {
+        outcome = static_cast<unsigned long long>(kind);
+        break;
+      }
       if (global_ns() - t0 > wait_ns) break;
-      __nanosleep(200);
+      __nanosleep(20);
     }
     if (outcome == kRun || outcome == kResidual) {
-      const unsigned long long high = static_cast<unsigned long long>(tag) << 32;
+      const unsigned long long high = static_cast<unsigned long long>(command_tag(seq, outcome)) << 32;
 #pragma unroll
       for (int k = 0; k < 12; ++k) store_relaxed_gpu(&m->words[k], high | __float_as_uint(rt[k]));
     }
     store_relaxed_gpu(&m->t_cmd, global_ns());
     store_relaxed_gpu(&m->ctrl, (seq << 3) | outcome);
   } else {
+    // The other blocks poll the control word alone (many of them wait while
+    // the last blocks of the previous pass still search), then read the payload.
     for (;;) {
       const unsigned long long c = load_relaxed_gpu(&m->ctrl);
       if ((c >> 3) >= seq) {
         outcome = (c >> 3) == seq ? (c & 7ull) : kStop;
         if (outcome == kRun || outcome == kResidual) {
-          while (!load_tagged<false>(m->words, tag, rt)) {
+          while (load_tagged<false>(m->words, seq, rt) != static_cast<int>(outcome)) {
             if (global_ns() - t0 > 2 * wait_ns) {
               outcome = kTimeout;
               break;

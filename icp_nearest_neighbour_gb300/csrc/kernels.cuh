@@ -48,15 +48,17 @@ struct alignas(16) CommandMirror {
 constexpr unsigned long long kCmdPass = 0, kCmdStop = 1, kCmdResidual = 2;
 
 // Command of the persistent registration kernel (host-mapped, written by the
-// host).  Every word carries the low 32 bits of the pass's sequence number in
+// host).  Every word carries a tag naming the pass and the command's kind in
 // its high half, so that a reader can tell a complete command from one caught
 // half-written without an acquire fence (which would invalidate the reader's
 // L1 cache, where the persistent kernel keeps the tree from pass to pass):
-// words[j] = (tag << 32) | float bits of rt[j] (R row-major, then t);
-// ctrl = (seq << 2) | kind: kCmdPass (a correspondence pass), kCmdStop (leave
-// the kernel) or kCmdResidual (the iteration's two residual passes, which use
-// sequence numbers seq and seq + 1).  The host writes the words first, then
-// ctrl.
+// words[j] = (tag << 32) | float bits of rt[j] (R row-major, then t), with
+// tag = low 32 bits of ((seq << 2) | kind) and the top bit set (zeroed memory
+// never carries a valid tag); ctrl = (seq << 2) | kind: kCmdPass (a
+// correspondence pass), kCmdStop (leave the kernel; no words) or kCmdResidual
+// (the iteration's two residual passes, which use sequence numbers seq and
+// seq + 1).  The host writes the words first, then ctrl; a run command is
+// taken from its words alone.
 struct alignas(16) TaggedCommand {
   unsigned long long words[12];
   unsigned long long ctrl;
