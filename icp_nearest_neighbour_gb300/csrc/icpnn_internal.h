@@ -137,6 +137,8 @@ int build_tree_device(const float* xyz_dev, int64_t n, int32_t leaf_size, int32_
 // the first exception a task throws is rethrown to the caller.
 void pool_submit(std::function<void()> job, int min_threads);
 void parallel_for(int tasks, const std::function<void(int)>& fn);
+// Wakes parked workers ahead of a burst of parallel_for calls.
+void pool_wake();
 
 // Host Kabsch solve (kabsch.cpp).  Returns ICPNN_OK or ICPNN_ERR_DEGENERATE.
 int kabsch_solve(const icpnn_moments& m, double T[16]);

@@ -367,6 +367,7 @@ int build_tree(const float* xyz, int64_t n, int32_t leaf_size, int32_t max_depth
   // sums (about the first point) and range, and the zeroing of the node and
   // box arrays.  Chunk sums are added in chunk order.
   const int64_t C = std::max<int64_t>(1, std::min<int64_t>(kMaxChunks, n / kChunk));
+  if (C > 1) pool_wake();  // the workers come up while the arrays are allocated
   try {
     std::vector<int64_t> first_bad(static_cast<size_t>(C), -1);
     std::vector<Sums> part(static_cast<size_t>(C));

@@ -118,6 +118,32 @@ def test_large_tree_matches_oracle_tree(lib, oracle_mod, name, round_robin):
                                   ["leaf_index"], ex["leaf_index"])
 
 
+def test_concurrent_builds_give_the_same_tree(lib):
+    """Several host threads build at once: their parallel regions share the
+    library's worker pool (nested, interleaved) and every tree still comes
+    out the same, leaf order included."""
+    import threading
+    pts = W.scene_case(60_000, 3).target
+    ref = lib.kdtree_export(lib.kdtree_build(pts, 12))
+    errors = []
+
+    def worker():
+        try:
+            for _ in range(6):
+                ex = lib.kdtree_export(lib.kdtree_build(pts, 12))
+                for k in ("split_val", "split_dim", "start", "end", "leaf_index"):
+                    np.testing.assert_array_equal(ex[k], ref[k], err_msg=k)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker) for _ in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[0]
+
+
 def test_tree_depth_cap(lib, oracle_mod):
     pts = W.uniform_cloud(3000, 4)
     t = lib.kdtree_build(pts, 1, max_depth=5)
