@@ -817,10 +817,12 @@ __device__ __forceinline__ float float_threshold_dev(double limit) {
 //
 // Grids of up to kSingleLevelBlocks blocks (every grid of the search kernels:
 // at most three blocks per SM) reduce in one level: the last block to finish
-// (counter[0]) adds every block's partial, each thread loading its (up to
-// kRowsPerThread) rows at once, so the whole sum costs one round trip to L2.
-// (Issued four at a time, the 28 rows per thread of a 391-block grid took
-// 4.2 us; a two-level scheme took 3.6 us for its two levels.)  Larger grids
+// (counter[0]) adds every block's partial, each thread its (up to
+// kRowsPerThread) rows, loaded sixteen at a time.  Partials and sums are
+// float-float pairs (see ff_add): with doubles, the last block's 7,000
+// additions for a 391-block grid took 3.6-4.1 us of FP64 pipe, the longest
+// step of a pass's tail; as float-float they cost a fraction of that (scene
+// registration 2.28 -> 2.21 ms, residual iteration 23 -> 16.5 us).  Larger grids
 // reduce in two fixed-order levels: the last block to finish of each group of
 // kGroupBlocks consecutive blocks (counter[2 + group]) adds the group's
 // partials in block order, one load per thread, and stores the sum over the
@@ -853,6 +855,23 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // order either way.  *t_start (if given) is the global time at which the pass
 // received its command; the last block stores it and the publish time in the
 // two words after the abort word.
+// Float-float sums (an unevaluated pair hi + lo of float32 values, about 44
+// significant bits): GB300's double-precision rate is a small fraction of its
+// float32 rate, and the final sum over every block's partial was the longest
+// step of a pass's tail.  TwoSum of the high parts, then the low parts added
+// in and the pair renormalised.
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  const float e = __fadd_rn(err, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s, e);
+  return FF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
 template <bool kPublish, bool kPersistent = false>
 __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
                                                double* __restrict__ partials,
@@ -861,8 +880,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
                                                unsigned int skipped = 0u,
                                                const unsigned long long* t_start = nullptr,
                                                unsigned long long* thr_word = nullptr) {
-  __shared__ double s_warp[kThreads / 32][kMomentSlots];
-  __shared__ double s_fin[kThreads / kMomentSlots][kMomentSlots];
+  __shared__ FF s_warp[kThreads / 32][kMomentSlots];
+  __shared__ FF s_fin[kThreads / kMomentSlots][kMomentSlots];
+  __shared__ double s_out[kMomentSlots];
+  float2* const pf = reinterpret_cast<float2*>(partials);
   __shared__ bool s_last;
 #pragma unroll
   for (int v = 0; v < 16; ++v) {
@@ -873,26 +894,26 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   c1 = __reduce_add_sync(kFull, c1);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
-    s_warp[warp][0] = static_cast<double>(c0);
-    s_warp[warp][1] = static_cast<double>(c1);
+    s_warp[warp][0] = FF{static_cast<float>(c0), 0.f};
+    s_warp[warp][1] = FF{static_cast<float>(c1), 0.f};
 #pragma unroll
-    for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = static_cast<double>(acc[v]);
+    for (int v = 0; v < 16; ++v) s_warp[warp][2 + v] = FF{acc[v], 0.f};
   }
   __syncthreads();
   // every thread of the block is past its search: a kernel launched as a
   // programmatic dependent of this one may start once all blocks are here
   if (!kPersistent) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x < kMomentSlots) {
-    double s = 0.0;
+    FF s{0.f, 0.f};
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s += s_warp[w][threadIdx.x];
+    for (int w = 0; w < kThreads / 32; ++w) s = ff_add(s, s_warp[w][threadIdx.x]);
     s_fin[0][threadIdx.x] = s;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v)
-      partials[static_cast<int64_t>(blockIdx.x) * kMomentSlots + v] = s_fin[0][v];
+      pf[static_cast<int64_t>(blockIdx.x) * kMomentSlots + v] = make_float2(s_fin[0][v].hi, s_fin[0][v].lo);
     if (skipped != 0u) atomicAdd(counter + 1, skipped);
   }
   const int r = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
@@ -908,19 +929,22 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     if (!s_last) return;
     if (threadIdx.x == 0) fence_acq_rel_gpu();
     __syncthreads();
-    if (threadIdx.x < kGroupBlocks * kMomentSlots)
-      s_fin[r][v] = static_cast<unsigned int>(r) < in_group
-                        ? __ldcg(&partials[static_cast<int64_t>(g0 + r) * kMomentSlots + v]) : 0.0;
+    if (threadIdx.x < kGroupBlocks * kMomentSlots) {
+      const float2 x = static_cast<unsigned int>(r) < in_group
+                           ? __ldcg(&pf[static_cast<int64_t>(g0 + r) * kMomentSlots + v]) : make_float2(0.f, 0.f);
+      s_fin[r][v] = FF{x.x, x.y};
+    }
     __syncthreads();
     if (threadIdx.x < kMomentSlots) {
-      double s = 0.0;
-      for (unsigned int k = 0; k < in_group; ++k) s += s_fin[k][threadIdx.x];
+      FF s{0.f, 0.f};
+      for (unsigned int k = 0; k < in_group; ++k) s = ff_add(s, s_fin[k][threadIdx.x]);
       s_warp[0][threadIdx.x] = s;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
 #pragma unroll
-      for (int u = 0; u < kMomentSlots; ++u) partials[static_cast<int64_t>(g0) * kMomentSlots + u] = s_warp[0][u];
+      for (int u = 0; u < kMomentSlots; ++u)
+        pf[static_cast<int64_t>(g0) * kMomentSlots + u] = make_float2(s_warp[0][u].hi, s_warp[0][u].lo);
       counter[2 + group] = 0u;  // ordered before the next level's release increment
     }
     rows = (gridDim.x + kGroupBlocks - 1) / kGroupBlocks;
@@ -945,26 +969,27 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   constexpr int kGroups = kThreads / kMomentSlots;
   if (threadIdx.x < kGroups * kMomentSlots) {
     // rows r, r + 14, ... added in order; all of a batch's loads in flight at once
-    double s = 0.0;
-    for (unsigned int j = r; j < rows; j += kRowsPerThread * kGroups) {
-      double x[kRowsPerThread];
+    FF s{0.f, 0.f};
+    constexpr int kBatch = 16;
+    for (unsigned int j = r; j < rows; j += kBatch * kGroups) {
+      float2 x[kBatch];
 #pragma unroll
-      for (int u = 0; u < kRowsPerThread; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const unsigned int row = j + u * kGroups;
-        x[u] = row < rows ? __ldcg(&partials[static_cast<int64_t>(row) * row_stride * kMomentSlots + v]) : 0.0;
+        x[u] = row < rows ? __ldcg(&pf[static_cast<int64_t>(row) * row_stride * kMomentSlots + v]) : make_float2(0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < kRowsPerThread; ++u)
-        if (j + u * kGroups < rows) s += x[u];
+      for (int u = 0; u < kBatch; ++u)
+        if (j + u * kGroups < rows) s = ff_add(s, FF{x[u].x, x[u].y});
     }
     s_fin[r][v] = s;
   }
   __syncthreads();
   if (threadIdx.x < kMomentSlots) {
-    double s = 0.0;
+    FF s{0.f, 0.f};
 #pragma unroll
-    for (int g = 0; g < kGroups; ++g) s += s_fin[g][threadIdx.x];
-    s_fin[0][threadIdx.x] = s;  // row 0 was read above by this thread only
+    for (int g = 0; g < kGroups; ++g) s = ff_add(s, s_fin[g][threadIdx.x]);
+    s_out[threadIdx.x] = static_cast<double>(s.hi) + static_cast<double>(s.lo);
   }
   __syncthreads();
   // One thread stores the result and, after one system-scope fence that
@@ -982,8 +1007,8 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
       return;
     }
     if (thr_out != nullptr || thr_word != nullptr) {
-      const double pairs = s_fin[0][1];
-      const double sigma2 = pairs > 0.0 ? s_fin[0][17] / pairs : 0.0;
+      const double pairs = s_out[1];
+      const double sigma2 = pairs > 0.0 ? s_out[17] / pairs : 0.0;
       const float thr = float_threshold_dev(9.0 * sigma2);
       if (thr_out != nullptr) *thr_out = thr;
       // release: the counters reset above are in place before any block that
@@ -996,7 +1021,7 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
                      : "memory");
     }
 #pragma unroll
-    for (int v = 0; v < kMomentSlots; ++v) out[v] = s_fin[0][v];
+    for (int v = 0; v < kMomentSlots; ++v) out[v] = s_out[v];
     if (kPublish) {
       if (t_start != nullptr) {
         unsigned long long* tw = reinterpret_cast<unsigned long long*>(out + kMomentSlots + 2);
@@ -1013,12 +1038,13 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
 //
 // Precision of the sums.  Each thread adds its pairs' moments in float32, a
 // warp adds its 32 lanes in a five-level float32 butterfly, and everything
-// above (warps, blocks, groups) is added in double.  A thread sums at most
+// above (warps, blocks, groups) is added as float-float pairs (about 44
+// significant bits, converted to double at the end).  A thread sums at most
 // k = ceil(n / resident threads) pairs (1 on the 100k scene, 18 on the 2M
 // source), so a float32 partial carries an error of at most
 // gamma_(k+4) * sum |terms| with gamma_m = m u / (1 - m u), u = 2^-24: for
-// k = 18 about 1.3e-6 of the absolute sum, which the double levels then
-// preserve.  The centroids and H are compared with 1e-5 bounds, which this
+// k = 18 about 1.3e-6 of the absolute sum, which the float-float levels then
+// preserve (each of their additions errs by about 2^-44 of its operands).  The centroids and H are compared with 1e-5 bounds, which this
 // meets with room for the cancellation between the shifted second moments
 // and the product of the means.  The distance sum (acc[15], whose mean is
 // compared at 1e-6) is kept compensated per thread instead: the rounding
