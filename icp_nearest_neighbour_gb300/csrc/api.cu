@@ -144,12 +144,14 @@ thread_local MappedBuffer tl_mapped;
 //   [kSecondSlot, kSecondSlot + kMomentSlots + 1]  the other residual pass's result and words
 //   [kCommandOffset, + sizeof(PassCommand))    the host-written command of pre-launched passes
 //   [kTaggedOffset, + sizeof(TaggedCommand))   the host-written commands of the persistent kernel
+//   [kBboxOffset, + 3)                         the source's box, copied from the device (Source)
 // A result slot holds the 18 moments, the publish word, the abort word and
 // (persistent kernel) the pass's start and end global times.
 constexpr int kSecondSlot = 32;
 constexpr int kCommandOffset = 64;
 constexpr int kTaggedOffset = 80;
-constexpr int kMappedDoubles = 96;
+constexpr int kBboxOffset = 96;  // the source's box, six ordered integers, copied from the device
+constexpr int kMappedDoubles = 112;
 static_assert(kSecondSlot >= kMomentSlots + 4, "result slot: moments + 4 words");
 static_assert(kTaggedOffset * sizeof(double) >= kCommandOffset * sizeof(double) + sizeof(PassCommand) &&
                   kTaggedOffset * sizeof(double) + sizeof(TaggedCommand) <= kMappedDoubles * sizeof(double) &&
@@ -157,6 +159,9 @@ static_assert(kTaggedOffset * sizeof(double) >= kCommandOffset * sizeof(double) 
               "tagged command block must fit the mapped buffer after the pass command");
 static_assert(kSecondSlot > kMomentSlots + 1 && kCommandOffset > kSecondSlot + kMomentSlots + 1,
               "mapped-buffer regions must not overlap");
+static_assert(kTaggedOffset * sizeof(double) + sizeof(TaggedCommand) <= kBboxOffset * sizeof(double) &&
+                  kBboxOffset + 3 <= kMappedDoubles,
+              "the source box's copy must fit after the tagged command");
 static_assert(kCommandOffset * sizeof(double) + sizeof(PassCommand) <= kMappedDoubles * sizeof(double),
               "command block must fit the mapped buffer");
 
@@ -208,10 +213,28 @@ float rejection_threshold(double dmax) {
 }
 
 // The source in Morton order as float4 records, plus the float32 centre of
-// its bounding box (the shift c_s of the moment sums).
+// its bounding box (the shift c_s of the moment sums).  The box is computed on
+// the device; the kernels take the centre from it there (bbox6), and the host
+// reads its copy in mapped memory only when it first decodes a pass's result
+// (shift()), by which time the copy, queued before every pass, has landed.
 struct Source {
   float4* recs = nullptr;
-  float shift[3] = {0, 0, 0};
+  const int32_t* bbox6 = nullptr;                     // device, null without a shift
+  const volatile int32_t* bbox6_host = nullptr;       // mapped copy of bbox6
+  mutable float shift_[3] = {0, 0, 0};
+  mutable bool shift_ready = true;
+  const float* shift() const {
+    if (!shift_ready) {
+      std::atomic_thread_fence(std::memory_order_acquire);
+      int32_t h6[6];
+      for (int k = 0; k < 6; ++k) h6[k] = bbox6_host[k];
+      float lo[3], hi[3];
+      decode_bbox(h6, lo, hi);
+      for (int d = 0; d < 3; ++d) shift_[d] = 0.5f * (lo[d] + hi[d]);
+      shift_ready = true;
+    }
+    return shift_;
+  }
 };
 
 int prepare_source(const float* xyz, int64_t n, bool morton, bool want_shift, cudaStream_t s,
@@ -249,12 +272,11 @@ int prepare_source(const float* xyz, int64_t n, bool morton, bool want_shift, cu
   if (want_shift) {
     MappedBuffer* mb = nullptr;
     if (int rc = mapped_buffer(&mb)) return rc;
-    int32_t* h6 = reinterpret_cast<int32_t*>(mb->host);
+    int32_t* h6 = reinterpret_cast<int32_t*>(mb->host + kBboxOffset);
     ICPNN_CUDA(cudaMemcpyAsync(h6, bbox6, 6 * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
-    ICPNN_CUDA(cudaStreamSynchronize(s));
-    float lo[3], hi[3];
-    decode_bbox(h6, lo, hi);
-    for (int d = 0; d < 3; ++d) out->shift[d] = 0.5f * (lo[d] + hi[d]);
+    out->bbox6 = bbox6;
+    out->bbox6_host = h6;
+    out->shift_ready = false;
   }
   return ICPNN_OK;
 }
@@ -400,12 +422,12 @@ void read_moments(const Pass& ps, icpnn_moments* m) {
   std::atomic_thread_fence(std::memory_order_acquire);
   double raw[kMomentSlots];
   std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
-  decode_moments(raw, ps.src.shift, ps.shift_q, m);
+  decode_moments(raw, ps.src.shift(), ps.shift_q, m);
 }
 
 IcpPassParams pass_params(const Pass& ps) {
   IcpPassParams p{};
-  std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
+  p.src_bbox6 = ps.src.bbox6;
   std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
   p.max_d2 = ps.max_d2;
   p.seq = ++ps.mb->seq;
@@ -570,7 +592,7 @@ int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream
   IcpPassParams p{};
   std::memcpy(p.R, R, sizeof(p.R));
   std::memcpy(p.t, tr, sizeof(p.t));
-  std::memcpy(p.shift_s, ps.src.shift, sizeof(p.shift_s));
+  p.src_bbox6 = ps.src.bbox6;
   std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
   p.max_d2 = INFINITY;
   const unsigned long long seq_a = ++ps.mb->seq;
@@ -593,7 +615,7 @@ int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream
   const double pairs = raw[1];
   *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
   std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
-  decode_moments(raw, ps.src.shift, ps.shift_q, kept);
+  decode_moments(raw, ps.src.shift(), ps.shift_q, kept);
   kept->n_nonfinite = 0;
   kept->sum_d2 = 0.0;
   kept->mse = NAN;
@@ -1087,7 +1109,7 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
       const double pairs = raw[1];
       *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
       std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
-      decode_moments(raw, ps.src.shift, ps.shift_q, kept);
+      decode_moments(raw, ps.src.shift(), ps.shift_q, kept);
       kept->n_nonfinite = 0;
       kept->sum_d2 = 0.0;
       kept->mse = NAN;

@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(kThreads) bbox_kernel(const float* __restrict_
       hi[d] = max(hi[d], o[d]);
     }
   }
+  // warp, then block, then one atomic per block and bound (per-warp atomics
+  // on the six words serialised: 14 us for 100k points)
+  __shared__ int32_t s_box[kThreads / 32][6];
 #pragma unroll
   for (int d = 0; d < 3; ++d) {
     lo[d] = __reduce_min_sync(kFull, lo[d]);
@@ -104,9 +107,17 @@ __global__ void __launch_bounds__(kThreads) bbox_kernel(const float* __restrict_
   if ((threadIdx.x & 31) == 0) {
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-      if (lo[d] != INT_MAX) atomicMin(&bbox6[d], lo[d]);
-      if (hi[d] != INT_MIN) atomicMax(&bbox6[3 + d], hi[d]);
+      s_box[threadIdx.x >> 5][d] = lo[d];
+      s_box[threadIdx.x >> 5][3 + d] = hi[d];
     }
+  }
+  __syncthreads();
+  if (threadIdx.x < 6) {
+    const int d = threadIdx.x;
+    int32_t v = s_box[0][d];
+    for (int w = 1; w < kThreads / 32; ++w) v = d < 3 ? min(v, s_box[w][d]) : max(v, s_box[w][d]);
+    if (d < 3 && v != INT_MAX) atomicMin(&bbox6[d], v);
+    if (d >= 3 && v != INT_MIN) atomicMax(&bbox6[d], v);
   }
 }
 
@@ -123,6 +134,15 @@ __device__ __forceinline__ uint32_t spread10(uint32_t v) {
 
 __device__ __forceinline__ float decode_ordered(int32_t o) {
   return __int_as_float(ordered_from_bits(o));
+}
+
+// shift_s from the device-computed source box (see IcpPassParams).
+__device__ __forceinline__ void resolve_shift(IcpPassParams& p) {
+  if (p.src_bbox6 == nullptr) return;
+#pragma unroll
+  for (int d = 0; d < 3; ++d)
+    p.shift_s[d] = __fmul_rn(0.5f, __fadd_rn(decode_ordered(__ldg(&p.src_bbox6[d])),
+                                             decode_ordered(__ldg(&p.src_bbox6[3 + d]))));
 }
 
 __global__ void __launch_bounds__(kThreads) morton_kernel(const float* __restrict__ xyz, int64_t n,
@@ -1256,6 +1276,7 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_kernel(
   extern __shared__ __align__(16) uint2 s_nodes[];
   __shared__ float s_rt[12];
   __shared__ unsigned int s_skip;
+  resolve_shift(p);
   if (p.cmd == nullptr) {
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -1324,6 +1345,7 @@ __global__ void __launch_bounds__(kThreads) residual_pass_kernel(
     const float4* __restrict__ pts, const float4* __restrict__ src, const int32_t* __restrict__ slot_of,
     int64_t n, IcpPassParams p, double* __restrict__ partials, unsigned int* __restrict__ counter,
     double* out, const float* thr_in, float* thr_out) {
+  resolve_shift(p);
   if (thr_in != nullptr) p.max_d2 = *thr_in;  // written by the previous pass on this stream
   float rt[12];
 #pragma unroll
@@ -1478,6 +1500,7 @@ __global__ void __launch_bounds__(kThreads, 3) icp_registration_kernel(
   __shared__ float s_rt[12];
   __shared__ float s_thr;
   __shared__ unsigned int s_skip;
+  resolve_shift(p);
   stage_top(nodes, s_nodes, smem_slots);  // once for the whole registration
   const TreeView tv{nodes, boxes, pts, s_nodes, static_cast<uint32_t>(smem_slots)};
   for (unsigned long long seq = p.seq;;) {

@@ -80,7 +80,7 @@ struct alignas(16) TaggedMirror {
 struct IcpPassParams {
   float R[9];
   float t[3];
-  float shift_s[3];   // c_s
+  float shift_s[3];   // c_s (replaced on the device when src_bbox6 is set)
   float shift_q[3];   // c_q
   float max_d2;       // accept iff d2 <= max_d2 (float threshold equivalent to the double test)
   unsigned long long seq;  // published after the result, see launch_icp_pass
@@ -93,6 +93,12 @@ struct IcpPassParams {
   const PassCommand* cmd;
   CommandMirror* mirror;
   unsigned long long wait_ns;
+  // If set: the source's bounding box as ordered integers (lo xyz, hi xyz),
+  // computed on the device; every kernel then takes shift_s as its centre,
+  // 0.5f * (lo + hi) per axis in float32 -- the same value the host decodes
+  // the moments with -- so the host need not wait for the box before it
+  // launches the passes.
+  const int32_t* src_bbox6;
 };
 
 constexpr unsigned long long kCommandWaitNs = 50ull * 1000 * 1000;
