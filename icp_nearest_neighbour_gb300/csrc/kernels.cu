@@ -837,20 +837,22 @@ __device__ __forceinline__ float float_threshold_dev(double limit) {
 //
 // Grids of up to kSingleLevelBlocks blocks (every grid of the search kernels:
 // at most three blocks per SM) reduce in one level: the last block to finish
-// (counter[0]) adds every block's partial, each thread its (up to
-// kRowsPerThread) rows, loaded sixteen at a time.  Partials and sums are
+// (counter[0]) adds every block's partial: 252 threads, each taking two
+// slots of every 28th row, one 16-byte load per row and up to 14 loads in
+// flight (one round trip for a 391-block grid).  Partials and sums are
 // float-float pairs (see ff_add): with doubles, the last block's 7,000
 // additions for a 391-block grid took 3.6-4.1 us of FP64 pipe, the longest
 // step of a pass's tail; as float-float they cost a fraction of that (scene
-// registration 2.28 -> 2.21 ms, residual iteration 23 -> 16.5 us).  Larger grids
+// registration 2.28 -> 2.21 ms, residual iteration 23 -> 16.5 us; the 16-byte
+// loads then 2.19 -> 2.16 ms and 16.6 -> 15.0 us).  Larger grids
 // reduce in two fixed-order levels: the last block to finish of each group of
 // kGroupBlocks consecutive blocks (counter[2 + group]) adds the group's
 // partials in block order, one load per thread, and stores the sum over the
 // group's first partial; the last group to finish (counter[0]) adds the group
 // sums.
 constexpr unsigned int kSkipStopped = 1u, kSkipTimedOut = 1u << 16;
-constexpr int kRowsPerThread = 33;
-constexpr unsigned int kSingleLevelBlocks = kRowsPerThread * (kThreads / kMomentSlots);
+// at least every grid of the search kernels (three blocks per SM on 152 SMs)
+constexpr unsigned int kSingleLevelBlocks = 462;
 static_assert(kGroupBlocks * kMomentSlots <= kThreads, "one thread per partial of a group");
 
 // Release-only increment: orders this thread's earlier stores before the
@@ -986,29 +988,40 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     counter[0] = 0u;
   }
   __syncthreads();
-  constexpr int kGroups = kThreads / kMomentSlots;
-  if (threadIdx.x < kGroups * kMomentSlots) {
-    // rows r, r + 14, ... added in order; all of a batch's loads in flight at once
-    FF s{0.f, 0.f};
-    constexpr int kBatch = 16;
-    for (unsigned int j = r; j < rows; j += kBatch * kGroups) {
-      float2 x[kBatch];
+  // rows r, r + 28, ... added in order, two slots per 16-byte load; all of a
+  // thread's (up to 14) loads in flight at once
+  constexpr int kPairs = kMomentSlots / 2;
+  constexpr int kRowGroups = kThreads / kPairs;
+  constexpr int kBatch = 14;
+  __shared__ FF s_rows[kRowGroups][kMomentSlots];
+  if (threadIdx.x < kRowGroups * kPairs) {
+    const int g = threadIdx.x / kPairs, vp = threadIdx.x % kPairs;
+    const float4* pf4 = reinterpret_cast<const float4*>(partials);
+    FF s0{0.f, 0.f}, s1{0.f, 0.f};
+    for (unsigned int j = g; j < rows; j += kBatch * kRowGroups) {
+      float4 x[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const unsigned int row = j + u * kGroups;
-        x[u] = row < rows ? __ldcg(&pf[static_cast<int64_t>(row) * row_stride * kMomentSlots + v]) : make_float2(0.f, 0.f);
+        const unsigned int row = j + u * kRowGroups;
+        x[u] = row < rows ? __ldcg(&pf4[static_cast<int64_t>(row) * row_stride * kPairs + vp])
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (j + u * kGroups < rows) s = ff_add(s, FF{x[u].x, x[u].y});
+      for (int u = 0; u < kBatch; ++u) {
+        if (j + u * kRowGroups < rows) {
+          s0 = ff_add(s0, FF{x[u].x, x[u].y});
+          s1 = ff_add(s1, FF{x[u].z, x[u].w});
+        }
+      }
     }
-    s_fin[r][v] = s;
+    s_rows[g][2 * vp] = s0;
+    s_rows[g][2 * vp + 1] = s1;
   }
   __syncthreads();
   if (threadIdx.x < kMomentSlots) {
     FF s{0.f, 0.f};
 #pragma unroll
-    for (int g = 0; g < kGroups; ++g) s = ff_add(s, s_fin[g][threadIdx.x]);
+    for (int g = 0; g < kRowGroups; ++g) s = ff_add(s, s_rows[g][threadIdx.x]);
     s_out[threadIdx.x] = static_cast<double>(s.hi) + static_cast<double>(s.lo);
   }
   __syncthreads();
