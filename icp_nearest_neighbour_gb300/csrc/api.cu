@@ -184,6 +184,8 @@ int mapped_buffer(MappedBuffer** out) {
   return ICPNN_OK;
 }
 
+int wait_tree_ready(const icpnn_tree* t, cudaStream_t s);
+
 int check_tree_on_device(const icpnn_tree* t) {
   if (t == nullptr) return fail(ICPNN_ERR_INVALID_ARG, "tree is NULL");
   if (t->dev.nodes == nullptr) return fail(ICPNN_ERR_NOT_UPLOADED, "tree has not been uploaded");
@@ -358,6 +360,7 @@ struct Pass {
 
 int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bool want_slots,
                bool warm_start, cudaStream_t s, Scratch& sc, Pass* ps) {
+  if (int rc = wait_tree_ready(t, s)) return rc;
   ps->tree = t;
   ps->n = n;
   if (want_slots) {
@@ -637,13 +640,20 @@ void release_device_tree(DeviceTree* d) {
   int cur = -1;
   cudaGetDevice(&cur);
   cudaSetDevice(d->device);
-  cudaDeviceSynchronize();
+  cudaDeviceSynchronize();  // also ends an upload still copying from the host arrays
   cudaFreeAsync(d->nodes, nullptr);
   if (d->points) cudaFreeAsync(d->points, nullptr);
   cudaStreamSynchronize(nullptr);
+  if (d->ready) cudaEventDestroy(d->ready);
   cudaGetLastError();
   cudaSetDevice(cur);
   *d = DeviceTree{};
+}
+
+// Orders stream s after the tree's upload (see DeviceTree::ready).
+int wait_tree_ready(const icpnn_tree* t, cudaStream_t s) {
+  if (t->dev.ready != nullptr) ICPNN_CUDA(cudaStreamWaitEvent(s, t->dev.ready, 0));
+  return ICPNN_OK;
 }
 
 // Host copies of a device-built tree's nodes, boxes and records, made on first
@@ -771,8 +781,14 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   if (e == cudaSuccess) e = cudaMemcpyAsync(nodes, t->nodes.data(), nb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(boxes, t->boxes.data(), bb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pts, t->records.data(), pb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  // The host arrays are page-locked: the copies are DMAs that run on while
+  // the caller goes on; calls that use the tree wait for this event on their
+  // own stream, and freeing the tree synchronises the device first.
+  cudaEvent_t ready = nullptr;
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventRecord(ready, s);
   if (e != cudaSuccess) {
+    if (ready) cudaEventDestroy(ready);
     cudaGetLastError();
     if (nodes) cudaFreeAsync(nodes, s);
     if (pts) cudaFreeAsync(pts, s);
@@ -785,6 +801,7 @@ int icpnn_kdtree_upload(icpnn_tree* t, void* stream) {
   t->dev.nodes = nodes;
   t->dev.boxes = boxes;
   t->dev.points = pts;
+  t->dev.ready = ready;
   return ICPNN_OK;
 }
 
@@ -861,6 +878,7 @@ int icpnn_nn_query(const icpnn_tree* t, const float* xyz, int64_t n, int32_t* id
   if (n == 0) return ICPNN_OK;
   if (!xyz || !idx || !dist2) return fail(ICPNN_ERR_INVALID_ARG, "nn_query: NULL pointer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = wait_tree_ready(t, s)) return rc;
   PointOutputs po;
   {
     Scratch sc(s);
@@ -922,6 +940,7 @@ int icpnn_icp_step_noalloc(const icpnn_tree* t, const float* src, int64_t n, con
   if (idx != nullptr && (!is_current_device_pointer(idx) || !is_current_device_pointer(dist2)))
     return fail(ICPNN_ERR_INVALID_ARG, "icp_step_noalloc: idx and dist2 must be memory of the current device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = wait_tree_ready(t, s)) return rc;
   double* scratch = nullptr;
   ICPNN_CUDA(noalloc_scratch(&scratch));
   // the reduction's counters must start at zero; the other words are

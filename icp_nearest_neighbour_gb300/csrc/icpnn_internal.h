@@ -55,6 +55,9 @@ struct DeviceTree {
   Node* nodes = nullptr;      // heap_slots entries; the boxes follow in the same allocation
   float* boxes = nullptr;     // heap_slots x 8 floats
   float* points = nullptr;    // n float4 records (x, y, z, index bits)
+  // Recorded after the upload's copies, which the upload does not wait for:
+  // every call that uses the tree makes its stream wait on it first.
+  cudaEvent_t ready = nullptr;
 };
 
 }  // namespace icpnn
@@ -84,6 +87,33 @@ struct UninitAllocator : std::allocator<T> {
 template <class T>
 using UninitVector = std::vector<T, UninitAllocator<T>>;
 
+// Page-locked host memory when a CUDA device is present (ordinary memory
+// otherwise), from a process-wide cache of freed blocks (host_pinned.cpp):
+// the tree's host arrays, so that the upload is a plain DMA rather than a
+// copy staged through the driver's pinned buffers.
+void* pinned_alloc(size_t bytes);
+void pinned_free(void* p) noexcept;
+
+template <class T>
+struct PinnedAllocator : UninitAllocator<T> {
+  using value_type = T;
+  template <class U>
+  struct rebind {
+    using other = PinnedAllocator<U>;
+  };
+  PinnedAllocator() = default;
+  template <class U>
+  PinnedAllocator(const PinnedAllocator<U>&) noexcept {}
+  T* allocate(size_t n) { return static_cast<T*>(pinned_alloc(n * sizeof(T))); }
+  void deallocate(T* p, size_t) noexcept { pinned_free(p); }
+  template <class U>
+  bool operator==(const PinnedAllocator<U>&) const noexcept { return true; }
+  template <class U>
+  bool operator!=(const PinnedAllocator<U>&) const noexcept { return false; }
+};
+template <class T>
+using PinnedVector = std::vector<T, PinnedAllocator<T>>;
+
 }  // namespace icpnn
 
 struct icpnn_tree {
@@ -96,11 +126,11 @@ struct icpnn_tree {
   int64_t heap_slots = 0;     // 2^(depth+1)
   float bbox_lo[3] = {0, 0, 0};
   float bbox_hi[3] = {0, 0, 0};
-  icpnn::UninitVector<icpnn::Node> nodes;   // heap layout, heap_slots entries
-  icpnn::UninitVector<float> records;       // 4 floats per point, leaf order
+  icpnn::PinnedVector<icpnn::Node> nodes;   // heap layout, heap_slots entries
+  icpnn::PinnedVector<float> records;       // 4 floats per point, leaf order
   // Tight bounding box of each node's points, 8 floats per heap slot:
   // lo.x, lo.y, lo.z, 0, hi.x, hi.y, hi.z, 0 (unused slots zero).
-  icpnn::UninitVector<float> boxes;
+  icpnn::PinnedVector<float> boxes;
   icpnn::DeviceTree dev;
   // Built on the device: nodes, boxes and records exist there only until a
   // caller needs them on the host (export, upload to another device).

@@ -124,14 +124,18 @@ int icpnn_kdtree_build_device(const float* xyz, int64_t n, int32_t leaf_size, in
                               uint32_t flags, icpnn_tree** out, void* stream);
 
 /* icpnn_kdtree_upload -- copy the tree (node array and leaf-ordered point
- * records) to the current device, enqueued on `stream`, which is then
- * synchronised.  Done once per target (page sections 2.3, 5.5).  A second call
- * on the same device is a no-op; a call on another device moves the copy.
- * Errors: INVALID_ARG, CUDA, NO_MEMORY. */
+ * records) to the current device, enqueued on `stream`; the call returns
+ * without waiting for the copies (the host arrays are page-locked when a
+ * device is present).  Every later call that uses the tree orders its own
+ * stream after them, so the tree may be used on any stream at once.  Done
+ * once per target (page sections 2.3, 5.5).  A second call on the same device
+ * is a no-op; a call on another device moves the copy.  Errors: INVALID_ARG,
+ * CUDA, NO_MEMORY (a failed copy surfaces at the next call that waits). */
 int icpnn_kdtree_upload(icpnn_tree* tree, void* stream);
 
-/* icpnn_kdtree_free -- release the host and device copies.  NULL is a no-op.
- * The caller must make sure no enqueued work still reads the tree. */
+/* icpnn_kdtree_free -- release the host and device copies (it synchronises
+ * the tree's device first, so an upload still copying is finished).  NULL is
+ * a no-op.  The caller must make sure no enqueued work still reads the tree. */
 void icpnn_kdtree_free(icpnn_tree* tree);
 
 /* icpnn_kdtree_info -- shape of a built tree.  Any output may be NULL.

@@ -10,7 +10,7 @@ Tolerances:
   * per-point indices and squared distances: bit-identical;
   * accepted-pair counts: identical (the accept test is an exact float
     comparison on bit-identical distances);
-  * mse: 1e-6 relative (float32 partial sums per warp, double above);
+  * mse: 1e-6 relative (float32 partial sums per warp, float-float pairs above);
   * centroids: 1e-5 of max(|mu|, scene extent); H: 1e-5 relative in the
     Frobenius norm;
   * transforms: 1e-4 rad rotation and 1e-5 * scene extent translation.
@@ -294,6 +294,33 @@ def test_align_is_deterministic(nn):
     b = nn.icp_align(t, dev(c.source), 10, 0.0, 1.0, trace=True)
     np.testing.assert_array_equal(a["T"], b["T"])
     assert [r["mse"] for r in a["trace"]] == [r["mse"] for r in b["trace"]]
+
+
+def test_upload_on_one_stream_registration_on_another(nn):
+    """The upload does not wait for its copies: a registration (and a query)
+    issued at once on another stream must still see the whole tree."""
+    import torch
+    c = W.scene_case()
+    ref_t = nn.kdtree_build(c.target, c.leaf_size)
+    nn.kdtree_upload(ref_t)
+    ref = nn.icp_align(ref_t, dev(c.source), 10, 0.0, 1.0)
+    q = dev(c.source)
+    ref_idx = torch.empty(len(c.source), dtype=torch.int32, device="cuda")
+    ref_d2 = torch.empty(len(c.source), dtype=torch.float32, device="cuda")
+    nn.nn_query(ref_t, q, ref_idx, ref_d2)
+    torch.cuda.synchronize()
+    up, use = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        t = nn.kdtree_build(c.target, c.leaf_size)
+        nn.kdtree_upload(t, stream=up)
+        idx = torch.empty_like(ref_idx)
+        d2 = torch.empty_like(ref_d2)
+        nn.nn_query(t, q, idx, d2, stream=use)
+        r = nn.icp_align(t, dev(c.source), 10, 0.0, 1.0, stream=use)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(r["T"], ref["T"])
+        assert torch.equal(idx, ref_idx) and torch.equal(d2, ref_d2)
+        t.free()
 
 
 @pytest.mark.parametrize("name", ["tiny", "scene", "lidar"])
