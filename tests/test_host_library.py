@@ -144,6 +144,22 @@ def test_concurrent_builds_give_the_same_tree(lib):
     assert not errors, errors[0]
 
 
+def test_builds_of_changing_sizes_reuse_host_blocks_safely(lib):
+    """The tree's host arrays come from a cache of freed blocks, handed out
+    again to requests they can hold: trees of alternating sizes, built and
+    freed in turn, must come out exactly as the first build of each size."""
+    small = W.uniform_cloud(1500, 11)
+    big = W.scene_case(40_000, 3).target
+    ref = {k: lib.kdtree_export(lib.kdtree_build(c, 8)) for k, c in (("s", small), ("b", big))}
+    for _ in range(4):
+        for k, c in (("b", big), ("s", small), ("s", small), ("b", big)):
+            t = lib.kdtree_build(c, 8)
+            ex = lib.kdtree_export(t)
+            for f in ("split_val", "split_dim", "start", "end", "leaf_index"):
+                np.testing.assert_array_equal(ex[f], ref[k][f], err_msg=f)
+            t.free()
+
+
 def test_tree_depth_cap(lib, oracle_mod):
     pts = W.uniform_cloud(3000, 4)
     t = lib.kdtree_build(pts, 1, max_depth=5)
