@@ -84,9 +84,6 @@ struct UninitAllocator : std::allocator<T> {
     ::new (static_cast<void*>(p)) U(std::forward<A>(a)...);
   }
 };
-template <class T>
-using UninitVector = std::vector<T, UninitAllocator<T>>;
-
 // Page-locked host memory when a CUDA device is present (ordinary memory
 // otherwise), from a process-wide cache of freed blocks (host_pinned.cpp):
 // the tree's host arrays, so that the upload is a plain DMA rather than a
