@@ -140,25 +140,21 @@ struct MappedBuffer {
 };
 thread_local MappedBuffer tl_mapped;
 // Layout, in doubles, each region on cache lines of its own:
-//   [0, kMomentSlots + 1]                      a pass's result, its publish word, its abort word
-//   [kSecondSlot, kSecondSlot + kMomentSlots + 1]  the other residual pass's result and words
+//   [0, kMomentSlots + 3]                      a pass's result, its publish word, its abort word
 //   [kCommandOffset, + sizeof(PassCommand))    the host-written command of pre-launched passes
 //   [kTaggedOffset, + sizeof(TaggedCommand))   the host-written commands of the persistent kernel
 //   [kBboxOffset, + 3)                         the source's box, copied from the device (Source)
 // A result slot holds the 18 moments, the publish word, the abort word and
 // (persistent kernel) the pass's start and end global times.
-constexpr int kSecondSlot = 32;
 constexpr int kCommandOffset = 64;
 constexpr int kTaggedOffset = 80;
 constexpr int kBboxOffset = 96;  // the source's box, six ordered integers, copied from the device
 constexpr int kMappedDoubles = 112;
-static_assert(kSecondSlot >= kMomentSlots + 4, "result slot: moments + 4 words");
+static_assert(kCommandOffset >= kMomentSlots + 4, "result slot: moments + 4 words");
 static_assert(kTaggedOffset * sizeof(double) >= kCommandOffset * sizeof(double) + sizeof(PassCommand) &&
                   kTaggedOffset * sizeof(double) + sizeof(TaggedCommand) <= kMappedDoubles * sizeof(double) &&
                   (kTaggedOffset * sizeof(double)) % 16 == 0,
               "tagged command block must fit the mapped buffer after the pass command");
-static_assert(kSecondSlot > kMomentSlots + 1 && kCommandOffset > kSecondSlot + kMomentSlots + 1,
-              "mapped-buffer regions must not overlap");
 static_assert(kTaggedOffset * sizeof(double) + sizeof(TaggedCommand) <= kBboxOffset * sizeof(double) &&
                   kBboxOffset + 3 <= kMappedDoubles,
               "the source box's copy must fit after the tagged command");
@@ -397,16 +393,17 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
 // one queued behind it, say, when launches are serialised or the host stalls)
 // cannot hide this pass's outcome: an abort word at or beyond `seq` means that
 // pass `seq` has finished, and the publish word then tells whether it
-// published.  (`abort_word`, if given, replaces the word after `flag`: the
-// persistent kernel records every give-up in the first slot's abort word.)
-// Bounded: the stream is queried every few thousand polls, so a failed or
-// finished kernel ends the wait.
+// published.  (`abort_from`, if given, is the first sequence number whose
+// abort also ends the wait: a residual command's two passes publish only the
+// second's result, and either may give up.)  Bounded: the stream is queried
+// every few thousand polls, so a failed or finished kernel ends the wait.
 int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s,
-                   bool* aborted = nullptr, const volatile unsigned long long* abort_word = nullptr) {
-  if (abort_word == nullptr) abort_word = flag + 1;
+                   bool* aborted = nullptr, unsigned long long abort_from = 0) {
+  const volatile unsigned long long* abort_word = flag + 1;
+  if (abort_from == 0) abort_from = seq;
   for (uint64_t spins = 1;; ++spins) {
     if (*flag == seq) return ICPNN_OK;
-    if (aborted != nullptr && *abort_word >= seq) {
+    if (aborted != nullptr && *abort_word >= abort_from) {
       std::atomic_thread_fence(std::memory_order_acquire);
       if (*flag == seq) return ICPNN_OK;
       *aborted = true;
@@ -414,7 +411,7 @@ int wait_published(const volatile unsigned long long* flag, unsigned long long s
     }
     if ((spins & 4095u) == 0) {
       const cudaError_t e = cudaStreamQuery(s);
-      if (*flag == seq || (aborted != nullptr && *abort_word >= seq)) continue;
+      if (*flag == seq || (aborted != nullptr && *abort_word >= abort_from)) continue;
       if (e == cudaSuccess) return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
       if (e != cudaErrorNotReady) return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
     }
@@ -581,14 +578,12 @@ int timing_events(size_t count, cudaEvent_t** out) {
   return ICPNN_OK;
 }
 
-// One residual pass (see launch_residual_pass) under float32 (R, t): returns
-// the number of matched pairs, the sum of their squared residuals, and the
-// moments of the pairs with e2 <= thr.
-// Residual rejection of one iteration (page section 4.4), two passes back to
-// back on the stream: the first sums e2 over all matched pairs and leaves the
-// 3-sigma threshold in device memory, the second keeps the pairs within it
-// and sums their moments; the host waits once.  The first pass publishes at
-// kSecondSlot of the mapped buffer.
+// Residual rejection of one iteration (page section 4.4) under float32 (R, t),
+// two passes back to back on the stream: the first sums e2 over all matched
+// pairs and leaves the 3-sigma threshold in device memory, the second keeps
+// the pairs within it and publishes their moments together with the pair
+// count and the sum of e2 (the first pass's sums, bit for bit); the host
+// waits once.  Returns sigma^2 and the kept pairs' moments.
 
 int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream_t s, double* sigma2,
                  icpnn_moments* kept) {
@@ -598,26 +593,21 @@ int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream
   p.src_bbox6 = ps.src.bbox6;
   std::memcpy(p.shift_q, ps.shift_q, sizeof(p.shift_q));
   p.max_d2 = INFINITY;
-  const unsigned long long seq_a = ++ps.mb->seq;
-  p.seq = seq_a;
+  p.seq = ++ps.mb->seq;
   ICPNN_CUDA(launch_residual_pass(*ps.tree, ps.src.recs, ps.slot_of, ps.n, p, ps.partials, ps.counter,
-                                  ps.mb->dev + kSecondSlot, ps.grid, s, nullptr, ps.thr));
+                                  ps.mb->dev, ps.grid, s, nullptr, ps.thr));
   const unsigned long long seq_b = ++ps.mb->seq;
   p.seq = seq_b;
   ICPNN_CUDA(launch_residual_pass(*ps.tree, ps.src.recs, ps.slot_of, ps.n, p, ps.partials, ps.counter,
                                   ps.mb->dev, ps.grid, s, ps.thr, nullptr));
   const volatile unsigned long long* flag_b =
       reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-  const volatile unsigned long long* flag_a =
-      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kSecondSlot + kMomentSlots);
   if (int rc = wait_published(flag_b, seq_b, s)) return rc;
-  if (int rc = wait_published(flag_a, seq_a, s)) return rc;
   std::atomic_thread_fence(std::memory_order_acquire);
   double raw[kMomentSlots];
-  std::memcpy(raw, const_cast<const double*>(ps.mb->host + kSecondSlot), sizeof(raw));
+  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
   const double pairs = raw[1];
   *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
-  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
   decode_moments(raw, ps.src.shift(), ps.shift_q, kept);
   kept->n_nonfinite = 0;
   kept->sum_d2 = 0.0;
@@ -1023,8 +1013,8 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     p.wait_ns = kCommandWaitNs;
     const TaggedCommand* dev_cmd = reinterpret_cast<const TaggedCommand*>(ps.mb->dev + kTaggedOffset);
     const cudaError_t e = launch_registration(*ps.tree, ps.src.recs, ps.n, p, dev_cmd, ps.tmirror, ps.partials,
-                                              ps.counter, ps.mb->dev, ps.mb->dev + kSecondSlot, ps.thr_word,
-                                              ps.slot_of, ps.leaf_of, ps.grid, s);
+                                              ps.counter, ps.mb->dev, ps.thr_word, ps.slot_of, ps.leaf_of,
+                                              ps.grid, s);
     if (e == cudaSuccess) {
       run.active = true;
       prelaunch = false;
@@ -1106,33 +1096,29 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   };
 
   // The persistent kernel's residual passes of one iteration under (R1, t1):
-  // one command, the first pass's sums (second slot) and the kept pairs'
-  // moments (first slot) read back; the same fallback as persistent_pass.
+  // one command, the second pass's result read back (the kept pairs' moments,
+  // the pair count and the sum of e2); the same fallback as persistent_pass.
   auto persistent_residual = [&](const float R1[9], const float t1[3], double* sigma2,
                                  icpnn_moments* kept, float* resid_ms) -> int {
     const unsigned long long seq_a = ++ps.mb->seq;
     const unsigned long long seq_b = ++ps.mb->seq;
     tagged_command(ps.mb, seq_a, R1, t1, kCmdResidual);
-    const volatile unsigned long long* flag_a =
-        reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kSecondSlot + kMomentSlots);
     // a kernel that gave up -- waiting for this command, or for the threshold
-    // between the two passes -- records it in the first slot's abort word
+    // between the two passes -- records seq_a or seq_b in the abort word
     bool aborted = false;
-    if (int rc = wait_published(flag_a, seq_a, s, &aborted, flag0 + 1)) return rc;
-    if (!aborted)
-      if (int rc = wait_published(flag0, seq_b, s, &aborted)) return rc;
+    if (int rc = wait_published(flag0, seq_b, s, &aborted, seq_a)) return rc;
     if (!aborted) {
       std::atomic_thread_fence(std::memory_order_acquire);
       double raw[kMomentSlots];
-      std::memcpy(raw, const_cast<const double*>(ps.mb->host + kSecondSlot), sizeof(raw));
+      std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
       const double pairs = raw[1];
       *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
-      std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
       decode_moments(raw, ps.src.shift(), ps.shift_q, kept);
       kept->n_nonfinite = 0;
       kept->sum_d2 = 0.0;
       kept->mse = NAN;
-      const unsigned long long t0 = flag_a[2], t1 = flag0[3];
+      // the residual command's arrival and the second pass's publish
+      const unsigned long long t0 = flag0[2], t1 = flag0[3];
       *resid_ms = t1 > t0 ? static_cast<float>(static_cast<double>(t1 - t0) * 1e-6) : 0.f;
       return ICPNN_OK;
     }

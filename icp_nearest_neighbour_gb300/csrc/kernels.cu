@@ -919,7 +919,29 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
   return FF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
 }
 
-template <bool kPublish, bool kPersistent = false>
+// Shared memory of reduce_moments, one instance per block whichever variants
+// of the reduction a kernel uses (a __shared__ array declared inside the
+// template would be allocated once per instantiation).
+constexpr int kRowGroups = kThreads / (kMomentSlots / 2);
+struct ReduceShared {
+  FF warp[kThreads / 32][kMomentSlots];
+  FF fin[kThreads / kMomentSlots][kMomentSlots];
+  FF rows[kRowGroups][kMomentSlots];
+  double out[kMomentSlots];
+  bool last;
+};
+__device__ __forceinline__ ReduceShared& reduce_shared() {
+  __shared__ ReduceShared s;
+  return s;
+}
+
+// kSigmaOnly: only c1 (slot 1) and acc[15] (slot 17) are reduced -- the first
+// residual pass, whose one product is the threshold.  Those two sums take
+// exactly the operations, in the same order, that a full reduction of the same
+// values takes, so the threshold's sigma^2 is the one the host later reads from
+// the second residual pass (which carries the same two sums).  Nothing is
+// stored to `out` but the abort word.
+template <bool kPublish, bool kPersistent = false, bool kSigmaOnly = false>
 __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, uint32_t c1,
                                                double* __restrict__ partials,
                                                unsigned int* __restrict__ counter, double* out,
@@ -927,17 +949,21 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
                                                unsigned int skipped = 0u,
                                                const unsigned long long* t_start = nullptr,
                                                unsigned long long* thr_word = nullptr) {
-  __shared__ FF s_warp[kThreads / 32][kMomentSlots];
-  __shared__ FF s_fin[kThreads / kMomentSlots][kMomentSlots];
-  __shared__ double s_out[kMomentSlots];
+  ReduceShared& sh = reduce_shared();
+  auto& s_warp = sh.warp;
+  auto& s_fin = sh.fin;
+  auto& s_out = sh.out;
+  bool& s_last = sh.last;
   float2* const pf = reinterpret_cast<float2*>(partials);
-  __shared__ bool s_last;
+  // the slots this reduction produces
+  const auto wanted = [](int slot) { return !kSigmaOnly || slot == 1 || slot == 17; };
 #pragma unroll
   for (int v = 0; v < 16; ++v) {
+    if (!wanted(2 + v)) continue;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc[v] = __fadd_rn(acc[v], __shfl_xor_sync(kFull, acc[v], off));
   }
-  c0 = __reduce_add_sync(kFull, c0);
+  if (!kSigmaOnly) c0 = __reduce_add_sync(kFull, c0);
   c1 = __reduce_add_sync(kFull, c1);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
@@ -950,7 +976,7 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // every thread of the block is past its search: a kernel launched as a
   // programmatic dependent of this one may start once all blocks are here
   if (!kPersistent) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x < kMomentSlots) {
+  if (threadIdx.x < kMomentSlots && wanted(threadIdx.x)) {
     FF s{0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) s = ff_add(s, s_warp[w][threadIdx.x]);
@@ -960,7 +986,8 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v)
-      pf[static_cast<int64_t>(blockIdx.x) * kMomentSlots + v] = make_float2(s_fin[0][v].hi, s_fin[0][v].lo);
+      if (wanted(v))
+        pf[static_cast<int64_t>(blockIdx.x) * kMomentSlots + v] = make_float2(s_fin[0][v].hi, s_fin[0][v].lo);
     if (skipped != 0u) atomicAdd(counter + 1, skipped);
   }
   const int r = threadIdx.x / kMomentSlots, v = threadIdx.x % kMomentSlots;
@@ -976,13 +1003,13 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     if (!s_last) return;
     if (threadIdx.x == 0) fence_acq_rel_gpu();
     __syncthreads();
-    if (threadIdx.x < kGroupBlocks * kMomentSlots) {
+    if (threadIdx.x < kGroupBlocks * kMomentSlots && wanted(v)) {
       const float2 x = static_cast<unsigned int>(r) < in_group
                            ? __ldcg(&pf[static_cast<int64_t>(g0 + r) * kMomentSlots + v]) : make_float2(0.f, 0.f);
       s_fin[r][v] = FF{x.x, x.y};
     }
     __syncthreads();
-    if (threadIdx.x < kMomentSlots) {
+    if (threadIdx.x < kMomentSlots && wanted(threadIdx.x)) {
       FF s{0.f, 0.f};
       for (unsigned int k = 0; k < in_group; ++k) s = ff_add(s, s_fin[k][threadIdx.x]);
       s_warp[0][threadIdx.x] = s;
@@ -991,7 +1018,8 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     if (threadIdx.x == 0) {
 #pragma unroll
       for (int u = 0; u < kMomentSlots; ++u)
-        pf[static_cast<int64_t>(g0) * kMomentSlots + u] = make_float2(s_warp[0][u].hi, s_warp[0][u].lo);
+        if (wanted(u))
+          pf[static_cast<int64_t>(g0) * kMomentSlots + u] = make_float2(s_warp[0][u].hi, s_warp[0][u].lo);
       counter[2 + group] = 0u;  // ordered before the next level's release increment
     }
     rows = (gridDim.x + kGroupBlocks - 1) / kGroupBlocks;
@@ -1016,10 +1044,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // rows r, r + 28, ... added in order, two slots per 16-byte load; all of a
   // thread's (up to 14) loads in flight at once
   constexpr int kPairs = kMomentSlots / 2;
-  constexpr int kRowGroups = kThreads / kPairs;
   constexpr int kBatch = 14;
-  __shared__ FF s_rows[kRowGroups][kMomentSlots];
-  if (threadIdx.x < kRowGroups * kPairs) {
+  auto& s_rows = sh.rows;
+  if (threadIdx.x < kRowGroups * kPairs &&
+      (wanted(2 * (threadIdx.x % kPairs)) || wanted(2 * (threadIdx.x % kPairs) + 1))) {
     const int g = threadIdx.x / kPairs, vp = threadIdx.x % kPairs;
     const float4* pf4 = reinterpret_cast<const float4*>(partials);
     FF s0{0.f, 0.f}, s1{0.f, 0.f};
@@ -1043,7 +1071,7 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     s_rows[g][2 * vp + 1] = s1;
   }
   __syncthreads();
-  if (threadIdx.x < kMomentSlots) {
+  if (threadIdx.x < kMomentSlots && wanted(threadIdx.x)) {
     FF s{0.f, 0.f};
 #pragma unroll
     for (int g = 0; g < kRowGroups; ++g) s = ff_add(s, s_rows[g][threadIdx.x]);
@@ -1078,6 +1106,7 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
                      "l"((static_cast<unsigned long long>(static_cast<uint32_t>(seq)) << 32) | __float_as_uint(thr))
                      : "memory");
     }
+    if (kSigmaOnly) return;
 #pragma unroll
     for (int v = 0; v < kMomentSlots; ++v) out[v] = s_out[v];
     if (kPublish) {
@@ -1347,9 +1376,10 @@ __global__ void __launch_bounds__(kThreads, 3) icp_pass_kernel(
 // This thread's share of a residual pass: for each of its source records with
 // a match (slot_of >= 0), the squared residual e2 of the pair under rt, with
 // the search's float arithmetic; every pair is counted in n_pair and its e2
-// summed in acc[15]; pairs with e2 <= max_d2 are counted in n_keep and their
-// moments accumulated.  Shared by the residual kernel and the persistent
-// registration kernel.
+// summed in acc[15]; with kKeep, pairs with e2 <= max_d2 are counted in n_keep
+// and their moments accumulated.  Shared by the residual kernel and the
+// persistent registration kernel.
+template <bool kKeep>
 __device__ __forceinline__ void residual_chunks(const float4* __restrict__ pts, const float4* __restrict__ src,
                                                 const int32_t* __restrict__ slot_of, int64_t n, const float* rt,
                                                 float max_d2, const IcpPassParams& p, float (&acc)[16],
@@ -1366,7 +1396,7 @@ __device__ __forceinline__ void residual_chunks(const float4* __restrict__ pts, 
     const float e2 = dist2(r, q[0], q[1], q[2]);
     ++n_pair;
     const float sum_e2 = __fadd_rn(acc[15], e2);
-    if (e2 <= max_d2) {
+    if (kKeep && e2 <= max_d2) {
       ++n_keep;
       add_pair(acc, s.x, s.y, s.z, r, 0.f, p);
     }
@@ -1377,8 +1407,11 @@ __device__ __forceinline__ void residual_chunks(const float4* __restrict__ pts, 
 // Residual pass of the section 4.4 rejection: for every source record with a
 // match from the last correspondence pass (slot_of >= 0), the squared residual
 // e2 of the pair under the transform in p (same float arithmetic as the search
-// distance).  Counts every pair in c1 and sums its e2 in acc[15]; pairs with
-// e2 <= p.max_d2 are counted in c0 and their moments accumulated in acc[0..14].
+// distance).  Counts every pair in c1 and sums its e2 in acc[15].  kSigmaOnly
+// (the first pass): only those two sums, reduced to the 3-sigma threshold in
+// *thr_out.  Otherwise pairs with e2 <= p.max_d2 (or *thr_in) are counted in c0
+// and their moments accumulated in acc[0..14], and the result is published.
+template <bool kSigmaOnly>
 __global__ void __launch_bounds__(kThreads) residual_pass_kernel(
     const float4* __restrict__ pts, const float4* __restrict__ src, const int32_t* __restrict__ slot_of,
     int64_t n, IcpPassParams p, double* __restrict__ partials, unsigned int* __restrict__ counter,
@@ -1394,8 +1427,8 @@ __global__ void __launch_bounds__(kThreads) residual_pass_kernel(
 #pragma unroll
   for (int v = 0; v < 16; ++v) acc[v] = 0.f;
   uint32_t n_keep = 0, n_pair = 0;
-  residual_chunks(pts, src, slot_of, n, rt, p.max_d2, p, acc, n_keep, n_pair);
-  reduce_moments<true>(acc, n_keep, n_pair, partials, counter, out, p.seq, thr_out);
+  residual_chunks<!kSigmaOnly>(pts, src, slot_of, n, rt, p.max_d2, p, acc, n_keep, n_pair);
+  reduce_moments<true, false, kSigmaOnly>(acc, n_keep, n_pair, partials, counter, out, p.seq, thr_out);
 }
 
 // ------------------------------------------------ persistent registration
@@ -1522,17 +1555,18 @@ __device__ __forceinline__ bool await_threshold(const unsigned long long* word, 
 // kSlot: the registration uses the residual rejection -- correspondence
 // passes record each source record's matched slot, and a residual command
 // runs the two residual passes of the iteration back to back: A (sums e2
-// under the command's transform, publishes in the second result slot with
-// sequence number seq, and stores the 3-sigma threshold as a tagged word in
-// thr_word), then, once every block has read that threshold, B (the kept
-// pairs' moments, published in the first slot with seq + 1).  A residual
-// command thus uses two sequence numbers.
+// under the command's transform and stores the 3-sigma threshold as a tagged
+// word in thr_word; nothing crosses to the host), then, once every block has
+// read that threshold, B (the kept pairs' moments, with the pair count and the
+// sum of e2 that A reduced, published with seq + 1).  A residual command thus
+// uses two sequence numbers; a block that gives up waiting records it in the
+// abort word.
 template <bool kSlot>
 __global__ void __launch_bounds__(kThreads, 3) icp_registration_kernel(
     const uint2* __restrict__ nodes, const float4* __restrict__ boxes, const float4* __restrict__ pts,
     int smem_slots, const float4* __restrict__ src, int64_t n, IcpPassParams p, const TaggedCommand* cmd,
     TaggedMirror* mirror, double* __restrict__ partials, unsigned int* __restrict__ counter, double* out,
-    double* out_second, unsigned long long* thr_word, int32_t* __restrict__ slot_of,
+    unsigned long long* thr_word, int32_t* __restrict__ slot_of,
     uint32_t* __restrict__ leaf_of) {
   extern __shared__ __align__(16) uint2 s_nodes[];
   __shared__ float s_rt[12];
@@ -1551,16 +1585,16 @@ __global__ void __launch_bounds__(kThreads, 3) icp_registration_kernel(
     for (int v = 0; v < 16; ++v) acc[v] = 0.f;
     if (kSlot && code == kRunResidual) {
       uint32_t n_keep = 0, n_pair = 0;
-      residual_chunks(pts, src, slot_of, n, s_rt, __int_as_float(0x7f800000), p, acc, n_keep, n_pair);
-      reduce_moments<true, true>(acc, n_keep, n_pair, partials, counter, out_second, seq, nullptr, 0u,
-                                 &mirror->t_cmd, thr_word);
+      residual_chunks<false>(pts, src, slot_of, n, s_rt, 0.f, p, acc, n_keep, n_pair);
+      reduce_moments<true, true, true>(acc, n_keep, n_pair, partials, counter, out, seq, nullptr, 0u,
+                                       nullptr, thr_word);
       if (threadIdx.x == 0) s_skip = await_threshold(thr_word, seq, p.wait_ns, &s_thr) ? 0u : kSkipTimedOut;
       __syncthreads();
       const unsigned int skipped = s_skip;
 #pragma unroll
       for (int v = 0; v < 16; ++v) acc[v] = 0.f;
       n_keep = n_pair = 0;
-      if (skipped == 0u) residual_chunks(pts, src, slot_of, n, s_rt, s_thr, p, acc, n_keep, n_pair);
+      if (skipped == 0u) residual_chunks<true>(pts, src, slot_of, n, s_rt, s_thr, p, acc, n_keep, n_pair);
       reduce_moments<true, true>(acc, n_keep, n_pair, partials, counter, out, seq + 1, nullptr, skipped,
                                  &mirror->t_cmd);
       if (skipped != 0u) return;
@@ -1724,9 +1758,8 @@ bool registration_kernel_fits(const icpnn_tree& t, int grid) {
 
 cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t n, const IcpPassParams& p,
                                 const TaggedCommand* cmd, TaggedMirror* mirror, double* partials,
-                                uint32_t* counter, double* out, double* out_second,
-                                unsigned long long* thr_word, int32_t* slot_of, uint32_t* leaf_of, int grid,
-                                cudaStream_t s) {
+                                uint32_t* counter, double* out, unsigned long long* thr_word,
+                                int32_t* slot_of, uint32_t* leaf_of, int grid, cudaStream_t s) {
   const int slots = smem_slots_for(t);
   const uint2* nodes = reinterpret_cast<const uint2*>(t.dev.nodes);
   const float4* boxes = reinterpret_cast<const float4*>(t.dev.boxes);
@@ -1745,7 +1778,7 @@ cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, nodes, boxes, pts, slots, src, n, p, cmd, mirror,
-                                           partials, counter, out, out_second, thr_word, slot_of, leaf_of);
+                                           partials, counter, out, thr_word, slot_of, leaf_of);
   if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1754,8 +1787,9 @@ cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const i
                                  int64_t n, const IcpPassParams& p, double* partials,
                                  uint32_t* counter, double* out, int grid, cudaStream_t s,
                                  const float* thr_in, float* thr_out) {
-  residual_pass_kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(t.dev.points), src,
-                                                 slot_of, n, p, partials, counter, out, thr_in, thr_out);
+  auto kernel = thr_out != nullptr ? residual_pass_kernel<true> : residual_pass_kernel<false>;
+  kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(t.dev.points), src, slot_of, n, p, partials,
+                                   counter, out, thr_in, thr_out);
   g_launch_count.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

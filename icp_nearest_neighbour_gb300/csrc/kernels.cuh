@@ -165,10 +165,10 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
 // and wait for the next command.  With slot_of (the residual rejection) the
 // correspondence passes record each record's matched slot, and a residual
 // command runs the iteration's two residual passes (see
-// launch_residual_pass) back to back: the first publishes in out_second with
-// seq and hands the 3-sigma threshold to the second through thr_word (a
-// device word, the pass's tag above the float's bits), the second publishes
-// in out with seq + 1.  A stop command (or a later sequence number) ends the
+// launch_residual_pass) back to back: the first hands the 3-sigma threshold
+// to the second through thr_word (a device word, the pass's tag above the
+// float's bits) and publishes nothing, the second publishes in out with
+// seq + 1.  A stop command (or a later sequence number) ends the
 // kernel; a block that gives up waiting reports the pass aborted and leaves.  The tree is read-only for the kernel's lifetime, so the L1 cache of
 // each SM keeps the part of it its queries touched in the previous pass; the
 // reduction takes an acquire fence only in the blocks that finish a level.
@@ -177,16 +177,18 @@ cudaError_t launch_icp_pass(const icpnn_tree& t, const float4* src, int64_t n,
 bool registration_kernel_fits(const icpnn_tree& t, int grid);
 cudaError_t launch_registration(const icpnn_tree& t, const float4* src, int64_t n, const IcpPassParams& p,
                                 const TaggedCommand* cmd, TaggedMirror* mirror, double* partials,
-                                uint32_t* counter, double* out, double* out_second,
-                                unsigned long long* thr_word, int32_t* slot_of, uint32_t* leaf_of, int grid,
-                                cudaStream_t s);
+                                uint32_t* counter, double* out, unsigned long long* thr_word,
+                                int32_t* slot_of, uint32_t* leaf_of, int grid, cudaStream_t s);
 
 // Residual pass of the residual rejection (same grid, partials, counter and
 // published result layout as the ICP pass): out[0] = pairs with
 // e2 <= threshold, out[1] = pairs with a match, out[2..16] = moments of the
 // kept pairs, out[17] = sum of e2 over all matched pairs.  The threshold is
-// p.max_d2, or *thr_in (device) when thr_in is given; with thr_out the pass
-// stores float_threshold(9 * out[17] / out[1]) there for the next pass.
+// p.max_d2, or *thr_in (device) when thr_in is given.  With thr_out the pass
+// reduces out[1] and out[17] only, stores float_threshold(9 * out[17] /
+// out[1]) at thr_out for the next pass and publishes nothing; the next pass's
+// out[1] and out[17] are then the same sums, bit for bit (same per-thread
+// sums, same reduction order).
 cudaError_t launch_residual_pass(const icpnn_tree& t, const float4* src, const int32_t* slot_of,
                                  int64_t n, const IcpPassParams& p, double* partials,
                                  uint32_t* counter, double* out, int grid, cudaStream_t s,

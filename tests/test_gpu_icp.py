@@ -380,9 +380,9 @@ def test_pass_command_wait_is_bounded(nn):
 
 
 def test_residual_and_prelaunched_registrations_alternate(nn):
-    """The residual passes publish in a second slot of the thread's mapped
-    buffer and the pre-launched passes read their commands from a third: a
-    registration of either kind leaves the other's region untouched."""
+    """Residual registrations and pre-launched ones share the thread's mapped
+    buffer (result slot, command regions): a registration of either kind
+    leaves nothing behind that changes the other's result."""
     c = W.tiny_case()
     t = nn.kdtree_build(c.target, c.leaf_size)
     nn.kdtree_upload(t)
