@@ -140,17 +140,17 @@ struct MappedBuffer {
 };
 thread_local MappedBuffer tl_mapped;
 // Layout, in doubles, each region on cache lines of its own:
-//   [0, kMomentSlots + 3]                      a pass's result, its publish word, its abort word
+//   [0, kAbortWord]                            a pass's result (tagged words) and its abort word
 //   [kCommandOffset, + sizeof(PassCommand))    the host-written command of pre-launched passes
 //   [kTaggedOffset, + sizeof(TaggedCommand))   the host-written commands of the persistent kernel
 //   [kBboxOffset, + 3)                         the source's box, copied from the device (Source)
-// A result slot holds the 18 moments, the publish word, the abort word and
-// (persistent kernel) the pass's start and end global times.
+// The result is kResultWords tagged words (the 18 moments as float-float
+// pairs, then the pass's start and publish times) and the abort word.
 constexpr int kCommandOffset = 64;
 constexpr int kTaggedOffset = 80;
 constexpr int kBboxOffset = 96;  // the source's box, six ordered integers, copied from the device
 constexpr int kMappedDoubles = 112;
-static_assert(kCommandOffset >= kMomentSlots + 4, "result slot: moments + 4 words");
+static_assert(kCommandOffset > kAbortWord, "result words and abort word before the command block");
 static_assert(kTaggedOffset * sizeof(double) >= kCommandOffset * sizeof(double) + sizeof(PassCommand) &&
                   kTaggedOffset * sizeof(double) + sizeof(TaggedCommand) <= kMappedDoubles * sizeof(double) &&
                   (kTaggedOffset * sizeof(double)) % 16 == 0,
@@ -385,43 +385,78 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
   return ICPNN_OK;
 }
 
+// Pass `seq`'s result is complete in the mapped words w: every word carries
+// the pass's tag (the device stores them with no fence, in any order).
+bool result_published(const volatile unsigned long long* w, unsigned long long seq) {
+  const uint32_t tag = result_tag(seq);
+  if (static_cast<uint32_t>(w[kResultWords - 1] >> 32) != tag) return false;
+  for (int i = 0; i < kResultWords - 1; ++i)
+    if (static_cast<uint32_t>(w[i] >> 32) != tag) return false;
+  return true;
+}
+
+const volatile unsigned long long* result_words(const MappedBuffer* mb) {
+  return reinterpret_cast<const volatile unsigned long long*>(mb->host);
+}
+
+// A complete published result: the slots as doubles (double(hi) + double(lo),
+// the device's own conversion) and, if asked, the pass's device time in ms
+// (command seen to publish; 0 when the pass did not record it).
+void decode_published(const volatile unsigned long long* w, double raw[kMomentSlots], float* ms = nullptr) {
+  for (int v = 0; v < kMomentSlots; ++v) {
+    const uint32_t a = static_cast<uint32_t>(w[2 * v]), b = static_cast<uint32_t>(w[2 * v + 1]);
+    float hi, lo;
+    std::memcpy(&hi, &a, sizeof(float));
+    std::memcpy(&lo, &b, sizeof(float));
+    raw[v] = static_cast<double>(hi) + static_cast<double>(lo);
+  }
+  if (ms != nullptr) {
+    const uint32_t t0 = static_cast<uint32_t>(w[2 * kMomentSlots]);
+    const uint32_t t1 = static_cast<uint32_t>(w[2 * kMomentSlots + 1]);
+    *ms = static_cast<float>(static_cast<double>(t1 - t0) * 1e-6);
+  }
+}
+
 // Wait until the pass with sequence number `seq` has published its result in
 // mapped memory, or -- for a pre-launched pass, with `aborted` given -- until
-// it is known to have given up waiting for its command.  `flag` is the
-// publish word; the abort word follows it.  A pass that gives up stores its
-// sequence number in the abort word, so a later pass that gives up too (the
-// one queued behind it, say, when launches are serialised or the host stalls)
-// cannot hide this pass's outcome: an abort word at or beyond `seq` means that
-// pass `seq` has finished, and the publish word then tells whether it
+// it is known to have given up waiting for its command.  A pass that gives up
+// stores its sequence number in the abort word, so a later pass that gives up
+// too (the one queued behind it, say, when launches are serialised or the
+// host stalls) cannot hide this pass's outcome: an abort word at or beyond
+// `seq` means that pass `seq` has finished, and its tags then tell whether it
 // published.  (`abort_from`, if given, is the first sequence number whose
 // abort also ends the wait: a residual command's two passes publish only the
 // second's result, and either may give up.)  Bounded: the stream is queried
 // every few thousand polls, so a failed or finished kernel ends the wait.
-int wait_published(const volatile unsigned long long* flag, unsigned long long seq, cudaStream_t s,
-                   bool* aborted = nullptr, unsigned long long abort_from = 0) {
-  const volatile unsigned long long* abort_word = flag + 1;
+int wait_published(const MappedBuffer* mb, unsigned long long seq, cudaStream_t s, bool* aborted = nullptr,
+                   unsigned long long abort_from = 0) {
+  const volatile unsigned long long* w = result_words(mb);
+  const volatile unsigned long long* abort_word = w + kAbortWord;
   if (abort_from == 0) abort_from = seq;
   for (uint64_t spins = 1;; ++spins) {
-    if (*flag == seq) return ICPNN_OK;
+    if (result_published(w, seq)) break;
     if (aborted != nullptr && *abort_word >= abort_from) {
       std::atomic_thread_fence(std::memory_order_acquire);
-      if (*flag == seq) return ICPNN_OK;
+      if (result_published(w, seq)) break;
       *aborted = true;
       return ICPNN_OK;
     }
     if ((spins & 4095u) == 0) {
       const cudaError_t e = cudaStreamQuery(s);
-      if (*flag == seq || (aborted != nullptr && *abort_word >= abort_from)) continue;
+      if (result_published(w, seq) || (aborted != nullptr && *abort_word >= abort_from)) continue;
       if (e == cudaSuccess) return fail(ICPNN_ERR_CUDA, "ICP pass finished without publishing its result");
       if (e != cudaErrorNotReady) return fail(ICPNN_ERR_CUDA, std::string("ICP pass: ") + cudaGetErrorString(e));
     }
   }
+  std::atomic_thread_fence(std::memory_order_acquire);
+  return ICPNN_OK;
 }
 
-void read_moments(const Pass& ps, icpnn_moments* m) {
-  std::atomic_thread_fence(std::memory_order_acquire);
+// The moments of the result that wait_published has just seen (and, if
+// asked, the pass's device time).
+void read_moments(const Pass& ps, icpnn_moments* m, float* ms = nullptr) {
   double raw[kMomentSlots];
-  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
+  decode_published(result_words(ps.mb), raw, ms);
   decode_moments(raw, ps.src.shift(), ps.shift_q, m);
 }
 
@@ -556,9 +591,7 @@ int pass_run(const Pass& ps, const float R[9], const float tr[3], int32_t* idx, 
   ICPNN_CUDA(launch_icp_pass(*ps.tree, ps.src.recs, ps.n, p, ps.partials, ps.counter, ps.mb->dev,
                              idx, d2, ps.slot_of, idx == nullptr ? ps.leaf_of : nullptr, ps.grid, s));
   if (ev1) ICPNN_CUDA(cudaEventRecord(ev1, s));
-  const volatile unsigned long long* flag =
-      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-  if (int rc = wait_published(flag, p.seq, s)) return rc;
+  if (int rc = wait_published(ps.mb, p.seq, s)) return rc;
   read_moments(ps, m);
   return ICPNN_OK;
 }
@@ -600,12 +633,9 @@ int residual_run(const Pass& ps, const float R[9], const float tr[3], cudaStream
   p.seq = seq_b;
   ICPNN_CUDA(launch_residual_pass(*ps.tree, ps.src.recs, ps.slot_of, ps.n, p, ps.partials, ps.counter,
                                   ps.mb->dev, ps.grid, s, ps.thr, nullptr));
-  const volatile unsigned long long* flag_b =
-      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-  if (int rc = wait_published(flag_b, seq_b, s)) return rc;
-  std::atomic_thread_fence(std::memory_order_acquire);
+  if (int rc = wait_published(ps.mb, seq_b, s)) return rc;
   double raw[kMomentSlots];
-  std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
+  decode_published(result_words(ps.mb), raw);
   const double pairs = raw[1];
   *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
   decode_moments(raw, ps.src.shift(), ps.shift_q, kept);
@@ -1049,10 +1079,8 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     if (more)
       if (int rc = pass_prelaunch(ps, s, ev0, ev1, &next.seq)) return rc;
     injected_collect_delay();
-    const volatile unsigned long long* flag =
-        reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
     bool aborted = false;
-    if (int rc = wait_published(flag, cur, s, &aborted)) return rc;
+    if (int rc = wait_published(ps.mb, cur, s, &aborted)) return rc;
     if (!aborted) {
       read_moments(ps, m);
       return ICPNN_OK;
@@ -1073,8 +1101,6 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
   // have left behind are cleared, and the pass and the rest of the
   // registration run as ordinary launches.  *pass_ms: the pass's device time
   // (command seen to result published), 0 after a fallback.
-  const volatile unsigned long long* flag0 =
-      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
   auto persistent_pass = [&](icpnn_moments* m, float* pass_ms) -> int {
     float R32[9], t32[3];
     transform_to_f32(T, R32, t32);
@@ -1082,11 +1108,9 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     tagged_command(ps.mb, seq, R32, t32);
     injected_collect_delay();
     bool aborted = false;
-    if (int rc = wait_published(flag0, seq, s, &aborted)) return rc;
+    if (int rc = wait_published(ps.mb, seq, s, &aborted)) return rc;
     if (!aborted) {
-      read_moments(ps, m);
-      const unsigned long long t0 = flag0[2], t1 = flag0[3];
-      *pass_ms = t1 > t0 ? static_cast<float>(static_cast<double>(t1 - t0) * 1e-6) : 0.f;
+      read_moments(ps, m, pass_ms);
       return ICPNN_OK;
     }
     run.stop();
@@ -1106,20 +1130,18 @@ int icpnn_icp_align(const icpnn_tree* t, const float* src, int64_t n_src, int32_
     // a kernel that gave up -- waiting for this command, or for the threshold
     // between the two passes -- records seq_a or seq_b in the abort word
     bool aborted = false;
-    if (int rc = wait_published(flag0, seq_b, s, &aborted, seq_a)) return rc;
+    if (int rc = wait_published(ps.mb, seq_b, s, &aborted, seq_a)) return rc;
     if (!aborted) {
-      std::atomic_thread_fence(std::memory_order_acquire);
       double raw[kMomentSlots];
-      std::memcpy(raw, const_cast<const double*>(ps.mb->host), sizeof(raw));
+      // the device time from the residual command's arrival to the second
+      // pass's publish
+      decode_published(result_words(ps.mb), raw, resid_ms);
       const double pairs = raw[1];
       *sigma2 = pairs > 0.0 ? raw[17] / pairs : 0.0;  // the device's threshold came from the same sums
       decode_moments(raw, ps.src.shift(), ps.shift_q, kept);
       kept->n_nonfinite = 0;
       kept->sum_d2 = 0.0;
       kept->mse = NAN;
-      // the residual command's arrival and the second pass's publish
-      const unsigned long long t0 = flag0[2], t1 = flag0[3];
-      *resid_ms = t1 > t0 ? static_cast<float>(static_cast<double>(t1 - t0) * 1e-6) : 0.f;
       return ICPNN_OK;
     }
     *resid_ms = 0.f;
@@ -1300,9 +1322,8 @@ int icpnn_probe_command_wait(const icpnn_tree* t, const float* src, int64_t n, u
     pass_command(ps, p.seq, R, tr);
   }
   ICPNN_CUDA(cudaStreamSynchronize(s));
-  const volatile unsigned long long* words =
-      reinterpret_cast<const volatile unsigned long long*>(ps.mb->host + kMomentSlots);
-  *outcome = words[0] == p.seq ? 2 : words[1] == p.seq ? 1 : 0;
+  const volatile unsigned long long* words = result_words(ps.mb);
+  *outcome = result_published(words, p.seq) ? 2 : words[kAbortWord] == p.seq ? 1 : 0;
   return ICPNN_OK;
 }
 

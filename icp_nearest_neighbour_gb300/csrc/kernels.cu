@@ -836,11 +836,11 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
 // Reduction of the per-thread moments of a pass, in a fixed order: warp
 // butterfly in float (lane 0's association order is the same every run),
 // warps of a block in order in double, then the last block to finish sums
-// the block partials in block order.  out[0] = c0, out[1] = c1 (counts),
-// out[2 + v] = acc[v].  With kPublish the last block then publishes `seq`
-// in the word after the result, once the result is visible system-wide; a
-// pass that gave up waiting for its command stores `seq` in the next word
-// instead (the abort word) and leaves the result and its word untouched.
+// the block partials in block order.  Slots: [0] = c0, [1] = c1 (counts),
+// [2 + v] = acc[v].  Without kPublish the last block stores them as doubles
+// at out; with kPublish it publishes them as tagged words (kResultWords), or,
+// in a pass that gave up waiting for its command, stores `seq` in the abort
+// word instead and leaves the result untouched.
 // The float threshold t with float(e2) <= t exactly when e2 <= limit in
 // double: the largest float not above limit (+inf stays +inf).
 __device__ __forceinline__ float float_threshold_dev(double limit) {
@@ -900,8 +900,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // then increments the counters with release atomics; only a block that finds
 // itself last takes the acquire fence.  The sums are the same in the same
 // order either way.  *t_start (if given) is the global time at which the pass
-// received its command; the last block stores it and the publish time in the
-// two words after the abort word.
+// received its command; the last block publishes its low 32 bits and those of
+// the publish time with the result.
 // Float-float sums (an unevaluated pair hi + lo of float32 values, about 44
 // significant bits): GB300's double-precision rate is a small fraction of its
 // float32 rate, and the final sum over every block's partial was the longest
@@ -927,8 +927,10 @@ struct ReduceShared {
   FF warp[kThreads / 32][kMomentSlots];
   FF fin[kThreads / kMomentSlots][kMomentSlots];
   FF rows[kRowGroups][kMomentSlots];
+  FF res[kMomentSlots];  // the final sums, published as float-float pairs
   double out[kMomentSlots];
-  bool last;
+  unsigned long long t_cmd;
+  bool last, publish;
 };
 __device__ __forceinline__ ReduceShared& reduce_shared() {
   __shared__ ReduceShared s;
@@ -1075,24 +1077,31 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     FF s{0.f, 0.f};
 #pragma unroll
     for (int g = 0; g < kRowGroups; ++g) s = ff_add(s, s_rows[g][threadIdx.x]);
+    sh.res[threadIdx.x] = s;
     s_out[threadIdx.x] = static_cast<double>(s.hi) + static_cast<double>(s.lo);
   }
   __syncthreads();
-  // One thread stores the result and, after one system-scope fence that
-  // orders its own stores, the sequence word: the host never sees the new
-  // sequence before the values.
+  unsigned long long* const out_words = reinterpret_cast<unsigned long long*>(out);
+  // Thread 0: the abort word of a pass that gave up, the residual threshold,
+  // the doubles of a device result; a published result then goes out as
+  // tagged words, one 16-byte store by each of the first 19 threads, with no
+  // fence (the host checks every word's tag).
   if (threadIdx.x == 0) {
+    bool publish = false;
     if (skips != 0u) {
       // The abort marker has a word of its own: the pass queued behind this
       // one may give up too, and its marker must not overwrite this pass's
       // outcome, nor this marker a predecessor's published result.
       if (kPublish && skips >= kSkipTimedOut) {
         __threadfence_system();
-        *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots + 1) = seq;
+        *reinterpret_cast<volatile unsigned long long*>(out_words + kAbortWord) = seq;
       }
-      return;
+    } else {
+      publish = kPublish && !kSigmaOnly;
+      sh.t_cmd = t_cmd;
     }
-    if (thr_out != nullptr || thr_word != nullptr) {
+    sh.publish = publish;
+    if (skips == 0u && (thr_out != nullptr || thr_word != nullptr)) {
       const double pairs = s_out[1];
       const double sigma2 = pairs > 0.0 ? s_out[17] / pairs : 0.0;
       const float thr = float_threshold_dev(9.0 * sigma2);
@@ -1106,17 +1115,26 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
                      "l"((static_cast<unsigned long long>(static_cast<uint32_t>(seq)) << 32) | __float_as_uint(thr))
                      : "memory");
     }
-    if (kSigmaOnly) return;
+    if (!kPublish && skips == 0u) {
 #pragma unroll
-    for (int v = 0; v < kMomentSlots; ++v) out[v] = s_out[v];
-    if (kPublish) {
-      if (t_start != nullptr) {
-        unsigned long long* tw = reinterpret_cast<unsigned long long*>(out + kMomentSlots + 2);
-        tw[0] = t_cmd;
-        tw[1] = global_ns();
+      for (int v = 0; v < kMomentSlots; ++v) out[v] = s_out[v];
+    }
+  }
+  if (kPublish && !kSigmaOnly) {
+    __syncthreads();
+    const int i = threadIdx.x;
+    if (sh.publish && i < kResultWords / 2) {
+      const unsigned long long tag = static_cast<unsigned long long>(result_tag(seq)) << 32;
+      uint32_t a, b;
+      if (i < kMomentSlots) {
+        a = __float_as_uint(sh.res[i].hi);
+        b = __float_as_uint(sh.res[i].lo);
+      } else {
+        a = static_cast<uint32_t>(sh.t_cmd);
+        b = t_start != nullptr ? static_cast<uint32_t>(global_ns()) : 0u;
       }
-      __threadfence_system();
-      *reinterpret_cast<volatile unsigned long long*>(out + kMomentSlots) = seq;
+      asm volatile("st.relaxed.sys.global.v2.u64 [%0], {%1, %2};" ::"l"(out_words + 2 * i), "l"(tag | a),
+                   "l"(tag | b) : "memory");
     }
   }
 }

@@ -19,6 +19,22 @@ constexpr int kSmemSlots = 4096;
 //   [8..16] sum (s - c_s)_a (q - c_q)_b at 8 + 3a + b, [17] sum d2.
 constexpr int kMomentSlots = 18;
 
+// Published result of a pass (`out` of launch_icp_pass and the persistent
+// kernel; may be host-mapped): kResultWords 64-bit words, each
+// (result_tag(seq) << 32) | payload.  Words 2v and 2v + 1 hold slot v as a
+// float-float pair (the float bits of hi, then of lo; the value is
+// double(hi) + double(lo)); words 36 and 37 the low 32 bits of the pass's
+// start and publish global times (0 when not recorded).  The words are
+// stored with no fence and in no particular order: a reader takes the
+// result once every word carries the pass's tag (an 8-byte aligned word is
+// written and read whole).  Word kAbortWord holds the sequence number of a
+// pass that gave up waiting for its command, stored after a system-scope
+// fence.
+constexpr int kResultWords = 2 * kMomentSlots + 2;
+constexpr int kAbortWord = kResultWords;
+// The top bit set: zeroed memory never carries a valid tag.
+__host__ __device__ constexpr uint32_t result_tag(unsigned long long seq) { return static_cast<uint32_t>(seq) | 0x80000000u; }
+
 // The moment reduction combines block partials in groups of kGroupBlocks
 // (one load per thread of a 256-thread block); its counter array holds
 // reduction_counter_words(grid) zeroed 32-bit words: [0] finished groups,
@@ -135,12 +151,10 @@ cudaError_t launch_nn(const icpnn_tree& t, const float4* queries, int64_t n, int
 
 // One fused ICP pass: transform, search, reject, reduce.  `partials` holds
 // grid * kMomentSlots doubles, `counter` reduction_counter_words(grid) zeroed
-// words (left zeroed), `out`
-// kMomentSlots doubles followed by two 64-bit words (may be host-mapped):
-// once the result is complete and visible system-wide the kernel stores p.seq
-// in the first (the publish word), so the host can poll it instead of
-// synchronising the stream; a pre-launched pass that gave up waiting for its
-// command stores p.seq in the second (the abort word) and nothing else.
+// words (left zeroed), `out` kAbortWord + 1 words (may be host-mapped): the
+// result, published as tagged words (see kResultWords) so that the host can
+// poll it instead of synchronising the stream; a pre-launched pass that gave
+// up waiting for its command stores p.seq in the abort word and nothing else.
 // Sequence numbers grow pass by pass, and a pass reaches its reduction only
 // after its predecessor on the stream has completed, so an abort word at or
 // beyond s proves that pass s has finished, published or not.
