@@ -364,7 +364,7 @@ int icpnn_icp_align_batch(const icpnn_tree* target, int32_t n_frames, const floa
  * call allocates or frees memory, host or device (the 18-double result is
  * copied into the caller's `out` through a stack buffer).
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for later calls.
  * Sharing: every call on a device uses the same array, and each call leaves
  * its contents behind (the counter that must start at zero is cleared at the
  * start of every call).  Calls that overlap on the GPU -- concurrent streams
