@@ -834,9 +834,9 @@ __global__ void __launch_bounds__(kThreads) nn_kernel(const uint2* __restrict__ 
 // ------------------------------------------------------------ ICP pass --
 
 // Reduction of the per-thread moments of a pass, in a fixed order: warp
-// butterfly in float (lane 0's association order is the same every run),
-// warps of a block in order in double, then the last block to finish sums
-// the block partials in block order.  Slots: [0] = c0, [1] = c1 (counts),
+// butterfly in float (lane 0's association order is the same every run), the
+// block's 8 warps in a float-float butterfly of 8 lanes, then the last block
+// to finish sums the block partials (see below).  Slots: [0] = c0, [1] = c1 (counts),
 // [2 + v] = acc[v].  Without kPublish the last block stores them as doubles
 // at out; with kPublish it publishes them as tagged words (kResultWords), or,
 // in a pass that gave up waiting for its command, stores `seq` in the abort
@@ -863,8 +863,10 @@ __device__ __forceinline__ float float_threshold_dev(double limit) {
 // Grids of up to kSingleLevelBlocks blocks (every grid of the search kernels:
 // at most three blocks per SM) reduce in one level: the last block to finish
 // (counter[0]) adds every block's partial: 252 threads, each taking two
-// slots of every 28th row, one 16-byte load per row and up to 14 loads in
-// flight (one round trip for a 391-block grid).  Partials and sums are
+// slots of every 28th row in row order, one 16-byte load per row and up to 14
+// loads in flight (one round trip for a 391-block grid); then 8 lanes per slot
+// add the 28 row groups, lane j groups j, j + 8, ... in order, and an 8-lane
+// butterfly adds the lanes (a 28-step chain before: 0.3 us longer).  Partials and sums are
 // float-float pairs (see ff_add): with doubles, the last block's 7,000
 // additions for a 391-block grid took 3.6-4.1 us of FP64 pipe, the longest
 // step of a pass's tail; as float-float they cost a fraction of that (scene
@@ -918,6 +920,21 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
   const float hi = __fadd_rn(s, e);
   return FF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
 }
+
+// Sum of s over each aligned group of 8 lanes, left in all 8 lanes: a
+// three-level butterfly (ff_add is commutative bit for bit: TwoSum's error
+// term is exact whichever operand comes first).
+__device__ __forceinline__ FF ff_allreduce8(FF s) {
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) {
+    const FF o{__shfl_xor_sync(kFull, s.hi, off), __shfl_xor_sync(kFull, s.lo, off)};
+    s = ff_add(s, o);
+  }
+  return s;
+}
+// Threads that take part in the 8-lane sums: 8 per slot, whole warps.
+constexpr int kTreeThreads = (kMomentSlots * 8 + 31) / 32 * 32;
+static_assert(kTreeThreads <= kThreads, "8 lanes per slot within the block");
 
 // Shared memory of reduce_moments, one instance per block whichever variants
 // of the reduction a kernel uses (a __shared__ array declared inside the
@@ -978,11 +995,14 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   // every thread of the block is past its search: a kernel launched as a
   // programmatic dependent of this one may start once all blocks are here
   if (!kPersistent) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x < kMomentSlots && wanted(threadIdx.x)) {
-    FF s{0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s = ff_add(s, s_warp[w][threadIdx.x]);
-    s_fin[0][threadIdx.x] = s;
+  // the block's warps: 8 lanes per slot, lane w holding warp w's value
+  static_assert(kThreads / 32 == 8, "one lane of an 8-lane group per warp");
+  if (threadIdx.x < kTreeThreads) {
+    const int v = threadIdx.x >> 3, w = threadIdx.x & 7;
+    const bool mine = v < kMomentSlots && wanted(v);
+    FF s = mine ? s_warp[w][v] : FF{0.f, 0.f};
+    s = ff_allreduce8(s);
+    if (w == 0 && mine) s_fin[0][v] = s;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1073,12 +1093,20 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     s_rows[g][2 * vp + 1] = s1;
   }
   __syncthreads();
-  if (threadIdx.x < kMomentSlots && wanted(threadIdx.x)) {
+  // the row groups: 8 lanes per slot, lane j adding groups j, j + 8, ... in
+  // order, then the 8 lanes' sums together
+  if (threadIdx.x < kTreeThreads) {
+    const int v = threadIdx.x >> 3, j = threadIdx.x & 7;
+    const bool mine = v < kMomentSlots && wanted(v);
     FF s{0.f, 0.f};
+    if (mine)
 #pragma unroll
-    for (int g = 0; g < kRowGroups; ++g) s = ff_add(s, s_rows[g][threadIdx.x]);
-    sh.res[threadIdx.x] = s;
-    s_out[threadIdx.x] = static_cast<double>(s.hi) + static_cast<double>(s.lo);
+      for (int g = j; g < kRowGroups; g += 8) s = ff_add(s, s_rows[g][v]);
+    s = ff_allreduce8(s);
+    if (j == 0 && mine) {
+      sh.res[v] = s;
+      s_out[v] = static_cast<double>(s.hi) + static_cast<double>(s.lo);
+    }
   }
   __syncthreads();
   unsigned long long* const out_words = reinterpret_cast<unsigned long long*>(out);
