@@ -944,8 +944,7 @@ struct ReduceShared {
   FF warp[kThreads / 32][kMomentSlots];
   FF fin[kThreads / kMomentSlots][kMomentSlots];
   FF rows[kRowGroups][kMomentSlots];
-  FF res[kMomentSlots];  // the final sums, published as float-float pairs
-  double out[kMomentSlots];
+  FF res[kMomentSlots];  // the final sums, as float-float pairs
   unsigned long long t_cmd;
   bool last, publish;
 };
@@ -971,7 +970,6 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
   ReduceShared& sh = reduce_shared();
   auto& s_warp = sh.warp;
   auto& s_fin = sh.fin;
-  auto& s_out = sh.out;
   bool& s_last = sh.last;
   float2* const pf = reinterpret_cast<float2*>(partials);
   // the slots this reduction produces
@@ -1103,10 +1101,7 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
 #pragma unroll
       for (int g = j; g < kRowGroups; g += 8) s = ff_add(s, s_rows[g][v]);
     s = ff_allreduce8(s);
-    if (j == 0 && mine) {
-      sh.res[v] = s;
-      s_out[v] = static_cast<double>(s.hi) + static_cast<double>(s.lo);
-    }
+    if (j == 0 && mine) sh.res[v] = s;
   }
   __syncthreads();
   unsigned long long* const out_words = reinterpret_cast<unsigned long long*>(out);
@@ -1130,8 +1125,10 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     }
     sh.publish = publish;
     if (skips == 0u && (thr_out != nullptr || thr_word != nullptr)) {
-      const double pairs = s_out[1];
-      const double sigma2 = pairs > 0.0 ? s_out[17] / pairs : 0.0;
+      // the slots as doubles, as the host converts them
+      const double pairs = static_cast<double>(sh.res[1].hi) + static_cast<double>(sh.res[1].lo);
+      const double sum_e2 = static_cast<double>(sh.res[17].hi) + static_cast<double>(sh.res[17].lo);
+      const double sigma2 = pairs > 0.0 ? sum_e2 / pairs : 0.0;
       const float thr = float_threshold_dev(9.0 * sigma2);
       if (thr_out != nullptr) *thr_out = thr;
       // release: the counters reset above are in place before any block that
@@ -1145,7 +1142,8 @@ __device__ __forceinline__ void reduce_moments(float (&acc)[16], uint32_t c0, ui
     }
     if (!kPublish && skips == 0u) {
 #pragma unroll
-      for (int v = 0; v < kMomentSlots; ++v) out[v] = s_out[v];
+      for (int v = 0; v < kMomentSlots; ++v)
+        out[v] = static_cast<double>(sh.res[v].hi) + static_cast<double>(sh.res[v].lo);
     }
   }
   if (kPublish && !kSigmaOnly) {
