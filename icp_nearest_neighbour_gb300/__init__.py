@@ -111,6 +111,7 @@ def load(build_if_missing: bool = False):
         "icpnn_probe_command_wait": ([P, P, i64, ctypes.c_uint64, i32, P, P], ctypes.c_int),
         "icpnn_probe_delay_commands": ([i32, i32, ctypes.c_uint64], ctypes.c_int),
         "icpnn_probe_delay_collect": ([i32, i32, ctypes.c_uint64], ctypes.c_int),
+        "icpnn_probe_read_result": ([P, i64, ctypes.c_uint64, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -254,6 +255,23 @@ def probe_delay_collect(skip: int, count: int, delay_ns: int):
     pre-launched pass's result (after `skip` normal ones) only after sleeping
     delay_ns, between queuing the successor pass and reading the result."""
     _check(load().icpnn_probe_delay_collect(int(skip), int(count), int(delay_ns)))
+
+
+RESULT_WORDS = 38  # 64-bit words of a pass's published result
+
+
+def probe_read_result(words, seq: int):
+    """Test helper: the host's reader of a pass's published result applied to
+    `words` (RESULT_WORDS uint64 on the host).  Returns (slots, pass_ms) once
+    every word carries pass `seq`'s tag, else None."""
+    w = np.ascontiguousarray(words, dtype=np.uint64)
+    slots = np.zeros(18, dtype=np.float64)
+    ms = ctypes.c_float(0.0)
+    complete = ctypes.c_int32(0)
+    _check(load().icpnn_probe_read_result(w.ctypes.data_as(ctypes.c_void_p), int(w.size), int(seq),
+                                          slots.ctypes.data_as(ctypes.c_void_p), ctypes.byref(ms),
+                                          ctypes.byref(complete)))
+    return (slots, float(ms.value)) if complete.value else None
 
 
 def kdtree_upload(tree: KDTree, stream=None):

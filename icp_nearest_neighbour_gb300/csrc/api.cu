@@ -1347,6 +1347,19 @@ int icpnn_probe_delay_collect(int32_t skip, int32_t count, uint64_t delay_ns) {
   return ICPNN_OK;
 }
 
+int icpnn_probe_read_result(const uint64_t* words, int64_t n_words, uint64_t seq, double* slots, float* pass_ms,
+                            int32_t* complete) {
+  clear_error();
+  if (words == nullptr || slots == nullptr || pass_ms == nullptr || complete == nullptr)
+    return fail(ICPNN_ERR_INVALID_ARG, "probe_read_result: NULL argument");
+  if (n_words != kResultWords)
+    return fail(ICPNN_ERR_INVALID_ARG, "probe_read_result: n_words must be " + std::to_string(kResultWords));
+  const volatile unsigned long long* w = reinterpret_cast<const volatile unsigned long long*>(words);
+  *complete = result_published(w, seq) ? 1 : 0;
+  if (*complete) decode_published(w, slots, pass_ms);
+  return ICPNN_OK;
+}
+
 const char* icpnn_last_error(void) { return tl_error.c_str(); }
 
 int64_t icpnn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }

@@ -41,6 +41,23 @@
  * The registration must still read pass k's outcome, then fall back to
  * ordinary launches.  count = 0 switches it off.
  * Errors: INVALID_ARG. */
+/* icpnn_probe_read_result -- the host's reader of a pass's published result,
+ * applied to caller-supplied words (no GPU needed).  A pass publishes its 18
+ * sums into mapped host memory as n_words = 38 64-bit words, each carrying in
+ * its high 32 bits the pass's tag (the low 32 bits of its sequence number
+ * with the top bit set) above a payload: words 2v and 2v + 1 the float bits
+ * of the hi and lo halves of sum v (value double(hi) + double(lo)), words 36
+ * and 37 the low 32 bits of the pass's start and publish global times in ns.
+ * The words reach the host in no particular order, so the reader takes the
+ * result only once every word carries pass `seq`'s tag.
+ *   words     host array of n_words words; only read.
+ *   n_words   38 (anything else is INVALID_ARG).
+ *   seq       the pass's sequence number.
+ *   slots     out: 18 doubles, written only when the result is complete.
+ *   pass_ms   out: (publish - start) mod 2^32 ns, in ms, written only when
+ *             complete.
+ *   complete  out: 1 if every word names pass seq, else 0.
+ * Errors: INVALID_ARG. */
 #ifndef ICPNN_PROBE_H
 #define ICPNN_PROBE_H
 
@@ -57,6 +74,8 @@ int icpnn_probe_command_wait(const struct icpnn_tree* tree, const float* src, in
                              int32_t mode, int32_t* outcome, void* stream);
 int icpnn_probe_delay_commands(int32_t skip, int32_t count, uint64_t delay_ns);
 int icpnn_probe_delay_collect(int32_t skip, int32_t count, uint64_t delay_ns);
+int icpnn_probe_read_result(const uint64_t* words, int64_t n_words, uint64_t seq, double* slots, float* pass_ms,
+                            int32_t* complete);
 
 #ifdef __cplusplus
 }
