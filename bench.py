@@ -326,8 +326,8 @@ def run_ours(args):
                              stream=stream)
             e2e_iters += r["iters"]
             h2d += tree_bytes + n * 12
-            # the source's box (24 B) and, per pass, 18 doubles + 2 words written to mapped memory
-            d2h += 24 + (r["iters"] + 1) * (18 * 8 + 16)
+            # the source's box (24 B) and, per pass, the result's tagged words written to mapped memory
+            d2h += 24 + (r["iters"] + 1) * nn.RESULT_WORDS * 8
             t_h.free()
         torch.cuda.synchronize()
         e2e_s = time.perf_counter() - e0
