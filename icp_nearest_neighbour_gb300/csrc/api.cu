@@ -386,7 +386,10 @@ int pass_setup(const icpnn_tree* t, const float* src, int64_t n, double dmax, bo
 }
 
 // Pass `seq`'s result is complete in the mapped words w: every word carries
-// the pass's tag (the device stores them with no fence, in any order).
+// the pass's tag (the device stores them with no fence, in any order).  A
+// pass that publishes rewrites all the words, so a word is at most one
+// published pass stale, and the tag's 31 bits of sequence number tell the two
+// apart however long the thread keeps registering.
 bool result_published(const volatile unsigned long long* w, unsigned long long seq) {
   const uint32_t tag = result_tag(seq);
   if (static_cast<uint32_t>(w[kResultWords - 1] >> 32) != tag) return false;
